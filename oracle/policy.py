@@ -1,0 +1,103 @@
+"""GrowPage's boundary policy in fp64: working sets, decision, kept set.
+
+Test infrastructure only (see the package docstring).
+
+Source: "GrowPage: On-Demand KV Budgeting for Efficient LLM Reasoning
+Serving", evolve.pub review, Summary -- at each PagedAttention capacity
+boundary the Top-p attention working-set sizes induced by the short and the
+long query summary are compared; a larger recent (short) working set
+allocates one more physical page, otherwise historical KV is compacted within
+the current allocation using the maximum of the two importance scores.  The
+review's FAQ section gives Top-p 0.99, demand threshold tau = 0 and a local
+retention quota of 64 tokens.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def softmax(u: np.ndarray) -> np.ndarray:
+    """softmax over the last axis in fp64 (max-shifted)."""
+    u = np.asarray(u, dtype=np.float64)
+    e = np.exp(u - u.max(axis=-1, keepdims=True))
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def topp_count(p: np.ndarray, top_p: float) -> int:
+    """Top-p working-set size of a probability vector.
+
+    W = min { k : sum of the k largest probabilities >= top_p * sum(p) }.
+    Reading: ">=" (the set reaches the mass), ties in value do not change W.
+    """
+    p = np.asarray(p, dtype=np.float64)
+    srt = np.sort(p)[::-1]
+    cs = np.cumsum(srt)
+    thr = float(top_p) * cs[-1]
+    return int(np.searchsorted(cs, thr, side="left")) + 1 if thr > 0 else 1
+
+
+def topp_range(p: np.ndarray, top_p: float, rel: float = 1e-5):
+    """(W at top_p*(1-rel), W at min(1, top_p*(1+rel))): the near-tie band."""
+    lo = topp_count(p, top_p * (1.0 - rel))
+    hi = topp_count(p, min(1.0, top_p * (1.0 + rel)))
+    return lo, hi
+
+
+def demand_delta(w_short, w_long) -> int:
+    """Delta = sum over (layer, kv head) of (W_short - W_long).
+
+    Reading: the pages say only that a larger recent working set triggers
+    growth; summing the per-head differences over all layers and kv heads
+    gives one signal per request, and any positive normalisation would give
+    the same sign at tau = 0.
+    """
+    return int(np.sum(np.asarray(w_short, dtype=np.int64) - np.asarray(w_long, dtype=np.int64)))
+
+
+def wants_grow(delta: int, tau: float) -> bool:
+    """Grow iff Delta > tau (strict: Delta == 0 compacts)."""
+    return float(delta) > float(tau)
+
+
+def importance(p_short: np.ndarray, p_long: np.ndarray) -> np.ndarray:
+    """Per-token importance: the maximum of the two summaries' probabilities."""
+    return np.maximum(np.asarray(p_short, np.float64), np.asarray(p_long, np.float64))
+
+
+def drop_set(imp: np.ndarray, pos: np.ndarray, n_drop: int) -> np.ndarray:
+    """Indices of the n_drop candidates ranked lowest by (importance, position).
+
+    Ascending importance; at equal importance the older (smaller position)
+    token goes first, i.e. the more recent one is kept.
+    """
+    order = np.lexsort((np.asarray(pos), np.asarray(imp)))
+    return order[:n_drop]
+
+
+def compaction_plan(imp_priv: np.ndarray, pos_priv: np.ndarray, pos_now: int,
+                    capacity: int, page_size: int, recent_window: int):
+    """Which private tokens a compaction drops, and the near-tie gap at the cut.
+
+    The request holds ``capacity`` private tokens (all its pages full).  It
+    keeps capacity - page_size of them, so that one page-worth of slots is
+    free within the same allocation: the most recent W = min(recent_window,
+    capacity - page_size) tokens always, plus the best of the older ones by
+    importance.  Returns (indices dropped, relative gap at the cut or inf).
+    """
+    n = len(pos_priv)
+    assert n == capacity
+    w_eff = min(recent_window, capacity - page_size)
+    keep_total = capacity - page_size
+    recent = pos_priv >= pos_now - w_eff
+    assert int(recent.sum()) == w_eff, (int(recent.sum()), w_eff)
+    cand = np.nonzero(~recent)[0]
+    n_drop = len(cand) - (keep_total - w_eff)
+    assert n_drop == page_size
+    order = np.lexsort((pos_priv[cand], imp_priv[cand]))
+    dropped = cand[order[:n_drop]]
+    gap = np.inf
+    if len(cand) > n_drop and n_drop > 0:
+        a = imp_priv[cand[order[n_drop - 1]]]   # largest dropped
+        b = imp_priv[cand[order[n_drop]]]       # smallest kept
+        gap = abs(b - a) / max(b, 1e-300)
+    return dropped, gap
