@@ -1,0 +1,480 @@
+// gp_host.cu -- the C ABI (include/growpage.h): validation, layout of the
+// caller's buffer, host-side bookkeeping and kernel launches.
+//
+// The library never allocates device memory: every region, scratch included,
+// lives in the buffer the caller passes to gp_create_pool.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "gp_internal.cuh"
+
+namespace gp {
+cudaError_t launch_attention(const PoolDev& p, int layer, const void* q, const void* k,
+                             const void* v, void* out, int grid, cudaStream_t st);
+cudaError_t attention_occupancy(const PoolDev& p, int* blocks);
+cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, cudaStream_t st);
+cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st);
+cudaError_t launch_decide(const PoolDev& p, cudaStream_t st);
+cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st);
+cudaError_t launch_init(const PoolDev& p, cudaStream_t st);
+cudaError_t launch_pop_pages(const PoolDev& p, int32_t* dst, int count, cudaStream_t st);
+cudaError_t launch_prefix_meta(const PoolDev& p, int pid, int npages, int len, cudaStream_t st);
+cudaError_t launch_admit(const PoolDev& p, int slot, int budget, int prefix_id, int prompt_len,
+                         cudaStream_t st);
+cudaError_t launch_write_tokens(const PoolDev& p, const int32_t* pages, const void* k,
+                                const void* v, int count, int pos0, cudaStream_t st);
+cudaError_t launch_free(const PoolDev& p, int slot, cudaStream_t st);
+cudaError_t launch_release_prefix(const PoolDev& p, int pid, cudaStream_t st);
+}  // namespace gp
+
+struct gp_pool {
+  gp_config cfg;
+  gp::PoolDev dev;
+  gp_layout lay;
+  uint8_t* base = nullptr;
+  cudaStream_t stream = nullptr;
+  std::string err;
+  int next_layer = 0;
+  int step_n = -1;
+  const int32_t* step_slots = nullptr;
+  int attn_grid = 0, select_grid = 0, commit_grid = 0;
+  int64_t launches = 0;
+  std::vector<char> slot_active;
+  std::vector<int> slot_prefix;
+  std::vector<int> prefix_refs;  // host mirror of the device reference counts
+  std::vector<char> prefix_held;
+  std::vector<int> prefix_len;
+};
+
+namespace {
+
+constexpr uint64_t kAlign = 256;
+
+uint64_t align_up(uint64_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int fail(gp_pool* p, int code, const std::string& msg) {
+  if (p) p->err = msg;
+  return code;
+}
+
+int cuda_fail(gp_pool* p, cudaError_t e, const char* what) {
+  return fail(p, GP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+const char* check_config(const gp_config* c) {
+  if (!c) return "null config";
+  if (c->num_layers < 1 || c->num_q_heads < 1 || c->num_kv_heads < 1) return "bad head/layer counts";
+  if (c->num_q_heads % c->num_kv_heads) return "num_q_heads must be a multiple of num_kv_heads";
+  const int G = c->num_q_heads / c->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return "G = Hq/Hk must be 1, 2 or 4";
+  if (c->dtype != GP_DTYPE_F32 && c->dtype != GP_DTYPE_BF16) return "unknown dtype";
+  if (!((c->head_dim == 64 && c->dtype == GP_DTYPE_F32) || c->head_dim == 128))
+    return "head_dim must be 128, or 64 with fp32 storage";
+  if (c->page_size < 16 || c->page_size % 16 || c->page_size > 256)
+    return "page_size must be a multiple of 16, at most 256";
+  if (c->num_pages < 1 || c->max_requests < 1 || c->max_pages_per_req < 1) return "bad pool sizes";
+  if (c->max_prefixes < 0 || c->max_prefix_len < 0 || c->max_prefix_len % c->page_size)
+    return "max_prefix_len must be a non-negative multiple of page_size";
+  if (c->max_seq_len < 1) return "bad max_seq_len";
+  if (c->mode != GP_MODE_GROWPAGE && c->mode != GP_MODE_FULL_KV) return "unknown mode";
+  if (c->recent_window < 0) return "recent_window < 0";
+  if (!(c->beta_s >= 0.f && c->beta_s < 1.f && c->beta_l >= 0.f && c->beta_l < 1.f))
+    return "betas must be in [0, 1)";
+  if (!(c->top_p > 0.f && c->top_p <= 1.f)) return "top_p must be in (0, 1]";
+  if (!(c->rope_theta >= 0.0)) return "rope_theta < 0";
+  if (c->flags != 0) return "flags must be 0";
+  const long long logit_w = (long long)c->max_prefix_len + (long long)c->max_pages_per_req * c->page_size;
+  if (logit_w > (1ll << 30)) return "max_pages_per_req too large";
+  return nullptr;
+}
+
+void compute_layout(const gp_config* c, gp_layout* l) {
+  const uint64_t eb = c->dtype == GP_DTYPE_BF16 ? 2 : 4;
+  const uint64_t L = c->num_layers, Hk = c->num_kv_heads, D = c->head_dim, P = c->page_size;
+  const uint64_t G = c->num_q_heads / c->num_kv_heads;
+  const uint64_t R = c->max_requests;
+  std::memset(l, 0, sizeof(*l));
+  l->max_prefix_pages = c->max_prefix_len / c->page_size;
+  l->block_width = l->max_prefix_pages + c->max_pages_per_req;
+  l->logit_width = c->max_prefix_len + c->max_pages_per_req * c->page_size;
+  l->page_bytes = L * Hk * 2 * P * D * eb;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) { uint64_t o = off; off = align_up(off + bytes); return o; };
+  l->kv = take((uint64_t)c->num_pages * l->page_bytes);
+  l->tok_pos = take((uint64_t)c->num_pages * L * Hk * P * 4);
+  l->block = take(R * (uint64_t)l->block_width * 4);
+  l->req = take(R * sizeof(gp_req_meta));
+  l->summary = take(R * L * Hk * 2 * D * 4);
+  l->staging = take(R * L * Hk * 2 * D * eb);
+  l->logits = take(c->mode == GP_MODE_GROWPAGE ? R * L * Hk * 2 * (uint64_t)l->logit_width * 4 : 0);
+  l->wset = take(R * L * Hk * 2 * 4);
+  l->free_stack = take((uint64_t)c->num_pages * 4);
+  l->ctrl = take(sizeof(gp_ctrl));
+  l->prefix = take((uint64_t)c->max_prefixes * sizeof(gp_prefix_meta));
+  l->prefix_pages = take((uint64_t)c->max_prefixes * l->max_prefix_pages * 4);
+  l->rope = take((uint64_t)c->max_seq_len * (D / 2) * (8 + 8 + 4 + 4));
+  l->scratch = off;
+  for (int k = 0; k < 10; ++k) take((R + 1) * 4);             // plan arrays
+  take(R * 8);                                                 // plan_delta
+  take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 2) * 4);  // partials
+  take(R * Hk * 4);                                            // seg_count
+  take(R * L * Hk * P * 2 * 4);                                // moves
+  take(R * L * Hk * 4);                                        // moves_n
+  l->total = off;
+}
+
+void fill_dev(gp_pool* p) {
+  const gp_config& c = p->cfg;
+  const gp_layout& l = p->lay;
+  gp::PoolDev& d = p->dev;
+  std::memset(&d, 0, sizeof(d));
+  d.L = c.num_layers; d.Hq = c.num_q_heads; d.Hk = c.num_kv_heads; d.D = c.head_dim;
+  d.G = c.num_q_heads / c.num_kv_heads; d.P = c.page_size;
+  d.num_pages = c.num_pages; d.max_req = c.max_requests; d.max_pages_per_req = c.max_pages_per_req;
+  d.max_prefixes = c.max_prefixes; d.max_prefix_pages = l.max_prefix_pages;
+  d.block_width = l.block_width; d.logit_width = l.logit_width; d.max_seq_len = c.max_seq_len;
+  d.dtype = c.dtype; d.mode = c.mode; d.recent_window = c.recent_window;
+  d.beta_s = c.beta_s; d.beta_l = c.beta_l; d.top_p = c.top_p; d.tau = c.tau;
+  d.rope = c.rope_theta != 0.0 ? 1 : 0;
+  d.elem_bytes = c.dtype == GP_DTYPE_BF16 ? 2 : 4;
+  d.half_bytes = (uint64_t)c.page_size * c.head_dim * d.elem_bytes;
+  d.head_bytes = 2 * d.half_bytes;
+  d.layer_bytes = (uint64_t)c.num_kv_heads * d.head_bytes;
+  d.page_bytes = l.page_bytes;
+  uint8_t* b = p->base;
+  d.kv = b + l.kv;
+  d.tok_pos = (int32_t*)(b + l.tok_pos);
+  d.block = (int32_t*)(b + l.block);
+  d.req = (gp_req_meta*)(b + l.req);
+  d.summary = (float*)(b + l.summary);
+  d.staging = b + l.staging;
+  d.logits = (float*)(b + l.logits);
+  d.wset = (int32_t*)(b + l.wset);
+  d.free_stack = (int32_t*)(b + l.free_stack);
+  d.ctrl = (gp_ctrl*)(b + l.ctrl);
+  d.prefix = (gp_prefix_meta*)(b + l.prefix);
+  d.prefix_pages = (int32_t*)(b + l.prefix_pages);
+  const uint64_t tab = (uint64_t)c.max_seq_len * (c.head_dim / 2);
+  d.cos64 = (const double*)(b + l.rope);
+  d.sin64 = d.cos64 + tab;
+  d.cos32 = (const float*)(d.sin64 + tab);
+  d.sin32 = d.cos32 + tab;
+  const uint64_t R = c.max_requests;
+  uint64_t off = l.scratch;
+  auto take = [&](uint64_t bytes) { uint64_t o = off; off = align_up(off + bytes); return b + o; };
+  d.plan_slot = (int32_t*)take((R + 1) * 4);
+  d.plan_R = (int32_t*)take((R + 1) * 4);
+  d.plan_nb = (int32_t*)take((R + 1) * 4);
+  d.plan_cum = (int32_t*)take((R + 1) * 4);
+  d.plan_flags = (int32_t*)take((R + 1) * 4);
+  d.plan_commit = (int32_t*)take((R + 1) * 4);
+  d.plan_cpos = (int32_t*)take((R + 1) * 4);
+  d.plan_dec = (int32_t*)take((R + 1) * 4);
+  d.plan_bnd = (int32_t*)take((R + 1) * 4);
+  d.plan_misc = (int32_t*)take((R + 1) * 4);
+  d.plan_delta = (long long*)take(R * 8);
+  d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 2) * 4);
+  d.seg_count = (int32_t*)take(R * c.num_kv_heads * 4);
+  d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 2 * 4);
+  d.moves_n = (int32_t*)take(R * c.num_layers * c.num_kv_heads * 4);
+}
+
+int sync_status(gp_pool* p) {
+  cudaError_t e = cudaStreamSynchronize(p->stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "cudaStreamSynchronize");
+  uint32_t st[2] = {0, 0};
+  e = cudaMemcpy(st, &p->dev.ctrl->status, 8, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(p, e, "read status");
+  if (st[0]) {
+    char buf[200];
+    std::snprintf(buf, sizeof(buf), "device status 0x%x (info %d):%s%s%s%s%s%s", st[0], (int)st[1],
+                  (st[0] & GP_ST_BAD_SLOTS) ? " bad-slot-list" : "",
+                  (st[0] & GP_ST_BAD_PAGE) ? " page-out-of-range" : "",
+                  (st[0] & GP_ST_TIMEOUT) ? " wait-timeout" : "",
+                  (st[0] & GP_ST_STARVED) ? " full-kv-starved" : "",
+                  (st[0] & GP_ST_BAD_PLAN) ? " bad-plan" : "",
+                  (st[0] & GP_ST_POS_RANGE) ? " position-beyond-max_seq_len" : "");
+    return fail(p, GP_ERR_DEVICE, buf);
+  }
+  return GP_OK;
+}
+
+int read_free_top(gp_pool* p, int* out) {
+  cudaError_t e = cudaMemcpyAsync(out, &p->dev.ctrl->free_top, 4, cudaMemcpyDeviceToHost, p->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+  if (e != cudaSuccess) return cuda_fail(p, e, "read free_top");
+  return GP_OK;
+}
+
+#define GP_LAUNCH(pool, expr)                                   \
+  do {                                                          \
+    cudaError_t _e = (expr);                                    \
+    if (_e != cudaSuccess) return cuda_fail(pool, _e, #expr);   \
+    (pool)->launches += 1;                                      \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+int gp_pool_bytes(const gp_config* cfg, size_t* bytes) {
+  if (!bytes) return GP_ERR_INVALID;
+  if (check_config(cfg)) return GP_ERR_INVALID;
+  gp_layout l;
+  compute_layout(cfg, &l);
+  *bytes = (size_t)l.total;
+  return GP_OK;
+}
+
+int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stream, gp_pool** out) {
+  if (!out || !cfg) return GP_ERR_INVALID;
+  *out = nullptr;
+  if (check_config(cfg)) return GP_ERR_INVALID;
+  gp_layout l;
+  compute_layout(cfg, &l);
+  if (!dev_buf || bytes < l.total || ((uintptr_t)dev_buf % kAlign)) return GP_ERR_INVALID;
+  gp_pool* p = new gp_pool();
+  p->cfg = *cfg;
+  p->lay = l;
+  p->base = (uint8_t*)dev_buf;
+  p->stream = (cudaStream_t)stream;
+  p->slot_active.assign(cfg->max_requests, 0);
+  p->slot_prefix.assign(cfg->max_requests, -1);
+  p->prefix_refs.assign(cfg->max_prefixes, 0);
+  p->prefix_held.assign(cfg->max_prefixes, 0);
+  p->prefix_len.assign(cfg->max_prefixes, 0);
+  fill_dev(p);
+  auto bail = [&](int code) { delete p; return code; };
+  cudaError_t e = cudaMemsetAsync(dev_buf, 0, l.total, p->stream);
+  if (e != cudaSuccess) return bail(GP_ERR_CUDA);
+  if (cfg->rope_theta != 0.0) {
+    // fp64 table from the C library (pow, cos, sin); fp32 copies rounded once
+    const int H = cfg->head_dim / 2;
+    const size_t tab = (size_t)cfg->max_seq_len * H;
+    std::vector<double> c64(tab), s64(tab);
+    std::vector<float> c32(tab), s32(tab);
+    std::vector<double> inv(H);
+    for (int i = 0; i < H; ++i) inv[i] = std::pow(cfg->rope_theta, -(2.0 * i) / cfg->head_dim);
+    for (int pos = 0; pos < cfg->max_seq_len; ++pos)
+      for (int i = 0; i < H; ++i) {
+        const double a = (double)pos * inv[i];
+        const size_t k = (size_t)pos * H + i;
+        c64[k] = std::cos(a);
+        s64[k] = std::sin(a);
+        c32[k] = (float)c64[k];
+        s32[k] = (float)s64[k];
+      }
+    const gp::PoolDev& d = p->dev;
+    e = cudaMemcpyAsync((void*)d.cos64, c64.data(), tab * 8, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin64, s64.data(), tab * 8, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.cos32, c32.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin32, s32.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
+    if (e != cudaSuccess) return bail(GP_ERR_CUDA);
+  }
+  e = gp::launch_init(p->dev, p->stream);
+  if (e != cudaSuccess) return bail(GP_ERR_CUDA);
+  p->launches += 1;
+  int dev = 0, sms = 0, blocks = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = gp::attention_occupancy(p->dev, &blocks);
+  if (e != cudaSuccess || sms <= 0 || blocks <= 0) return bail(GP_ERR_CUDA);
+  int grid = sms * blocks;
+  if (grid * gp::kAttnWarps > gp::kMaxWorkersBound) grid = gp::kMaxWorkersBound / gp::kAttnWarps;
+  p->attn_grid = grid;
+  p->dev.num_workers = grid * gp::kAttnWarps;
+  p->select_grid = sms * 4;
+  p->commit_grid = sms * 4;
+  e = cudaStreamSynchronize(p->stream);
+  if (e != cudaSuccess) return bail(GP_ERR_CUDA);
+  *out = p;
+  return GP_OK;
+}
+
+int gp_destroy_pool(gp_pool* pool) {
+  if (!pool) return GP_ERR_INVALID;
+  delete pool;
+  return GP_OK;
+}
+
+int gp_set_stream(gp_pool* pool, void* stream) {
+  if (!pool) return GP_ERR_INVALID;
+  pool->stream = (cudaStream_t)stream;
+  return GP_OK;
+}
+
+int gp_get_layout(const gp_pool* pool, gp_layout* out) {
+  if (!pool || !out) return GP_ERR_INVALID;
+  *out = pool->lay;
+  out->num_workers = pool->dev.num_workers;
+  return GP_OK;
+}
+
+int gp_add_prefix(gp_pool* pool, const void* k_prefix, const void* v_prefix, int32_t len,
+                  int32_t* prefix_id) {
+  if (!pool || !prefix_id) return GP_ERR_INVALID;
+  const gp_config& c = pool->cfg;
+  if (pool->next_layer != 0) return fail(pool, GP_ERR_INVALID, "add_prefix inside a step");
+  if (len <= 0 || len % c.page_size || len > c.max_prefix_len || !k_prefix || !v_prefix)
+    return fail(pool, GP_ERR_INVALID, "prefix length must be a positive multiple of page_size <= max_prefix_len");
+  if (len >= c.max_seq_len) return fail(pool, GP_ERR_INVALID, "prefix beyond max_seq_len");
+  int pid = -1;
+  for (int k = 0; k < c.max_prefixes; ++k)
+    if (pool->prefix_refs[k] == 0) { pid = k; break; }
+  if (pid < 0) return fail(pool, GP_ERR_INVALID, "no free prefix slot");
+  const int npages = len / c.page_size;
+  int free_top = 0;
+  int rc = read_free_top(pool, &free_top);
+  if (rc) return rc;
+  if (free_top < npages) return fail(pool, GP_ERR_NO_PAGES, "not enough free pages for the prefix");
+  int32_t* row = pool->dev.prefix_pages + (size_t)pid * pool->lay.max_prefix_pages;
+  GP_LAUNCH(pool, gp::launch_pop_pages(pool->dev, row, npages, pool->stream));
+  GP_LAUNCH(pool, gp::launch_prefix_meta(pool->dev, pid, npages, len, pool->stream));
+  GP_LAUNCH(pool, gp::launch_write_tokens(pool->dev, row, k_prefix, v_prefix, len, 0, pool->stream));
+  rc = sync_status(pool);
+  if (rc) return rc;
+  pool->prefix_refs[pid] = 1;
+  pool->prefix_held[pid] = 1;
+  pool->prefix_len[pid] = len;
+  *prefix_id = pid;
+  return GP_OK;
+}
+
+int gp_release_prefix(gp_pool* pool, int32_t prefix_id) {
+  if (!pool) return GP_ERR_INVALID;
+  if (prefix_id < 0 || prefix_id >= pool->cfg.max_prefixes || !pool->prefix_held[prefix_id])
+    return fail(pool, GP_ERR_INVALID, "prefix not held");
+  GP_LAUNCH(pool, gp::launch_release_prefix(pool->dev, prefix_id, pool->stream));
+  pool->prefix_held[prefix_id] = 0;
+  pool->prefix_refs[prefix_id] -= 1;
+  return GP_OK;
+}
+
+int gp_add_request(gp_pool* pool, int32_t slot, const void* k_prompt, const void* v_prompt,
+                   int32_t prompt_len, int32_t budget_pages, int32_t prefix_id) {
+  if (!pool) return GP_ERR_INVALID;
+  const gp_config& c = pool->cfg;
+  if (pool->next_layer != 0) return fail(pool, GP_ERR_INVALID, "add_request inside a step");
+  if (slot < 0 || slot >= c.max_requests || pool->slot_active[slot])
+    return fail(pool, GP_ERR_INVALID, "slot out of range or in use");
+  if (budget_pages < 1 || budget_pages > c.max_pages_per_req)
+    return fail(pool, GP_ERR_INVALID, "budget_pages out of range");
+  if (prompt_len < 0 || prompt_len > budget_pages * c.page_size)
+    return fail(pool, GP_ERR_INVALID, "prompt does not fit the budget");
+  if (prompt_len > 0 && (!k_prompt || !v_prompt)) return fail(pool, GP_ERR_INVALID, "null prompt");
+  int plen = 0;
+  if (prefix_id >= 0) {
+    if (prefix_id >= c.max_prefixes || pool->prefix_refs[prefix_id] <= 0)
+      return fail(pool, GP_ERR_INVALID, "unknown prefix");
+    plen = pool->prefix_len[prefix_id];
+  } else if (prefix_id != -1) {
+    return fail(pool, GP_ERR_INVALID, "bad prefix id");
+  }
+  if ((long long)plen + prompt_len >= c.max_seq_len)
+    return fail(pool, GP_ERR_INVALID, "position beyond max_seq_len");
+  int free_top = 0;
+  int rc = read_free_top(pool, &free_top);
+  if (rc) return rc;
+  if (free_top < budget_pages) return fail(pool, GP_ERR_NO_PAGES, "not enough free pages for the budget");
+  GP_LAUNCH(pool, gp::launch_admit(pool->dev, slot, budget_pages, prefix_id, prompt_len, pool->stream));
+  const int npre = prefix_id >= 0 ? plen / c.page_size : 0;
+  const int32_t* row = pool->dev.block + (size_t)slot * pool->lay.block_width + npre;
+  if (prompt_len > 0)
+    GP_LAUNCH(pool, gp::launch_write_tokens(pool->dev, row, k_prompt, v_prompt, prompt_len, plen,
+                                            pool->stream));
+  rc = sync_status(pool);
+  if (rc) return rc;
+  pool->slot_active[slot] = 1;
+  pool->slot_prefix[slot] = prefix_id;
+  if (prefix_id >= 0) pool->prefix_refs[prefix_id] += 1;
+  return GP_OK;
+}
+
+int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots_dev,
+                   const void* q, const void* k_new, const void* v_new, void* out) {
+  if (!pool) return GP_ERR_INVALID;
+  const gp_config& c = pool->cfg;
+  if (layer != pool->next_layer || layer >= c.num_layers)
+    return fail(pool, GP_ERR_INVALID, "layers must be called 0..L-1, then gp_boundary");
+  if (n < 0 || n > c.max_requests) return fail(pool, GP_ERR_INVALID, "n out of range");
+  if (n > 0 && (!slots_dev || !q || !k_new || !v_new || !out))
+    return fail(pool, GP_ERR_INVALID, "null tensor");
+  if (layer == 0) {
+    GP_LAUNCH(pool, gp::launch_plan(pool->dev, n, slots_dev, pool->stream));
+    pool->step_n = n;
+    pool->step_slots = slots_dev;
+  } else if (n != pool->step_n || slots_dev != pool->step_slots) {
+    return fail(pool, GP_ERR_INVALID, "every layer of a step must get the same slot list");
+  }
+  if (n > 0)
+    GP_LAUNCH(pool, gp::launch_attention(pool->dev, layer, q, k_new, v_new, out, pool->attn_grid,
+                                         pool->stream));
+  pool->next_layer = layer + 1;
+  return GP_OK;
+}
+
+int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev) {
+  if (!pool) return GP_ERR_INVALID;
+  if (pool->next_layer != pool->cfg.num_layers)
+    return fail(pool, GP_ERR_INVALID, "gp_boundary before all layers of the step");
+  if (n != pool->step_n || slots_dev != pool->step_slots)
+    return fail(pool, GP_ERR_INVALID, "gp_boundary must get the step's slot list");
+  pool->next_layer = 0;
+  if (n == 0) return GP_OK;
+  if (pool->cfg.mode == GP_MODE_GROWPAGE)
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, pool->stream));
+  GP_LAUNCH(pool, gp::launch_decide(pool->dev, pool->stream));
+  GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, pool->stream));
+  return GP_OK;
+}
+
+int gp_free(gp_pool* pool, int32_t slot) {
+  if (!pool) return GP_ERR_INVALID;
+  if (pool->next_layer != 0) return fail(pool, GP_ERR_INVALID, "free inside a step");
+  if (slot < 0 || slot >= pool->cfg.max_requests || !pool->slot_active[slot])
+    return fail(pool, GP_ERR_INVALID, "slot not active");
+  GP_LAUNCH(pool, gp::launch_free(pool->dev, slot, pool->stream));
+  pool->slot_active[slot] = 0;
+  const int pid = pool->slot_prefix[slot];
+  if (pid >= 0) pool->prefix_refs[pid] -= 1;
+  pool->slot_prefix[slot] = -1;
+  return GP_OK;
+}
+
+int gp_sync(gp_pool* pool) {
+  if (!pool) return GP_ERR_INVALID;
+  return sync_status(pool);
+}
+
+int gp_get_stats(gp_pool* pool, gp_ctrl* out) {
+  if (!pool || !out) return GP_ERR_INVALID;
+  cudaError_t e = cudaStreamSynchronize(pool->stream);
+  if (e == cudaSuccess) e = cudaMemcpy(out, pool->dev.ctrl, sizeof(gp_ctrl), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(pool, e, "gp_get_stats");
+  return GP_OK;
+}
+
+int gp_get_request(gp_pool* pool, int32_t slot, gp_req_meta* meta, int32_t* block_table, int32_t cap) {
+  if (!pool || !meta || slot < 0 || slot >= pool->cfg.max_requests || cap < 0)
+    return GP_ERR_INVALID;
+  cudaError_t e = cudaStreamSynchronize(pool->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(meta, pool->dev.req + slot, sizeof(gp_req_meta), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && block_table && cap > 0) {
+    const int w = cap < pool->lay.block_width ? cap : pool->lay.block_width;
+    e = cudaMemcpy(block_table, pool->dev.block + (size_t)slot * pool->lay.block_width, (size_t)w * 4,
+                   cudaMemcpyDeviceToHost);
+  }
+  if (e != cudaSuccess) return cuda_fail(pool, e, "gp_get_request");
+  return GP_OK;
+}
+
+const char* gp_last_error(const gp_pool* pool) { return pool ? pool->err.c_str() : "null pool"; }
+
+int64_t gp_launch_count(const gp_pool* pool) { return pool ? pool->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,194 @@
+// gp_internal.cuh -- device-side view of a GrowPage pool and shared helpers.
+//
+// Everything here is private to libgrowpage.so.  The public contract is
+// include/growpage.h; this file mirrors its structs and adds the scratch
+// regions (per-step plan, split partials, move lists) the kernels use.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "growpage.h"
+
+namespace gp {
+
+constexpr int kBlockTok = 16;     // tokens per attention block (one bulk-copy unit)
+constexpr int kAttnWarps = 4;     // warps per attention CTA (independent workers)
+constexpr int kMaxWorkersBound = 160 * 8 * kAttnWarps;  // sizing bound
+
+enum Decision : int32_t { kNone = 0, kGrow = 1, kCompact = 2, kCompactDenied = 3, kStarved = 4 };
+
+// Flags of a request in the current step's plan.
+constexpr int32_t kPlanBoundary = 1;  // all private pages full at step start
+constexpr int32_t kPlanFirst = 2;     // first decode step: summaries start at qbar
+constexpr int32_t kPlanScore = 4;     // boundary in GROWPAGE mode: score summaries
+
+struct PoolDev {
+  // configuration
+  int32_t L, Hq, Hk, D, G, P;
+  int32_t num_pages, max_req, max_pages_per_req, max_prefixes, max_prefix_pages;
+  int32_t block_width, logit_width, max_seq_len, dtype, mode, recent_window;
+  int32_t num_workers;
+  float beta_s, beta_l, top_p, tau;
+  int32_t rope;  // 1: rotary embedding on
+  int32_t elem_bytes;
+  uint64_t page_bytes, layer_bytes, head_bytes, half_bytes;  // kv strides
+  // public regions
+  uint8_t* kv;
+  int32_t* tok_pos;
+  int32_t* block;
+  gp_req_meta* req;
+  float* summary;
+  uint8_t* staging;
+  float* logits;
+  int32_t* wset;
+  int32_t* free_stack;
+  gp_ctrl* ctrl;
+  gp_prefix_meta* prefix;
+  int32_t* prefix_pages;
+  const double* cos64;
+  const double* sin64;
+  const float* cos32;
+  const float* sin32;
+  // scratch: per-step plan
+  int32_t* plan_slot;     // [max_req] slot of request i
+  int32_t* plan_R;        // [max_req] resident tokens (prefix + private)
+  int32_t* plan_nb;       // [max_req] attention blocks (>= 1)
+  int32_t* plan_cum;      // [max_req + 1] prefix sums of plan_nb
+  int32_t* plan_flags;    // [max_req]
+  int32_t* plan_commit;   // [max_req] private slot receiving the staged token
+  int32_t* plan_cpos;     // [max_req] its position
+  int32_t* plan_dec;      // [max_req] decision of this step
+  int32_t* plan_bnd;      // [max_req] indices i of scoring boundaries
+  int32_t* plan_misc;     // [0] n, [1] n scoring boundaries, [2] total blocks/Hk
+  long long* plan_delta;  // [max_req] Delta accumulators
+  // scratch: attention split-K
+  float* partials;        // [num_workers][2][G][D + 2]
+  int32_t* seg_count;     // [max_req][Hk]
+  // scratch: compaction moves
+  int32_t* moves;         // [max_req][L][Hk][P][2] (dst, src) private slots
+  int32_t* moves_n;       // [max_req][L][Hk]
+};
+
+// ------------------------------------------------------------ helpers ---
+
+__device__ __forceinline__ void set_status(const PoolDev& p, uint32_t bit, int32_t info) {
+  uint32_t old = atomicOr(&p.ctrl->status, bit);
+  if (old == 0u) atomicExch(&p.ctrl->status_info, info);
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Round an fp64 value once, to nearest-even, to a bfloat16 bit pattern.
+// Written from the IEEE-754 definition: bf16 keeps 8 significant bits and the
+// fp32 exponent range; below 2^-126 its spacing is 2^-133.
+__device__ __forceinline__ uint16_t f64_to_bf16_rne(double x) {
+  uint64_t u = (uint64_t)__double_as_longlong(x);
+  uint16_t sign = (uint16_t)((u >> 48) & 0x8000u);
+  uint64_t a = u & 0x7fffffffffffffffull;
+  if (a >= 0x7ff0000000000000ull) {  // inf or nan
+    if (a == 0x7ff0000000000000ull) return sign | 0x7f80u;
+    return sign | 0x7fc0u;
+  }
+  int e = (int)(a >> 52);  // biased fp64 exponent
+  if (e >= 1023 - 126) {   // normal in bf16 (or overflows)
+    // keep 1 + 7 mantissa bits: drop the low 45 bits with ties-to-even
+    uint64_t lsb = (a >> 45) & 1ull;
+    uint64_t r = a + ((1ull << 44) - 1ull) + lsb;
+    r >>= 45;                          // exponent(11) | mantissa(7)
+    int eb = (int)(r >> 7) - 1023 + 127;
+    if (eb >= 255) return sign | 0x7f80u;
+    return sign | (uint16_t)((eb << 7) | (int)(r & 0x7f));
+  }
+  // subnormal bf16 range: value / 2^-133 rounded to an integer (0..128);
+  // 128 is the bit pattern of the smallest normal.  Scaling by 2^133 is exact.
+  double s = fabs(x) * 0x1p133;
+  double r = rint(s);
+  return sign | (uint16_t)r;
+}
+
+template <typename T> struct ElemIO;
+template <> struct ElemIO<float> {
+  static __device__ __forceinline__ float load(const float* p, int i) { return p[i]; }
+};
+template <> struct ElemIO<__nv_bfloat16> {
+  static __device__ __forceinline__ float load(const __nv_bfloat16* p, int i) {
+    return __bfloat162float(p[i]);
+  }
+};
+
+// ------------------------------------------------- mbarrier / bulk copy ---
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing on an mbarrier (TMA engine).
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, "
+      "0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~limit_ns of wall time and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 63u && global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------- reductions ---
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace gp

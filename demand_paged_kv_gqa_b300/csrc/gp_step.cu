@@ -1,0 +1,763 @@
+// gp_step.cu -- the per-step kernels around the attention kernel.
+//
+//   plan_kernel     once per step (before layer 0): per request, resident
+//                   tokens, attention blocks, boundary flags; prefix sums.
+//   select_kernel   per (boundary request, layer, kv head): softmax of both
+//                   summaries' scores, Top-p working-set size by radix select
+//                   with exact integer mass, Delta contribution, and the
+//                   compaction plan (which private tokens to drop).
+//   decide_kernel   one CTA: grow or compact per request, pages popped from
+//                   the lock-free stack in ascending slot order, metadata.
+//   commit_kernel   per (request, layer, kv head): compaction moves, then the
+//                   staged token written into its slot.
+//
+// Method: "GrowPage: On-Demand KV Budgeting for Efficient LLM Reasoning
+// Serving" -- abstract (capacity boundaries; compress within the current
+// allocation or acquire one more physical page) and evolve.pub review,
+// Summary (Top-p working sets of the two summaries; a larger recent set grows
+// the request by one page, otherwise compaction by the maximum of both
+// importance scores) and FAQ (Top-p, tau, local retention quota).
+#include "gp_internal.cuh"
+
+namespace gp {
+
+// ------------------------------------------------------- block helpers ---
+
+// Exclusive scan of one int per thread over the block (<= 1024 threads).
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int t = (lane < (int)(blockDim.x >> 5)) ? s_warp[lane] : 0;
+    int u = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, u, o);
+      if (lane >= o) u += y;
+    }
+    s_warp[lane] = u - t;  // exclusive prefix of warp totals
+    if (lane == 31) s_warp[32] = u;
+  }
+  __syncthreads();
+  const int res = s_warp[wid] + x - v;
+  *total = s_warp[32];
+  __syncthreads();
+  return res;
+}
+
+// ---------------------------------------------------------------- plan ---
+
+__global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int32_t* slots) {
+  __shared__ int s_warp[33];
+  __shared__ int s_bad;
+  __shared__ unsigned long long s_tok, s_btok;
+  if (threadIdx.x == 0) { s_bad = 0; s_tok = 0ull; s_btok = 0ull; }
+  __syncthreads();
+  int carry = 0, bcarry = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    int nb = 0, isb = 0;
+    if (i < n) {
+      const int slot = slots[i];
+      bool ok = (unsigned)slot < (unsigned)p.max_req;
+      if (ok) ok = p.req[slot].active != 0;
+      if (ok && i > 0) ok = slots[i - 1] < slot;
+      if (ok && p.req[slot].pos >= p.max_seq_len) {
+        ok = false;
+        set_status(p, GP_ST_POS_RANGE, slot);
+      }
+      if (!ok) {
+        s_bad = 1;
+        set_status(p, GP_ST_BAD_SLOTS, i);
+        p.plan_slot[i] = 0; p.plan_R[i] = 0; p.plan_nb[i] = 1; p.plan_flags[i] = 0;
+        nb = 1;
+      } else {
+        const gp_req_meta m = p.req[slot];
+        const int R = m.n_pre_pages * p.P + m.seq_priv;
+        nb = (R + kBlockTok - 1) / kBlockTok;
+        if (nb < 1) nb = 1;
+        const bool at_b = m.seq_priv == m.n_pages * p.P;
+        int flags = 0;
+        if (at_b) flags |= kPlanBoundary;
+        if (m.steps == 0) flags |= kPlanFirst;
+        if (at_b && p.mode == GP_MODE_GROWPAGE) flags |= kPlanScore;
+        isb = (flags & kPlanScore) ? 1 : 0;
+        p.plan_slot[i] = slot; p.plan_R[i] = R; p.plan_nb[i] = nb; p.plan_flags[i] = flags;
+        p.plan_delta[i] = 0;
+        atomicAdd(&s_tok, (unsigned long long)R);
+        if (at_b) atomicAdd(&s_btok, (unsigned long long)R);
+      }
+    }
+    int tot, btot;
+    const int ex = block_excl_scan(nb, s_warp, &tot);
+    const int bex = block_excl_scan(isb, s_warp, &btot);
+    if (i < n) {
+      p.plan_cum[i] = carry + ex;
+      if (isb) p.plan_bnd[bcarry + bex] = i;
+    }
+    carry += tot;
+    bcarry += btot;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    p.plan_cum[n] = carry;
+    const int good = s_bad ? 0 : n;
+    p.plan_misc[0] = good;
+    p.plan_misc[1] = s_bad ? 0 : bcarry;
+    p.plan_misc[2] = carry;
+    p.ctrl->plan_n = good;
+    p.ctrl->steps += 1;
+    p.ctrl->tokens_attended += (long long)s_tok;
+    p.ctrl->boundary_tokens += (long long)s_btok;
+  }
+}
+
+// -------------------------------------------------------------- select ---
+
+constexpr int kSelThreads = 256;
+
+__device__ __forceinline__ float block_max_f(float v, float* red) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    float x = (lane < (int)(blockDim.x >> 5)) ? red[lane] : -INFINITY;
+    x = warp_max(x);
+    if (lane == 0) red[32] = x;
+  }
+  __syncthreads();
+  const float r = red[32];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ unsigned long long block_sum_ull(unsigned long long v,
+                                                            unsigned long long* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    unsigned long long x = (lane < (int)(blockDim.x >> 5)) ? red[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) red[32] = x;
+  }
+  __syncthreads();
+  const unsigned long long r = red[32];
+  __syncthreads();
+  return r;
+}
+
+// Probability mass of a token in fixed point: e * 2^40 rounded to nearest
+// (e in (0, 1]; the scaling is exact, the conversion rounds once).
+__device__ __forceinline__ unsigned long long mass_q(float e) {
+  return (unsigned long long)__float2ll_rn(e * 0x1p40f);
+}
+
+// ceil(top_p * T) exactly, top_p an fp32 value in (0, 1].
+__device__ __forceinline__ unsigned long long ceil_mul(float top_p, unsigned long long T) {
+  const uint32_t b = __float_as_uint(top_p);
+  const int E = (int)((b >> 23) & 0xff);
+  unsigned long long M = (E == 0) ? (b & 0x7fffffu) : ((b & 0x7fffffu) | 0x800000u);
+  const int sh = (E == 0 ? 1 : E) - 150;  // top_p = M * 2^sh, sh < 0
+  const unsigned long long lo = M * T, hi = __umul64hi(M, T);
+  const int r = -sh;
+  if (r >= 128) return (lo | hi) ? 1ull : 0ull;
+  unsigned long long qv, rem;
+  if (r >= 64) {
+    qv = (r == 64) ? hi : (hi >> (r - 64));
+    rem = lo | ((r == 64) ? 0ull : (hi & ((1ull << (r - 64)) - 1ull)));
+  } else if (r == 0) {
+    qv = lo; rem = 0;
+  } else {
+    qv = (lo >> r) | (hi << (64 - r));
+    rem = lo & ((1ull << r) - 1ull);
+  }
+  return qv + (rem ? 1ull : 0ull);
+}
+
+struct SelShared {
+  unsigned int cnt[256];
+  unsigned long long mass[256];
+  unsigned long long red[33];
+  float redf[33];
+  int holes[256];
+  int srcs[256];
+  unsigned int pick_d;
+  unsigned long long pick_a, pick_b;
+  int done;
+};
+
+// Top-p working-set size: smallest k with (mass of the k largest) >= thr,
+// by a 4-pass radix select (8 bits per pass, most significant first) on the
+// fp32 bit patterns of e_j = exp(u_j - max), weighting each by its mass.
+__device__ int topp_radix(const float* u, int R, float mx, unsigned long long thr, SelShared& sh) {
+  uint32_t prefix = 0u, pmask = 0u;
+  unsigned long long mass_above = 0ull, cnt_above = 0ull;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int d = threadIdx.x; d < 256; d += blockDim.x) { sh.cnt[d] = 0u; sh.mass[d] = 0ull; }
+    if (threadIdx.x == 0) { sh.pick_d = 0u; sh.pick_a = 0ull; sh.pick_b = 0ull; }
+    __syncthreads();
+    for (int j = threadIdx.x; j < R; j += blockDim.x) {
+      const float e = expf(u[j] - mx);
+      const uint32_t bits = __float_as_uint(e);
+      if ((bits & pmask) == prefix) {
+        const int d = (bits >> shift) & 255;
+        atomicAdd(&sh.cnt[d], 1u);
+        atomicAdd(&sh.mass[d], mass_q(e));
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // descending digits: lane L owns digits 255-8L .. 248-8L
+      const int lane = threadIdx.x;
+      unsigned long long mloc = 0ull, cloc = 0ull;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        mloc += sh.mass[255 - 8 * lane - t];
+        cloc += sh.cnt[255 - 8 * lane - t];
+      }
+      unsigned long long mex = mloc, cex = cloc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        unsigned long long y = __shfl_up_sync(0xffffffffu, mex, o);
+        unsigned long long z = __shfl_up_sync(0xffffffffu, cex, o);
+        if (lane >= o) { mex += y; cex += z; }
+      }
+      mex -= mloc; cex -= cloc;  // mass / count of the digits above this lane's
+      const unsigned long long need = thr - mass_above;
+      const bool here = (mex < need) && (mex + mloc >= need);
+      const unsigned int bal = __ballot_sync(0xffffffffu, here);
+      if (here && lane == __ffs(bal) - 1) {
+        unsigned long long macc = mex, cacc = cex;
+        for (int t = 0; t < 8; ++t) {
+          const int d = 255 - 8 * lane - t;
+          if (macc + sh.mass[d] >= need || t == 7) {
+            sh.pick_d = (unsigned)d;
+            sh.pick_a = macc;
+            sh.pick_b = cacc;
+            break;
+          }
+          macc += sh.mass[d];
+          cacc += sh.cnt[d];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= sh.pick_d << shift;
+    pmask |= 255u << shift;
+    mass_above += sh.pick_a;
+    cnt_above += sh.pick_b;
+    __syncthreads();
+  }
+  const unsigned long long qstar = mass_q(__uint_as_float(prefix));
+  const unsigned long long rest = thr > mass_above ? thr - mass_above : 0ull;
+  const unsigned long long k = qstar ? (rest + qstar - 1ull) / qstar : 1ull;
+  return (int)(cnt_above + (k ? k : 1ull));
+}
+
+struct SelCtx {
+  const float* uS;
+  const float* uL;
+  float mS, mL, invS, invL;
+  int npre;           // prefix tokens (logical index of private slot 0)
+  int cut_pos;        // positions below this are compaction candidates
+  const int32_t* bt;  // private block-table row
+  const int32_t* tok_pos;
+  int P, L, Hk, layer, h, num_pages;
+};
+
+__device__ __forceinline__ unsigned long long key_of(const SelCtx& c, int s, bool* cand) {
+  int page = c.bt[s / c.P];
+  if ((unsigned)page >= (unsigned)c.num_pages) page = 0;
+  const int pos = c.tok_pos[(((size_t)page * c.L + c.layer) * c.Hk + c.h) * c.P + (s % c.P)];
+  *cand = pos < c.cut_pos;
+  const float eS = expf(c.uS[c.npre + s] - c.mS);
+  const float eL = expf(c.uL[c.npre + s] - c.mL);
+  const float I = fmaxf(eS * c.invS, eL * c.invL);
+  return ((unsigned long long)__float_as_uint(I) << 32) | (unsigned long long)(uint32_t)pos;
+}
+
+// Threshold key such that exactly `k` candidates have key <= threshold (keys
+// are distinct: they end with the token position).  Radix select, 8 bits per
+// pass from the top, stopping as soon as the chosen bucket is taken whole.
+__device__ unsigned long long kth_smallest(const SelCtx& c, int C, int k, SelShared& sh) {
+  unsigned long long prefix = 0ull, pmask = 0ull;
+  unsigned int below = 0u;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    for (int d = threadIdx.x; d < 256; d += blockDim.x) sh.cnt[d] = 0u;
+    __syncthreads();
+    for (int s = threadIdx.x; s < C; s += blockDim.x) {
+      bool cand;
+      const unsigned long long key = key_of(c, s, &cand);
+      if (cand && (key & pmask) == prefix) atomicAdd(&sh.cnt[(key >> shift) & 255], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned int acc = below;
+      int d = 0;
+      for (; d < 255; ++d) {
+        if (acc + sh.cnt[d] >= (unsigned)k) break;
+        acc += sh.cnt[d];
+      }
+      sh.pick_d = (unsigned)d;
+      sh.pick_a = acc;
+      sh.done = (acc + sh.cnt[d] == (unsigned)k) ? 1 : 0;
+    }
+    __syncthreads();
+    const unsigned int d = sh.pick_d;
+    below = (unsigned int)sh.pick_a;
+    prefix |= (unsigned long long)d << shift;
+    pmask |= 255ull << shift;
+    const int done = sh.done;
+    __syncthreads();
+    if (done) return prefix | ((shift == 0) ? 0ull : ((1ull << shift) - 1ull));
+  }
+  return prefix;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(PoolDev p) {
+  __shared__ SelShared sh;
+  const int nb = p.plan_misc[1];
+  const int items = nb * p.L * p.Hk;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int bi = item / (p.L * p.Hk);
+    const int rem = item % (p.L * p.Hk);
+    const int layer = rem / p.Hk, h = rem % p.Hk;
+    const int i = p.plan_bnd[bi];
+    const int slot = p.plan_slot[i];
+    const int R = p.plan_R[i];
+    const gp_req_meta m = p.req[slot];
+    const int npre = m.n_pre_pages * p.P;
+    const int C = m.n_pages * p.P;
+    const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
+    const float* uS = p.logits + row * 2 * p.logit_width;
+    const float* uL = uS + p.logit_width;
+    float mx[2], inv[2];
+    int W[2];
+    for (int X = 0; X < 2; ++X) {
+      const float* u = X ? uL : uS;
+      float v = -INFINITY;
+      for (int j = threadIdx.x; j < R; j += blockDim.x) v = fmaxf(v, u[j]);
+      mx[X] = block_max_f(v, sh.redf);
+      unsigned long long s = 0ull;
+      for (int j = threadIdx.x; j < R; j += blockDim.x) s += mass_q(expf(u[j] - mx[X]));
+      const unsigned long long T = block_sum_ull(s, sh.red);
+      const unsigned long long thr = ceil_mul(p.top_p, T);
+      W[X] = topp_radix(u, R, mx[X], thr, sh);
+      inv[X] = (float)(0x1p40 / (double)(T ? T : 1ull));
+    }
+    if (threadIdx.x == 0) {
+      p.wset[row * 2 + 0] = W[0];
+      p.wset[row * 2 + 1] = W[1];
+      atomicAdd((unsigned long long*)&p.plan_delta[i],
+                (unsigned long long)(long long)(W[0] - W[1]));
+    }
+    // compaction plan: drop the P lowest (importance, position) candidates
+    SelCtx c;
+    c.uS = uS; c.uL = uL; c.mS = mx[0]; c.mL = mx[1]; c.invS = inv[0]; c.invL = inv[1];
+    c.npre = npre;
+    const int weff = min(p.recent_window, C - p.P);
+    c.cut_pos = m.pos - weff;
+    c.bt = p.block + (size_t)slot * p.block_width + m.n_pre_pages;
+    c.tok_pos = p.tok_pos;
+    c.P = p.P; c.L = p.L; c.Hk = p.Hk; c.layer = layer; c.h = h; c.num_pages = p.num_pages;
+    const unsigned long long thr_key = kth_smallest(c, C, p.P, sh);
+    // holes below C-P and survivors of the last page, both ascending
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      int nh = 0;
+      for (int base = 0; base < C - p.P; base += 32) {
+        const int s = base + lane;
+        bool dropped = false;
+        if (s < C - p.P) {
+          bool cand;
+          const unsigned long long key = key_of(c, s, &cand);
+          dropped = cand && key <= thr_key;
+        }
+        const unsigned int bal = __ballot_sync(0xffffffffu, dropped);
+        if (dropped) {
+          const int r = nh + __popc(bal & ((1u << lane) - 1u));
+          if (r < 256) sh.holes[r] = s;
+        }
+        nh += __popc(bal);
+      }
+      int ns = 0;
+      for (int base = C - p.P; base < C; base += 32) {
+        const int s = base + lane;
+        bool kept = false;
+        if (s < C) {
+          bool cand;
+          const unsigned long long key = key_of(c, s, &cand);
+          kept = !(cand && key <= thr_key);
+        }
+        const unsigned int bal = __ballot_sync(0xffffffffu, kept);
+        if (kept) {
+          const int r = ns + __popc(bal & ((1u << lane) - 1u));
+          if (r < 256) sh.srcs[r] = s;
+        }
+        ns += __popc(bal);
+      }
+      if (nh != ns || nh > p.P) {
+        if (lane == 0) set_status(p, GP_ST_BAD_PLAN, slot);
+        nh = 0;
+      }
+      int32_t* mv = p.moves + row * p.P * 2;
+      for (int t = lane; t < nh; t += 32) {
+        mv[2 * t] = sh.holes[t];
+        mv[2 * t + 1] = sh.srcs[t];
+      }
+      if (lane == 0) p.moves_n[row] = nh;
+    }
+    __syncthreads();
+  }
+}
+
+// -------------------------------------------------------------- decide ---
+
+__global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
+  __shared__ int s_warp[33];
+  __shared__ int s_avail;
+  __shared__ unsigned long long s_cnt[5];
+  const int n = p.plan_misc[0];
+  if (threadIdx.x < 5) s_cnt[threadIdx.x] = 0ull;
+  __syncthreads();
+  for (int base = 0; base < n; base += blockDim.x) {
+    if (threadIdx.x == 0) s_avail = p.ctrl->free_top;
+    __syncthreads();
+    const int avail = s_avail;
+    const int i = base + threadIdx.x;
+    int wg = 0, want = 0, at_b = 0, slot = 0;
+    gp_req_meta m;
+    if (i < n) {
+      slot = p.plan_slot[i];
+      m = p.req[slot];
+      at_b = (p.plan_flags[i] & kPlanBoundary) != 0;
+      if (at_b) {
+        want = (p.mode == GP_MODE_GROWPAGE)
+                   ? ((double)p.plan_delta[i] > (double)p.tau ? 1 : 0)
+                   : 1;
+        wg = (want && m.n_pages < p.max_pages_per_req) ? 1 : 0;
+      }
+    }
+    int total;
+    const int rank = block_excl_scan(wg, s_warp, &total);
+    if (i < n) {
+      const int C = m.n_pages * p.P;
+      int dec, commit;
+      if (wg && rank < avail) {
+        const int page = p.free_stack[avail - 1 - rank];
+        p.block[(size_t)slot * p.block_width + m.n_pre_pages + m.n_pages] = page;
+        m.n_pages += 1;
+        dec = kGrow; commit = C;
+        m.n_grows += 1;
+        atomicAdd(&s_cnt[1], 1ull);
+      } else if (at_b) {
+        if (p.mode == GP_MODE_GROWPAGE) {
+          dec = want ? kCompactDenied : kCompact;
+          commit = C - p.P;
+          m.n_compacts += 1;
+          atomicAdd(&s_cnt[2], 1ull);
+          if (want) { m.n_denied += 1; atomicAdd(&s_cnt[3], 1ull); }
+        } else {
+          dec = kStarved; commit = -1;
+          m.n_starved += 1;
+          atomicAdd(&s_cnt[4], 1ull);
+          set_status(p, GP_ST_STARVED, slot);
+        }
+      } else {
+        dec = kNone; commit = m.seq_priv;
+      }
+      if (at_b) {
+        m.n_boundaries += 1;
+        m.last_decision = dec;
+        m.delta = p.plan_delta[i];
+        atomicAdd(&s_cnt[0], 1ull);
+      }
+      p.plan_dec[i] = dec;
+      p.plan_commit[i] = commit;
+      p.plan_cpos[i] = m.pos;
+      if (commit >= 0) m.seq_priv = commit + 1;
+      m.pos += 1;
+      m.steps += 1;
+      p.req[slot] = m;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int g = total < avail ? total : avail;
+      atomicSub(&p.ctrl->free_top, g);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    p.ctrl->boundaries += (long long)s_cnt[0];
+    p.ctrl->grows += (long long)s_cnt[1];
+    p.ctrl->compacts += (long long)s_cnt[2];
+    p.ctrl->denied += (long long)s_cnt[3];
+    p.ctrl->starved += (long long)s_cnt[4];
+  }
+}
+
+// -------------------------------------------------------------- commit ---
+
+__device__ __forceinline__ uint8_t* slot_row(const PoolDev& p, const int32_t* bt, int s, int layer,
+                                             int h, int rowb, int* page_out) {
+  int page = bt[s / p.P];
+  if ((unsigned)page >= (unsigned)p.num_pages) {
+    set_status(p, GP_ST_BAD_PAGE, page);
+    page = 0;
+  }
+  *page_out = page;
+  return p.kv + (size_t)page * p.page_bytes + (size_t)layer * p.layer_bytes +
+         (size_t)h * p.head_bytes + (size_t)(s % p.P) * rowb;
+}
+
+__global__ void __launch_bounds__(256) commit_kernel(PoolDev p) {
+  const int n = p.plan_misc[0];
+  const int rowb = p.D * p.elem_bytes;
+  const int chunks = rowb / 16;
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const int items = n * p.L * p.Hk;
+  unsigned long long moved = 0ull;
+  for (int item = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); item < items; item += warps) {
+    const int i = item / (p.L * p.Hk);
+    const int rem = item % (p.L * p.Hk);
+    const int layer = rem / p.Hk, h = rem % p.Hk;
+    const int slot = p.plan_slot[i];
+    const int dec = p.plan_dec[i];
+    const int commit = p.plan_commit[i];
+    const int npre = p.req[slot].n_pre_pages;
+    const int32_t* bt = p.block + (size_t)slot * p.block_width + npre;
+    const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
+    if (dec == kCompact || dec == kCompactDenied) {
+      const int nm = p.moves_n[row];
+      const int32_t* mv = p.moves + row * p.P * 2;
+      for (int t = 0; t < nm; ++t) {
+        const int dst = mv[2 * t], src = mv[2 * t + 1];
+        int pd, ps;
+        uint8_t* rd = slot_row(p, bt, dst, layer, h, rowb, &pd);
+        const uint8_t* rs = slot_row(p, bt, src, layer, h, rowb, &ps);
+        for (int c = lane; c < chunks; c += 32) {
+          const uint4 kx = *reinterpret_cast<const uint4*>(rs + 16 * c);
+          const uint4 vx = *reinterpret_cast<const uint4*>(rs + p.half_bytes + 16 * c);
+          *reinterpret_cast<uint4*>(rd + 16 * c) = kx;
+          *reinterpret_cast<uint4*>(rd + p.half_bytes + 16 * c) = vx;
+        }
+        if (lane == 0) {
+          int32_t* tp_s = p.tok_pos + (((size_t)ps * p.L + layer) * p.Hk + h) * p.P + (src % p.P);
+          int32_t* tp_d = p.tok_pos + (((size_t)pd * p.L + layer) * p.Hk + h) * p.P + (dst % p.P);
+          *tp_d = *tp_s;
+        }
+      }
+      moved += (unsigned long long)nm;
+    }
+    __syncwarp();
+    if (commit >= 0) {
+      int pg;
+      uint8_t* rd = slot_row(p, bt, commit, layer, h, rowb, &pg);
+      const uint8_t* st = p.staging + row * 2 * rowb;
+      for (int c = lane; c < chunks; c += 32) {
+        *reinterpret_cast<uint4*>(rd + 16 * c) = *reinterpret_cast<const uint4*>(st + 16 * c);
+        *reinterpret_cast<uint4*>(rd + p.half_bytes + 16 * c) =
+            *reinterpret_cast<const uint4*>(st + rowb + 16 * c);
+      }
+      if (lane == 0)
+        p.tok_pos[(((size_t)pg * p.L + layer) * p.Hk + h) * p.P + (commit % p.P)] = p.plan_cpos[i];
+    }
+  }
+  if (lane == 0 && moved) atomicAdd((unsigned long long*)&p.ctrl->moved_tokens, moved);
+}
+
+// --------------------------------------------------------------- admin ---
+
+__global__ void init_kernel(PoolDev p) {
+  const int stride = gridDim.x * blockDim.x;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < p.num_pages; j += stride)
+    p.free_stack[j] = p.num_pages - 1 - j;  // top holds page 0
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.ctrl->free_top = p.num_pages;
+}
+
+// Pop `count` pages (the host checked availability) into dst[0..count).
+__global__ void pop_pages_kernel(PoolDev p, int32_t* dst, int count) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int top = p.ctrl->free_top;
+  for (int k = 0; k < count; ++k) dst[k] = p.free_stack[--top];
+  p.ctrl->free_top = top;
+}
+
+__global__ void prefix_meta_kernel(PoolDev p, int pid, int npages, int len) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  gp_prefix_meta m;
+  m.refs = 1; m.n_pages = npages; m.len = len; m.reserved = 0;
+  p.prefix[pid] = m;
+}
+
+// New request: block-table row = prefix pages + budget private pages.
+__global__ void admit_kernel(PoolDev p, int slot, int budget, int prefix_id, int prompt_len) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int32_t* bt = p.block + (size_t)slot * p.block_width;
+  int npre = 0, plen = 0;
+  if (prefix_id >= 0) {
+    gp_prefix_meta& pm = p.prefix[prefix_id];
+    npre = pm.n_pages;
+    plen = pm.len;
+    for (int k = 0; k < npre; ++k) bt[k] = p.prefix_pages[(size_t)prefix_id * p.max_prefix_pages + k];
+    pm.refs += 1;
+  }
+  int top = p.ctrl->free_top;
+  for (int k = 0; k < budget; ++k) bt[npre + k] = p.free_stack[--top];
+  p.ctrl->free_top = top;
+  gp_req_meta m = {};
+  m.active = 1;
+  m.prefix_id = prefix_id;
+  m.n_pre_pages = npre;
+  m.n_pages = budget;
+  m.seq_priv = prompt_len;
+  m.pos = plen + prompt_len;
+  p.req[slot] = m;
+}
+
+// Store tokens 0..count-1 of k, v ([L][count][Hk][d], keys not yet rotated)
+// into the pages listed in `pages` (token t -> page t/P, slot t%P), keys
+// rotated to position pos0 + t in fp64 and rounded once to the dtype.
+template <typename T>
+__global__ void write_tokens_kernel(PoolDev p, const int32_t* pages, const T* k, const T* v,
+                                    int count, int pos0) {
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  const int D = p.D, H = D / 2;
+  const long long items = (long long)p.L * count * p.Hk;
+  for (long long it = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+    const int layer = (int)(it / ((long long)count * p.Hk));
+    const int rem = (int)(it % ((long long)count * p.Hk));
+    const int t = rem / p.Hk, h = rem % p.Hk;
+    int page = pages[t / p.P];
+    if ((unsigned)page >= (unsigned)p.num_pages) { set_status(p, GP_ST_BAD_PAGE, page); continue; }
+    T* dst = reinterpret_cast<T*>(p.kv + (size_t)page * p.page_bytes + (size_t)layer * p.layer_bytes +
+                                  (size_t)h * p.head_bytes) + (size_t)(t % p.P) * D;
+    T* dstv = reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(dst) + p.half_bytes);
+    const T* src = k + (((size_t)layer * count + t) * p.Hk + h) * D;
+    const T* srcv = v + (((size_t)layer * count + t) * p.Hk + h) * D;
+    const int pos = pos0 + t;
+    for (int e = lane; e < H; e += 32) {
+      const double x = (double)ElemIO<T>::load(src, e), y = (double)ElemIO<T>::load(src, e + H);
+      double a = x, b = y;
+      if (p.rope) {
+        const double c = p.cos64[(size_t)pos * H + e], s = p.sin64[(size_t)pos * H + e];
+        a = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, s));
+        b = __dadd_rn(__dmul_rn(y, c), __dmul_rn(x, s));
+      }
+      if constexpr (sizeof(T) == 2) {
+        reinterpret_cast<uint16_t*>(dst)[e] = f64_to_bf16_rne(a);
+        reinterpret_cast<uint16_t*>(dst)[e + H] = f64_to_bf16_rne(b);
+      } else {
+        dst[e] = __double2float_rn(a);
+        dst[e + H] = __double2float_rn(b);
+      }
+    }
+    for (int e = lane; e < D; e += 32) dstv[e] = srcv[e];
+    if (lane == 0) p.tok_pos[(((size_t)page * p.L + layer) * p.Hk + h) * p.P + (t % p.P)] = pos;
+  }
+}
+
+__global__ void free_kernel(PoolDev p, int slot) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  gp_req_meta& m = p.req[slot];
+  const int32_t* bt = p.block + (size_t)slot * p.block_width;
+  int top = p.ctrl->free_top;
+  for (int k = 0; k < m.n_pages; ++k) p.free_stack[top++] = bt[m.n_pre_pages + k];
+  if (m.prefix_id >= 0) {
+    gp_prefix_meta& pm = p.prefix[m.prefix_id];
+    pm.refs -= 1;
+    if (pm.refs == 0)
+      for (int k = 0; k < pm.n_pages; ++k)
+        p.free_stack[top++] = p.prefix_pages[(size_t)m.prefix_id * p.max_prefix_pages + k];
+  }
+  p.ctrl->free_top = top;
+  m.active = 0;
+}
+
+__global__ void release_prefix_kernel(PoolDev p, int pid) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  gp_prefix_meta& pm = p.prefix[pid];
+  pm.refs -= 1;
+  if (pm.refs == 0) {
+    int top = p.ctrl->free_top;
+    for (int k = 0; k < pm.n_pages; ++k)
+      p.free_stack[top++] = p.prefix_pages[(size_t)pid * p.max_prefix_pages + k];
+    p.ctrl->free_top = top;
+  }
+}
+
+// ------------------------------------------------------------ launchers ---
+
+cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(p, n, slots);
+  return cudaGetLastError();
+}
+cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st) {
+  select_kernel<<<grid, kSelThreads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_decide(const PoolDev& p, cudaStream_t st) {
+  decide_kernel<<<1, 1024, 0, st>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st) {
+  commit_kernel<<<grid, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_init(const PoolDev& p, cudaStream_t st) {
+  init_kernel<<<256, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+cudaError_t launch_pop_pages(const PoolDev& p, int32_t* dst, int count, cudaStream_t st) {
+  pop_pages_kernel<<<1, 32, 0, st>>>(p, dst, count);
+  return cudaGetLastError();
+}
+cudaError_t launch_prefix_meta(const PoolDev& p, int pid, int npages, int len, cudaStream_t st) {
+  prefix_meta_kernel<<<1, 32, 0, st>>>(p, pid, npages, len);
+  return cudaGetLastError();
+}
+cudaError_t launch_admit(const PoolDev& p, int slot, int budget, int prefix_id, int prompt_len,
+                         cudaStream_t st) {
+  admit_kernel<<<1, 32, 0, st>>>(p, slot, budget, prefix_id, prompt_len);
+  return cudaGetLastError();
+}
+cudaError_t launch_write_tokens(const PoolDev& p, const int32_t* pages, const void* k, const void* v,
+                                int count, int pos0, cudaStream_t st) {
+  if (count <= 0) return cudaSuccess;
+  const long long items = (long long)p.L * count * p.Hk;
+  long long blocks = (items + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  if (p.dtype == GP_DTYPE_BF16)
+    write_tokens_kernel<__nv_bfloat16><<<(int)blocks, 256, 0, st>>>(
+        p, pages, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, count, pos0);
+  else
+    write_tokens_kernel<float><<<(int)blocks, 256, 0, st>>>(p, pages, (const float*)k,
+                                                            (const float*)v, count, pos0);
+  return cudaGetLastError();
+}
+cudaError_t launch_free(const PoolDev& p, int slot, cudaStream_t st) {
+  free_kernel<<<1, 32, 0, st>>>(p, slot);
+  return cudaGetLastError();
+}
+cudaError_t launch_release_prefix(const PoolDev& p, int pid, cudaStream_t st) {
+  release_prefix_kernel<<<1, 32, 0, st>>>(p, pid);
+  return cudaGetLastError();
+}
+
+}  // namespace gp
