@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Decode throughput of the GrowPage hot path on one B300 (or N replicas).
+
+Default workload: a 32-layer Llama-3-8B-shaped attention stack (32 q heads,
+8 kv heads, d=128, bf16 K/V/q, fp32 summaries), batch 64 kept full from a
+seeded request stream (prompts 128-1024 tokens, lognormal output lengths,
+median 4096, clipped to 1k-16k, demand phases every 512 steps), page 16,
+a 40 GB page pool, initial budget 64 pages, Top-p 0.9, recent window 64.
+
+One step = one decode step of the whole path: for every layer the fused
+paged-attention + summary kernel, then the boundary kernels (working sets,
+grow / compact, compaction moves, commit).  The same kernels are timed
+again in full-KV mode (every boundary grows, nothing is compacted; the host
+preempts when the pool is full).
+
+Timing: CUDA events on the pool's stream around each step's launches; the
+next step's inputs are drawn on the device between steps, outside the
+events.  The pool (tens of GB) is far larger than L2.  The attention
+kernel's average launch time comes from events around layers 1..L-1 of
+each timed step.  Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b_32layer")
+    ap.add_argument("--preroll", type=int, default=1024,
+                    help="untimed decode steps before warm-up (boundaries need history)")
+    ap.add_argument("--no-full-kv", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=16)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        smax = 0.0
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = max(smax, float(r[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.lower() in ("active", "1"):
+                    reasons.add(nm)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ byte counts
+
+def attention_bytes(w, tok, req_steps, btok):
+    """Algorithmic HBM bytes of the attention kernel for one layer.
+
+    tok: resident tokens summed over the requests (and steps) covered;
+    req_steps: request-steps covered; btok: resident tokens of requests at a
+    boundary (their summary scores are written).
+    """
+    eb = w.elem_bytes
+    hk, hq, d, P = w.num_kv_heads, w.num_q_heads, w.head_dim, w.page_size
+    kv = tok * hk * 2 * d * eb                       # K and V of resident tokens
+    per_req = (2 * hq * d * eb                       # q read, out written
+               + 2 * hk * d * eb                     # new k, v read
+               + 2 * hk * d * eb                     # staged token written
+               + 2 * 2 * hk * d * 4)                 # both summaries read + written
+    bt = tok / P * 4                                 # block-table entries
+    logits = btok * 2 * hk * 4                       # summary scores written
+    return kv + req_steps * per_req + bt + logits
+
+
+# ------------------------------------------------------------ our arm
+
+def run_ours(args, ws, rank, local):
+    from demand_paged_kv_gqa_b300 import growpage as gpb
+    from demand_paged_kv_gqa_b300 import synth
+    from demand_paged_kv_gqa_b300.engine import Engine
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = synth.WORKLOADS[args.workload]
+    peaks = {}
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        peaks = json.load(open(pk))
+    hbm_peak = float(peaks.get("hbm_gbs", 6400.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+
+    def measure(mode, label):
+        eng = Engine(w, mode=mode, device=dev, seed_offset=rank)
+        eng.fill()
+        stream = eng.pool.stream
+        for _ in range(args.preroll):
+            eng.prepare_inputs()
+            eng.step()
+        for _ in range(args.warmup):
+            eng.prepare_inputs()
+            eng.step()
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        st0 = eng.pool.stats()
+        launches0 = eng.pool.launch_count()
+        tok0 = eng.tokens_timed
+        L = w.num_layers
+        evs = []
+        req_steps = 0
+        clk = ClockSampler(local)
+        clk.start()
+        t_wall = time.time()
+        for _ in range(args.steps):
+            eng.prepare_inputs()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+            def before():
+                e[0].record(stream)
+
+            def after_layer(l):
+                if l == 0:
+                    e[1].record(stream)
+                elif l == L - 1:
+                    e[2].record(stream)
+
+            def after():
+                e[3].record(stream)
+
+            n = eng.step(timed=True, before_step=before, after_layer=after_layer, after_step=after)
+            req_steps += n
+            evs.append(e)
+        torch.cuda.synchronize()
+        wall = time.time() - t_wall
+        clocks = clk.stop()
+        st1 = eng.pool.stats()
+        launches = eng.pool.launch_count() - launches0
+        step_ms = sum(e[0].elapsed_time(e[3]) for e in evs)
+        attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+        tokens = eng.tokens_timed - tok0
+        dtok = st1.tokens_attended - st0.tokens_attended
+        dbtok = st1.boundary_tokens - st0.boundary_tokens
+        res = dict(label=label, step_ms=step_ms, attn_ms=attn_ms, tokens=tokens, wall=wall,
+                   clocks=clocks, launches=launches, dtok=dtok, dbtok=dbtok, req_steps=req_steps,
+                   boundaries=st1.boundaries - st0.boundaries, grows=st1.grows - st0.grows,
+                   compacts=st1.compacts - st0.compacts, denied=st1.denied - st0.denied,
+                   moved=st1.moved_tokens - st0.moved_tokens, preempted=eng.preempted,
+                   free_pages=st1.free_top, num_pages=eng.num_pages)
+        # attention kernel: layers 1..L-1 of each timed step
+        n_attn = (L - 1) * args.steps
+        per_layer_bytes = attention_bytes(w, dtok, req_steps, dbtok)  # one layer, all steps
+        res["attn_launch_ms"] = attn_ms / n_attn if n_attn else float("nan")
+        res["attn_bytes_per_launch"] = per_layer_bytes / args.steps
+        res["attn_gbs"] = (per_layer_bytes * (L - 1) / (attn_ms * 1e-3) / 1e9) if attn_ms else 0.0
+        res["step_bytes"] = per_layer_bytes * L / args.steps
+        res["step_gbs"] = per_layer_bytes * L / (step_ms * 1e-3) / 1e9 if step_ms else 0.0
+        res["e2e"] = measure_e2e(eng, args.e2e_steps) if (args.e2e_steps and label == "growpage") else None
+        eng.pool.sync()
+        del eng
+        torch.cuda.empty_cache()
+        return res
+
+    def measure_e2e(eng, k):
+        """Same metric through the C-ABI with inputs from pinned host memory
+        and outputs read back to pinned host memory, copies inside the events."""
+        stream = eng.pool.stream
+        hq_ = torch.empty_like(eng.q, device="cpu").pin_memory()
+        hk_ = torch.empty_like(eng.k, device="cpu").pin_memory()
+        hv_ = torch.empty_like(eng.v, device="cpu").pin_memory()
+        ho_ = torch.empty_like(eng.out, device="cpu").pin_memory()
+        ms = 0.0
+        toks = 0
+        h2d = d2h = 0
+        for _ in range(k):
+            eng.prepare_inputs()
+            hq_.copy_(eng.q); hk_.copy_(eng.k); hv_.copy_(eng.v)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+
+            def before():
+                e0.record(stream)
+                with torch.cuda.stream(stream):
+                    eng.q.copy_(hq_, non_blocking=True)
+                    eng.k.copy_(hk_, non_blocking=True)
+                    eng.v.copy_(hv_, non_blocking=True)
+
+            def after():
+                with torch.cuda.stream(stream):
+                    ho_.copy_(eng.out, non_blocking=True)
+                e1.record(stream)
+
+            n = eng.step(before_step=before, after_step=after)
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+            toks += n
+            h2d = hq_.nbytes + hk_.nbytes + hv_.nbytes
+            d2h = ho_.nbytes
+        return dict(value=toks / (ms * 1e-3), h2d=h2d, d2h=d2h)
+
+    gp_res = measure(gpb.GP_MODE_GROWPAGE, "growpage")
+    fk_res = None if args.no_full_kv else measure(gpb.GP_MODE_FULL_KV, "full_kv")
+
+    # max over ranks of the time, sum of tokens
+    t_ms = gp_res["step_ms"]
+    tokens = gp_res["tokens"]
+    if ws > 1:
+        tt = torch.tensor([t_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        nn = torch.tensor([tokens], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(nn)
+        t_ms, tokens = float(tt.item()), float(nn.item())
+    if rank != 0:
+        return None
+    value = tokens / (t_ms * 1e-3)
+    a_gbs = gp_res["attn_gbs"]
+    line = {
+        "metric": "decode tokens/s per B300 (GrowPage vs full-KV); % of HBM roofline",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded walk queries, planted keys, N(0,1) keys/values)",
+        "config": {
+            "workload": f"{w.name}: {w.num_layers} layers, {w.num_q_heads}q/{w.num_kv_heads}kv, "
+                        f"d={w.head_dim}, {w.dtype}, batch {w.batch}, page {w.page_size}, "
+                        f"pool {gp_res['num_pages']} pages, budget {w.budget_pages} pages, "
+                        f"top_p {w.top_p}, window {w.recent_window}",
+            "mode": "growpage",
+            "preroll_steps": args.preroll,
+            "l2": "inputs larger than L2 (page pool of tens of GB)",
+            "timing": "CUDA events around each step's launches; inputs drawn between steps",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "attn_kernel (paged GQA decode + summaries)",
+            "achieved": round(a_gbs, 1),
+            "peak": hbm_peak,
+            "peak_source": peak_src,
+            "unit": "GB/s",
+            "frac": round(a_gbs / hbm_peak, 4),
+            "traffic": None,
+            "bytes_per_launch": round(gp_res["attn_bytes_per_launch"]),
+            "launch_ms": round(gp_res["attn_launch_ms"], 5),
+        },
+        "step_roofline": {
+            "achieved": round(gp_res["step_gbs"], 1), "unit": "GB/s",
+            "frac": round(gp_res["step_gbs"] / hbm_peak, 4),
+            "frac_of_8tbs": round(gp_res["step_gbs"] / 8000.0, 4),
+        },
+        "gpu_launches": int(gp_res["launches"]),
+        "clocks": gp_res["clocks"],
+        "growpage": {k: gp_res[k] for k in ("boundaries", "grows", "compacts", "denied", "moved",
+                                            "tokens", "req_steps", "free_pages")},
+    }
+    line["growpage"]["mean_resident_tokens"] = round(gp_res["dtok"] / max(1, gp_res["req_steps"]), 1)
+    if gp_res["e2e"]:
+        e = gp_res["e2e"]
+        line["e2e"] = {"value": round(e["value"] * ws, 1), "unit": "tokens/s",
+                       "h2d_bytes_per_step": int(e["h2d"]), "d2h_bytes_per_step": int(e["d2h"])}
+    if fk_res:
+        fv = fk_res["tokens"] / (fk_res["step_ms"] * 1e-3)
+        line["full_kv"] = {
+            "value": round(fv * ws, 1), "unit": "tokens/s",
+            "ms_per_step": round(fk_res["step_ms"] / args.steps, 4),
+            "attn_gbs": round(fk_res["attn_gbs"], 1),
+            "mean_resident_tokens": round(fk_res["dtok"] / max(1, fk_res["req_steps"]), 1),
+            "preempted": fk_res["preempted"], "tokens": fk_res["tokens"],
+        }
+    return line
+
+
+# ------------------------------------------------------------ oracle arm
+
+def oracle_sample(w, seconds, max_steps=None):
+    """Time the CPU oracle on one request of the workload (all layers).
+
+    The request is admitted with a full initial budget (prompt = budget) so
+    that its first step is a boundary and every page-size-th step after it.
+    Returns (tokens/s, steps, seconds, threads).
+    """
+    import numpy as np
+    from demand_paged_kv_gqa_b300 import synth
+    from oracle.pool import OracleConfig, OraclePool
+    try:
+        from threadpoolctl import threadpool_limits
+        lim = threadpool_limits(1)
+    except Exception:
+        lim = None
+    torch.set_num_threads(1)
+    pl = w.budget_pages * w.page_size
+    st = synth.RequestStream(w, 0, 4096)
+    k, v = st.prompt(pl)
+    pool = OraclePool(OracleConfig.from_workload(w, num_pages=4 * w.budget_pages + 64))
+    pool.add_request(0, k.double().numpy(), v.double().numpy(), w.budget_pages)
+    steps = 0
+    t0 = time.time()
+    while True:
+        q, kk, vv = st.next_step()
+        pool.step([0], q[None].double().numpy(), kk[None].double().numpy(), vv[None].double().numpy())
+        steps += 1
+        el = time.time() - t0
+        if el >= seconds or (max_steps and steps >= max_steps):
+            break
+    del lim
+    return steps / el, steps, el, 1
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    from demand_paged_kv_gqa_b300 import synth
+    w = synth.WORKLOADS[args.workload]
+    per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    # warm-up then K timed samples, each a bounded run of the oracle
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step / 4, max_steps=1)
+    tps, steps, secs = [], 0, 0.0
+    for _ in range(args.steps):
+        v, s, e, _ = oracle_sample(w, per_step, max_steps=4)
+        steps += s
+        secs += e
+    value = steps / secs
+    sample = (f"one request of {w.name} ({w.num_layers} layers, prompt = budget "
+              f"{w.budget_pages * w.page_size} tokens, boundary on its first step), "
+              f"{steps} oracle decode steps over {args.steps} samples")
+    return {
+        "impl": "reference",
+        "metric": "decode tokens/s per B300 (GrowPage vs full-KV); % of HBM roofline",
+        "value": round(value, 4), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1000 * secs / max(1, steps), 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "mode": "growpage"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_info()
+    if ws > 1:
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        torch.distributed.init_process_group(backend)
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+    else:
+        line = run_ours(args, ws, rank, local)
+        if line is not None and not args.no_cpu_baseline:
+            from demand_paged_kv_gqa_b300 import synth
+            w = synth.WORKLOADS[args.workload]
+            v, s, e, cores = oracle_sample(w, args.cpu_seconds)
+            line["cpu_baseline"] = {
+                "value": round(v, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "sample": f"one request of {w.name}, all {w.num_layers} layers, {s} decode steps "
+                          f"({e:.1f} s), prompt = initial budget so boundaries occur"}
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

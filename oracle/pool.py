@@ -227,13 +227,23 @@ class OraclePool:
             self._unref(r.prefix_id)
 
     # ------------------------------------------------------------- step ----
-    def step(self, slots, q, k, v):
+    def step(self, slots, q, k, v, arbiter=None):
         """One decode step for the requests ``slots`` (ascending).
 
         q: [n][L][Hq][d], k, v: [n][L][Hk][d] (storage-dtype values).
         Returns a dict: out [n][L][Hq][d] fp64, staged_k [n][L][Hk][d] (the
         stored key of the step's token), summaries [n][L][Hk][2][d] fp32,
         boundary records by slot.
+
+        ``arbiter`` (optional) lets a checker resynchronise the simulation
+        at near-ties, where more than one outcome is correct.  It is asked
+        only at two points and only after the oracle has computed its own
+        choice: ``arbiter.decision(slot, record)`` may return another
+        decision for a boundary whose record is ``decision_exempt``, and
+        ``arbiter.dropped(slot, layer, head, pos_priv, dropped, gap)`` may
+        return another set of dropped indices when the relative importance
+        gap at the cut is at most 1e-5.  Anything else it returns is
+        rejected.  The arithmetic of the step does not change.
         """
         c = self.cfg
         L, hk, hq, d, G, P = (c.num_layers, c.num_kv_heads, c.num_q_heads,
@@ -326,6 +336,12 @@ class OraclePool:
             dmax = int(np.sum(band[:, :, 0, 1] - band[:, :, 1, 0]))
             exempt = pol.wants_grow(dmin, c.tau) != pol.wants_grow(dmax, c.tau)
             can = len(r.pages) < c.max_pages_per_req
+            if arbiter is not None and exempt:
+                # near-tie: the checker may adopt the other side of the rule
+                rec0 = BoundaryRecord(slot, delta, None, exempt, ws, wl, None, None)
+                forced = arbiter.decision(slot, rec0)
+                if forced is not None:
+                    want = bool(forced)
             if want and can and self.free:
                 r.pages.append(self.free.pop())
                 dec = GROW
@@ -358,6 +374,16 @@ class OraclePool:
                     posp = r.toks.pos[l, g, :cap]
                     dropped, gap = pol.compaction_plan(imp, posp, r.pos, cap, P,
                                                        c.recent_window)
+                    if arbiter is not None and gap <= 1e-5:
+                        alt = arbiter.dropped(slot, l, g, posp.copy(), dropped.copy(), gap)
+                        if alt is not None:
+                            alt = np.asarray(alt, dtype=np.int64)
+                            w_eff = min(c.recent_window, cap - P)
+                            ok = (len(set(alt.tolist())) == len(dropped)
+                                  and np.all(posp[alt] < r.pos - w_eff))
+                            if not ok:
+                                raise ValueError("arbiter returned an invalid dropped set")
+                            dropped = alt
                     gaps[l, g] = gap
                     keep = np.ones(cap, bool)
                     keep[dropped] = False

@@ -1,0 +1,106 @@
+"""CUDA path vs the CPU oracle, step by step, on the seeded workloads.
+
+Marked ``gpu``: these call the C-ABI library on a B300.  Sizes are the
+workloads' own where the oracle finishes in seconds to a minute; longer
+trajectories are cut to a window that still spans many boundaries.
+"""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from tests import gpu_harness
+    from demand_paged_kv_gqa_b300 import growpage, synth
+    return gpu_harness, growpage, synth
+
+
+def _check(rep):
+    assert not rep.failures, "\n".join(rep.failures)
+
+
+def test_tiny_growpage_full_trajectory(env):
+    # 1 request, 1 layer, 2 kv heads x 2 q heads, d=64, fp32, page 16,
+    # prompt 64 = initial budget: boundaries at step 1 and every 16 steps.
+    H, gp, synth = env
+    h = H.Harness(synth.WORKLOADS["tiny"], 1)
+    rep = h.run(256)
+    _check(rep)
+    assert rep.boundaries == 16
+    assert rep.max_out_err < 1e-4
+
+
+def test_tiny_full_kv(env):
+    H, gp, synth = env
+    h = H.Harness(synth.WORKLOADS["tiny"], 1, mode=gp.GP_MODE_FULL_KV)
+    rep = h.run(256)
+    _check(rep)
+    assert rep.compacts == 0 and rep.grows == rep.boundaries == 16
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_tiny_variants_gqa_group_and_rope(env, G):
+    # G=1 is plain multi-head attention; RoPE on with theta 10000.
+    H, gp, synth = env
+    w = synth.WORKLOADS["tiny"].replace(num_q_heads=2 * G, rope_theta=10000.0, batch=3)
+    h = H.Harness(w, 3)
+    rep = h.run(120)
+    _check(rep)
+    assert rep.boundaries >= 3 * 7
+
+
+def test_tiny_fp32_d128_several_requests(env):
+    H, gp, synth = env
+    w = synth.WORKLOADS["tiny"].replace(head_dim=128, num_q_heads=8, num_kv_heads=2,
+                                        rope_theta=500000.0, batch=4, prompt_min=20,
+                                        prompt_max=64, num_pages=64, num_layers=2)
+    h = H.Harness(w, 4)
+    rep = h.run(150)
+    _check(rep)
+    assert rep.boundaries > 10
+
+
+def test_llama8b_1layer_window(env):
+    # One Llama-3-8B-shaped layer (32q / 8kv, d=128, bf16, RoPE 5e5), the 16
+    # requests of the workload, first 640 decode steps (dozens of boundaries).
+    H, gp, synth = env
+    h = H.Harness(synth.WORKLOADS["llama8b_1layer"], 16)
+    rep = h.run(640)
+    _check(rep)
+    assert rep.boundaries > 50
+    assert rep.max_out_err < 2e-2
+
+
+def test_llama8b_1layer_small_budget_compacts(env):
+    # Same layer with a budget of 8 pages and Top-p 0.99: many compactions.
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=100, prompt_max=128, top_p=0.99,
+                                                  budget_pages=8, max_pages_per_req=12)
+    h = H.Harness(w, 6, budget_pages=8)
+    rep = h.run(300)
+    _check(rep)
+    assert rep.compacts > 20
+
+
+def test_llama8b_1layer_full_kv(env):
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=900, prompt_max=1024)
+    h = H.Harness(w, 8, mode=gp.GP_MODE_FULL_KV)
+    rep = h.run(200)
+    _check(rep)
+    assert rep.grows > 8 and rep.compacts == 0
+
+
+def test_pool_exhaustion_compacts_instead(env):
+    # tau < 0: every boundary wants to grow; 6 pages in the pool, 4 taken by
+    # the prompt: the first two boundaries grow, the rest compact (denied).
+    H, gp, synth = env
+    w = synth.WORKLOADS["tiny"].replace(tau=-1.0, num_pages=6)
+    h = H.Harness(w, 1)
+    rep = h.run(100)
+    _check(rep)
+    assert rep.grows == 2 and rep.compacts >= 4
