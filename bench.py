@@ -50,7 +50,25 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=16)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small profiling cases)")
+    ap.add_argument("--pool-gb", type=float, default=0.0,
+                    help="override the page-pool size in GB (small profiling cases)")
     return ap.parse_args()
+
+
+def workload_for(args):
+    """The named workload, with the profiling overrides applied."""
+    from demand_paged_kv_gqa_b300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.replace(num_layers=args.layers)
+    if args.layers or args.pool_gb:
+        gb = args.pool_gb or (w.num_pages * 2 * w.num_kv_heads * w.page_size * w.head_dim
+                              * w.elem_bytes * synth.WORKLOADS[args.workload].num_layers / 1e9)
+        page = w.num_layers * w.num_kv_heads * 2 * w.page_size * w.head_dim * w.elem_bytes
+        w = w.replace(num_pages=int(gb * 1e9 // page))
+    return w
 
 
 def dist_info():
@@ -149,7 +167,7 @@ def run_ours(args, ws, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = synth.WORKLOADS[args.workload]
+    w = workload_for(args)
     peaks = {}
     pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk):
@@ -222,11 +240,38 @@ def run_ours(args, ws, rank, local):
         res["attn_gbs"] = (per_layer_bytes * (L - 1) / (attn_ms * 1e-3) / 1e9) if attn_ms else 0.0
         res["step_bytes"] = per_layer_bytes * L / args.steps
         res["step_gbs"] = per_layer_bytes * L / (step_ms * 1e-3) / 1e9 if step_ms else 0.0
+        res["ceilings"] = measure_ceilings(eng) if label == "growpage" else None
         res["e2e"] = measure_e2e(eng, args.e2e_steps) if (args.e2e_steps and label == "growpage") else None
         eng.pool.sync()
         del eng
         torch.cuda.empty_cache()
         return res
+
+    def measure_ceilings(eng):
+        """Read-only streaming of the same resident K/V through the same grid:
+        paged (the attention kernel's access pattern), sequential TMA, and
+        sequential plain loads; GB/s of bytes moved."""
+        act = eng.active()
+        if eng.cfg.dtype != gpb.GP_DTYPE_BF16 or eng.cfg.head_dim != 128 or not act:
+            return None
+        slots = torch.tensor(act, dtype=torch.int32, device=dev)
+        sink = torch.zeros(4, dtype=torch.int32, device=dev)
+        stream = eng.pool.stream
+        L = w.num_layers
+        out = {}
+        for mode, name in ((0, "paged_tma"), (1, "seq_tma"), (2, "seq_ldg")):
+            eng.pool.kv_read_ceiling(0, L, mode, slots, sink)      # warm
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            eng.pool.kv_read_ceiling(0, L, mode, slots, sink)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            s = sink.cpu().tolist()
+            nbytes = (s[2] & 0xffffffff) + ((s[3] & 0xffffffff) << 32)
+            out[name + "_gbs"] = round(nbytes * L / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        out["bytes_per_launch"] = nbytes
+        return out
 
     def measure_e2e(eng, k):
         """Same metric through the C-ABI with inputs from pinned host memory
@@ -322,6 +367,7 @@ def run_ours(args, ws, rank, local):
             "frac": round(gp_res["step_gbs"] / hbm_peak, 4),
             "frac_of_8tbs": round(gp_res["step_gbs"] / 8000.0, 4),
         },
+        "read_ceilings": gp_res["ceilings"],
         "gpu_launches": int(gp_res["launches"]),
         "clocks": gp_res["clocks"],
         "growpage": {k: gp_res[k] for k in ("boundaries", "grows", "compacts", "denied", "moved",
@@ -383,8 +429,7 @@ def oracle_sample(w, seconds, max_steps=None):
 def run_reference(args, ws, rank):
     if rank != 0:
         return None
-    from demand_paged_kv_gqa_b300 import synth
-    w = synth.WORKLOADS[args.workload]
+    w = workload_for(args)
     per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     # warm-up then K timed samples, each a bounded run of the oracle
     for _ in range(args.warmup):
@@ -423,8 +468,7 @@ def main():
     else:
         line = run_ours(args, ws, rank, local)
         if line is not None and not args.no_cpu_baseline:
-            from demand_paged_kv_gqa_b300 import synth
-            w = synth.WORKLOADS[args.workload]
+            w = workload_for(args)
             v, s, e, cores = oracle_sample(w, args.cpu_seconds)
             line["cpu_baseline"] = {
                 "value": round(v, 4), "unit": "tokens/s", "cores": cores, "kind": "oracle",

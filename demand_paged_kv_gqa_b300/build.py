@@ -11,7 +11,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libgrowpage.so")
-SOURCES = ["gp_host.cu", "gp_attn.cu", "gp_step.cu"]
+SOURCES = ["gp_host.cu", "gp_attn.cu", "gp_attn_mma.cu", "gp_ceiling.cu", "gp_step.cu"]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -23,90 +23,9 @@
 // warps is merged by the warp that finishes its last piece (atomic arrival
 // counter; nobody waits).  Warps never synchronise with each other, so every
 // wait in this kernel is on the warp's own copies.
-#include "gp_internal.cuh"
+#include "gp_attn_common.cuh"
 
 namespace gp {
-
-template <typename T, int D>
-struct Geo {
-  static constexpr int EB = (int)sizeof(T);
-  static constexpr int EPC = 16 / EB;            // elements per 16-byte chunk
-  static constexpr int ROWB = D * EB;            // bytes of one token row
-  static constexpr int VEC = ROWB / (8 * 16);    // 16-byte chunks per lane per row
-  static constexpr int NE = VEC * EPC;           // elements per lane per row
-  static constexpr int BLKB = kBlockTok * ROWB;  // 16 rows
-  static constexpr int STAGEB = 2 * BLKB;        // K block + V block
-  static_assert(VEC == 2 || VEC == 4, "unsupported (dtype, head_dim)");
-};
-
-// Lane slice `sigma` (0..7) holds, of each row, the 16-byte chunks
-// c*8 + sigma, c < VEC.  Chunk c < VEC/2 lies in the first half of the row and
-// chunk c + VEC/2 holds its rotate-half partners, so RoPE is lane-local, and
-// 8 lanes reading one row touch 128 contiguous bytes (no bank conflicts).
-template <class Gm>
-__device__ __forceinline__ int dim_of(int e, int sigma) {
-  return ((e / Gm::EPC) * 8 + sigma) * Gm::EPC + (e % Gm::EPC);
-}
-
-template <typename T, class Gm>
-__device__ __forceinline__ void load_row(const uint8_t* row, int sigma, float (&f)[Gm::NE]) {
-#pragma unroll
-  for (int c = 0; c < Gm::VEC; ++c) {
-    const uint4 w = *reinterpret_cast<const uint4*>(row + (c * 8 + sigma) * 16);
-    if constexpr (sizeof(T) == 2) {
-      f[c * 8 + 0] = bf16lo(w.x); f[c * 8 + 1] = bf16hi(w.x);
-      f[c * 8 + 2] = bf16lo(w.y); f[c * 8 + 3] = bf16hi(w.y);
-      f[c * 8 + 4] = bf16lo(w.z); f[c * 8 + 5] = bf16hi(w.z);
-      f[c * 8 + 6] = bf16lo(w.w); f[c * 8 + 7] = bf16hi(w.w);
-    } else {
-      f[c * 4 + 0] = __uint_as_float(w.x); f[c * 4 + 1] = __uint_as_float(w.y);
-      f[c * 4 + 2] = __uint_as_float(w.z); f[c * 4 + 3] = __uint_as_float(w.w);
-    }
-  }
-}
-
-template <typename T, class Gm>
-__device__ __forceinline__ void store_row(T* row, int sigma, const float (&f)[Gm::NE]) {
-#pragma unroll
-  for (int e = 0; e < Gm::NE; ++e) {
-    const int dd = dim_of<Gm>(e, sigma);
-    if constexpr (sizeof(T) == 2) row[dd] = __float2bfloat16_rn(f[e]);
-    else row[dd] = f[e];
-  }
-}
-
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
-
-struct Cursor {
-  int i, h, blk, nb, slot;
-};
-
-__device__ __forceinline__ int find_req(const int32_t* cum, int n, int64_t x) {
-  // largest i in [0, n) with cum[i] <= x
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if ((int64_t)cum[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-__device__ __forceinline__ void cursor_at(const PoolDev& p, int n, int64_t b, Cursor& c) {
-  const int i = find_req(p.plan_cum, n, b / p.Hk);
-  const int nb = p.plan_nb[i];
-  const int64_t r = b - (int64_t)p.Hk * p.plan_cum[i];
-  c.i = i; c.nb = nb; c.h = (int)(r / nb); c.blk = (int)(r % nb); c.slot = p.plan_slot[i];
-}
-
-__device__ __forceinline__ void cursor_next(const PoolDev& p, Cursor& c) {
-  if (++c.blk == c.nb) {
-    c.blk = 0;
-    if (++c.h == p.Hk) {
-      c.h = 0; ++c.i;
-      c.nb = p.plan_nb[c.i]; c.slot = p.plan_slot[c.i];
-    }
-  }
-}
 
 template <class Gm>
 __device__ __forceinline__ void issue_block(const PoolDev& p, int layer, const Cursor& c,

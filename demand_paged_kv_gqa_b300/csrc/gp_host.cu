@@ -9,13 +9,25 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gp_internal.cuh"
 
 namespace gp {
 cudaError_t launch_attention(const PoolDev& p, int layer, const void* q, const void* k,
                              const void* v, void* out, int grid, cudaStream_t st);
 cudaError_t attention_occupancy(const PoolDev& p, int* blocks);
-cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, cudaStream_t st);
+cudaError_t launch_attention_mma(const PoolDev& p, const CUtensorMap* map, int layer, int n,
+                                 const void* q, const void* k, const void* v, void* out, int grid,
+                                 cudaStream_t st);
+cudaError_t attention_mma_occupancy(const PoolDev& p, int* blocks);
+int mma_warps_per_cta();
+cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count, cudaStream_t st);
+cudaError_t ceiling_setup();
+int ceiling_warps_per_cta();
+cudaError_t launch_kv_read(const PoolDev& p, const CUtensorMap* map, int layer, int mode,
+                           uint32_t* sink, int grid, cudaStream_t st);
 cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st);
 cudaError_t launch_decide(const PoolDev& p, cudaStream_t st);
 cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st);
@@ -31,6 +43,8 @@ cudaError_t launch_release_prefix(const PoolDev& p, int pid, cudaStream_t st);
 }  // namespace gp
 
 struct gp_pool {
+  CUtensorMap kvmap;  // (64-byte aligned type) K/V pages as [rows][d] bf16, 128-byte swizzle
+  bool use_mma = false;           // bf16 pages, head_dim 128: tensor-core kernel
   gp_config cfg;
   gp::PoolDev dev;
   gp_layout lay;
@@ -87,7 +101,9 @@ const char* check_config(const gp_config* c) {
   if (!(c->rope_theta >= 0.0)) return "rope_theta < 0";
   if (c->flags != 0) return "flags must be 0";
   const long long logit_w = (long long)c->max_prefix_len + (long long)c->max_pages_per_req * c->page_size;
-  if (logit_w > (1ll << 30)) return "max_pages_per_req too large";
+  if (logit_w > (1ll << 24)) return "max_prefix_len + max_pages_per_req * page_size > 2^24 tokens";
+  const long long rows = (long long)c->num_pages * c->num_layers * c->num_kv_heads * 2 * c->page_size;
+  if (rows >= (1ll << 31)) return "pool too large: pages x layers x kv heads x 2 x page_size >= 2^31";
   return nullptr;
 }
 
@@ -121,6 +137,9 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   take(R * 8);                                                 // plan_delta
   take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 2) * 4);  // partials
   take(R * Hk * 4);                                            // seg_count
+  take((uint64_t)gp::kMaxWorkersBound * 16);                   // wstart
+  take(R * Hk * 8 * 32 * 16);                                  // frag
+  take(R * Hk * 4 * 4);                                        // sstage
   take(R * L * Hk * P * 2 * 4);                                // moves
   take(R * L * Hk * 4);                                        // moves_n
   l->total = off;
@@ -178,6 +197,9 @@ void fill_dev(gp_pool* p) {
   d.plan_delta = (long long*)take(R * 8);
   d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 2) * 4);
   d.seg_count = (int32_t*)take(R * c.num_kv_heads * 4);
+  d.wstart = (int4*)take((uint64_t)gp::kMaxWorkersBound * 16);
+  d.frag = (uint4*)take(R * c.num_kv_heads * 8 * 32 * 16);
+  d.sstage = (float*)take(R * c.num_kv_heads * 4 * 4);
   d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 2 * 4);
   d.moves_n = (int32_t*)take(R * c.num_layers * c.num_kv_heads * 4);
 }
@@ -278,15 +300,39 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   e = gp::launch_init(p->dev, p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   p->launches += 1;
+  p->use_mma = cfg->dtype == GP_DTYPE_BF16 && cfg->head_dim == 128;
+  if (p->use_mma) {
+    // The pool's K/V pages viewed as one 2-D bf16 tensor [rows][d], rows =
+    // ((page * L + layer) * Hk + head) * 2 * P + kv * P + token; boxes of
+    // 16 rows x 64 columns (128 bytes) land in shared memory 128B-swizzled.
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
+    if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return bail(GP_ERR_CUDA);
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    const cuuint64_t rows = (cuuint64_t)cfg->num_pages * cfg->num_layers * cfg->num_kv_heads * 2 *
+                            cfg->page_size;
+    const cuuint64_t dims[2] = {(cuuint64_t)cfg->head_dim, rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cfg->head_dim * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)gp::kBlockTok};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&p->kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)p->dev.kv, dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return bail(GP_ERR_CUDA);
+    if (gp::ceiling_setup() != cudaSuccess) return bail(GP_ERR_CUDA);
+  }
   int dev = 0, sms = 0, blocks = 0;
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = gp::attention_occupancy(p->dev, &blocks);
+  if (e == cudaSuccess)
+    e = p->use_mma ? gp::attention_mma_occupancy(p->dev, &blocks) : gp::attention_occupancy(p->dev, &blocks);
   if (e != cudaSuccess || sms <= 0 || blocks <= 0) return bail(GP_ERR_CUDA);
+  const int wpc = p->use_mma ? gp::mma_warps_per_cta() : gp::kAttnWarps;
   int grid = sms * blocks;
-  if (grid * gp::kAttnWarps > gp::kMaxWorkersBound) grid = gp::kMaxWorkersBound / gp::kAttnWarps;
+  if (grid * wpc > gp::kMaxWorkersBound) grid = gp::kMaxWorkersBound / wpc;
   p->attn_grid = grid;
-  p->dev.num_workers = grid * gp::kAttnWarps;
+  p->dev.num_workers = grid * wpc;
   p->select_grid = sms * 4;
   p->commit_grid = sms * 4;
   e = cudaStreamSynchronize(p->stream);
@@ -404,15 +450,22 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
   if (n > 0 && (!slots_dev || !q || !k_new || !v_new || !out))
     return fail(pool, GP_ERR_INVALID, "null tensor");
   if (layer == 0) {
-    GP_LAUNCH(pool, gp::launch_plan(pool->dev, n, slots_dev, pool->stream));
+    GP_LAUNCH(pool, gp::launch_plan(pool->dev, n, slots_dev, 1, pool->stream));
     pool->step_n = n;
     pool->step_slots = slots_dev;
   } else if (n != pool->step_n || slots_dev != pool->step_slots) {
     return fail(pool, GP_ERR_INVALID, "every layer of a step must get the same slot list");
   }
-  if (n > 0)
-    GP_LAUNCH(pool, gp::launch_attention(pool->dev, layer, q, k_new, v_new, out, pool->attn_grid,
-                                         pool->stream));
+  if (n > 0) {
+    if (pool->use_mma) {
+      GP_LAUNCH(pool, gp::launch_attention_mma(pool->dev, &pool->kvmap, layer, n, q, k_new, v_new,
+                                               out, pool->attn_grid, pool->stream));
+      pool->launches += 2;  // prep, attention and combine kernels
+    }
+    else
+      GP_LAUNCH(pool, gp::launch_attention(pool->dev, layer, q, k_new, v_new, out, pool->attn_grid,
+                                           pool->stream));
+  }
   pool->next_layer = layer + 1;
   return GP_OK;
 }
@@ -442,6 +495,22 @@ int gp_free(gp_pool* pool, int32_t slot) {
   const int pid = pool->slot_prefix[slot];
   if (pid >= 0) pool->prefix_refs[pid] -= 1;
   pool->slot_prefix[slot] = -1;
+  return GP_OK;
+}
+
+int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mode, int32_t n,
+                       const int32_t* slots_dev, uint32_t* sink_dev) {
+  if (!pool) return GP_ERR_INVALID;
+  if (!pool->use_mma) return fail(pool, GP_ERR_INVALID, "read ceiling needs bf16 pages with head_dim 128");
+  if (pool->next_layer != 0) return fail(pool, GP_ERR_INVALID, "read ceiling inside a step");
+  if (layer0 < 0 || count < 1 || layer0 + count > pool->cfg.num_layers || mode < 0 || mode > 2 ||
+      n < 0 || n > pool->cfg.max_requests || !sink_dev || (n > 0 && !slots_dev))
+    return fail(pool, GP_ERR_INVALID, "bad read-ceiling arguments");
+  GP_LAUNCH(pool, gp::launch_plan(pool->dev, n, slots_dev, 0, pool->stream));
+  const int wpc = gp::ceiling_warps_per_cta();
+  const int grid = (pool->dev.num_workers + wpc - 1) / wpc;
+  for (int l = layer0; l < layer0 + count; ++l)
+    GP_LAUNCH(pool, gp::launch_kv_read(pool->dev, &pool->kvmap, l, mode, sink_dev, grid, pool->stream));
   return GP_OK;
 }
 

@@ -66,6 +66,13 @@ struct PoolDev {
   // scratch: attention split-K
   float* partials;        // [num_workers][2][G][D + 2]
   int32_t* seg_count;     // [max_req][Hk]
+  uint4* frag;            // [max_req][Hk][8][32] bf16 tensor-core operand rows per
+                          // (request, kv head) as held by each lane (prep kernel)
+  float* sstage;          // [max_req][Hk][4] each query head's score against the
+                          // staged token (log2 domain, prep kernel)
+  int4* wstart;           // [kMaxWorkersBound] first block of each attention worker:
+                          // request index, (head << 20) | block, blocks of the
+                          // segment, slot (written by the plan kernel)
   // scratch: compaction moves
   int32_t* moves;         // [max_req][L][Hk][P][2] (dst, src) private slots
   int32_t* moves_n;       // [max_req][L][Hk]

@@ -54,7 +54,9 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
 
 // ---------------------------------------------------------------- plan ---
 
-__global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int32_t* slots) {
+// count == 0: lay out the plan without touching the pool's step counters
+// (used by the read-ceiling measurement between steps).
+__global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int32_t* slots, int count) {
   __shared__ int s_warp[33];
   __shared__ int s_bad;
   __shared__ unsigned long long s_tok, s_btok;
@@ -106,16 +108,38 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
     bcarry += btot;
   }
   __syncthreads();
+  // Start cursor of every attention worker: worker w of Weff = min(workers,
+  // total blocks) takes blocks [w*Tb/Weff, (w+1)*Tb/Weff) of the sequence
+  // (request i, head h, block b) laid out request-major, then head, then block.
+  if (!s_bad && n > 0) {
+    const long long Tb = (long long)carry * p.Hk;
+    const long long W = p.num_workers;
+    const long long Weff = W < Tb ? W : Tb;
+    for (int w = threadIdx.x; w < Weff; w += blockDim.x) {
+      const long long b = ((long long)w * Tb) / Weff;
+      const long long x = b / p.Hk;  // largest i with cum[i] <= b / Hk
+      int lo = 0, hi = n - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)p.plan_cum[mid] <= x) lo = mid; else hi = mid - 1;
+      }
+      const int nb = p.plan_nb[lo];
+      const long long r = b - (long long)p.Hk * p.plan_cum[lo];
+      p.wstart[w] = make_int4(lo, (int)((r / nb) << 20) | (int)(r % nb), nb, p.plan_slot[lo]);
+    }
+  }
   if (threadIdx.x == 0) {
     p.plan_cum[n] = carry;
     const int good = s_bad ? 0 : n;
     p.plan_misc[0] = good;
     p.plan_misc[1] = s_bad ? 0 : bcarry;
     p.plan_misc[2] = carry;
-    p.ctrl->plan_n = good;
-    p.ctrl->steps += 1;
-    p.ctrl->tokens_attended += (long long)s_tok;
-    p.ctrl->boundary_tokens += (long long)s_btok;
+    if (count) {
+      p.ctrl->plan_n = good;
+      p.ctrl->steps += 1;
+      p.ctrl->tokens_attended += (long long)s_tok;
+      p.ctrl->boundary_tokens += (long long)s_btok;
+    }
   }
 }
 
@@ -704,8 +728,8 @@ __global__ void release_prefix_kernel(PoolDev p, int pid) {
 
 // ------------------------------------------------------------ launchers ---
 
-cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(p, n, slots);
+cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count, cudaStream_t st) {
+  plan_kernel<<<1, 1024, 0, st>>>(p, n, slots, count);
   return cudaGetLastError();
 }
 cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st) {

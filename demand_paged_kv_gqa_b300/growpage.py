@@ -14,7 +14,9 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libgrowpage.so")
+# GROWPAGE_LIB may name another build of the same library (e.g. a variant
+# compiled with different tile constants); the default is the in-tree build.
+LIB_PATH = os.environ.get("GROWPAGE_LIB") or os.path.join(_HERE, "libgrowpage.so")
 
 GP_OK, GP_ERR_INVALID, GP_ERR_NO_PAGES, GP_ERR_CUDA, GP_ERR_DEVICE = 0, 1, 2, 3, 4
 GP_DTYPE_F32, GP_DTYPE_BF16 = 0, 1
@@ -84,6 +86,7 @@ def _load():
         "gp_get_stats": (ctypes.c_int, [P, ctypes.POINTER(gp_ctrl)]),
         "gp_get_request": (ctypes.c_int, [P, I32, ctypes.POINTER(gp_req_meta),
                                           ctypes.POINTER(I32), I32]),
+        "gp_kv_read_ceiling": (ctypes.c_int, [P, I32, I32, I32, I32, P, P]),
         "gp_last_error": (ctypes.c_char_p, [P]),
         "gp_launch_count": (I64, [P]),
     }
@@ -211,6 +214,12 @@ class Pool:
         bt = (ctypes.c_int32 * w)()
         self._check(lib.gp_get_request(self.h, slot, ctypes.byref(m), bt, w))
         return m, list(bt)[: m.n_pre_pages + m.n_pages]
+
+    def kv_read_ceiling(self, layer0: int, count: int, mode: int, slots: torch.Tensor,
+                        sink: torch.Tensor):
+        """Read-only streaming of layers' resident K/V (a bandwidth ceiling)."""
+        self._check(lib.gp_kv_read_ceiling(self.h, layer0, count, mode, slots.numel(),
+                                           _ptr(slots), _ptr(sink)))
 
     def launch_count(self) -> int:
         return int(lib.gp_launch_count(self.h))

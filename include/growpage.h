@@ -250,6 +250,22 @@ int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev);
  * prefix whose last reference goes is pushed too.  Asynchronous. */
 int gp_free(gp_pool* pool, int32_t slot);
 
+/* Measurement, not part of the decode path: for each layer in
+ * [layer0, layer0 + count), one launch that reads every resident K/V block of
+ * that layer for the n requests in slots_dev (same list rules as
+ * gp_decode_step) through the same persistent grid, per-warp split and
+ * tensor-map copies as the bf16 attention kernel, with no arithmetic.  It
+ * gives the bandwidth ceiling of that access pattern.  mode 0: the requests'
+ * own pages (the attention kernel's pattern); mode 1: the same number of
+ * 8 KiB blocks in address order (tensor-map copies); mode 2: the same bytes
+ * in address order with plain 16-byte loads.  sink_dev: device uint32[4],
+ * caller-owned; [0] receives an XOR checksum of the data, [2..3] the bytes
+ * one launch moved (uint64, little-endian).  Only for bf16 pages with
+ * head_dim 128 (GP_ERR_INVALID otherwise) and between steps.  Leaves the
+ * pool's state and counters unchanged.  Asynchronous. */
+int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mode, int32_t n,
+                       const int32_t* slots_dev, uint32_t* sink_dev);
+
 /* Wait for the stream; GP_ERR_DEVICE if the device status word is set.
  * SYNC. */
 int gp_sync(gp_pool* pool);
