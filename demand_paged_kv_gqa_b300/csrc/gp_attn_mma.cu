@@ -29,6 +29,10 @@
 // a stage with four 2-D tensor-map copies (TMA, 128-byte swizzle: K and V,
 // two 64-column halves each) that complete on the stage's mbarrier.  The
 // swizzle makes the ldmatrix reads of both operands bank-conflict free.
+// Ahead of every piece, the same ring carries a "meta"
+// item (bulk copies of the query rows, the new key and value, the summaries
+// and the rotary rows), so building a piece's operands never waits on a
+// dependent global load.
 // Work is split over a persistent grid as in the fp32 kernel (equal ranges
 // of blocks per warp; a cut (request, head) is merged by the warp that
 // finishes its last piece).  Every wait is bounded and on the warp's own
@@ -125,224 +129,242 @@ __device__ __forceinline__ void issue_block_tma(const PoolDev& p, const CUtensor
   tma_load_2d(stage + 6144, map, 64, row + p.P, bar);
 }
 
-// Summary fold (fp32, exact order): s' = fl(fl(b*s) + fl((1-b)*qbar)), or
-// qbar on the request's first step; qbar = (sum of the G heads in order)/G.
+// ------------------------------------------------------------ meta items ---
+//
+// Besides K/V blocks, a warp's ring carries one "meta" item in front of each
+// piece: what the piece needs besides the keys, copied by the bulk-copy
+// engine with the blocks.  Offsets inside a stage:
+constexpr int kMetaQ = 0;       // the G query rows, bf16 (<= 1024 B)
+constexpr int kMetaK = 1024;    // the step's new key, bf16
+constexpr int kMetaV = 1280;    // the step's new value, bf16
+constexpr int kMetaS = 1536;    // short and long summary before this step, fp32
+constexpr int kMetaC32 = 2560;  // rotary cos / sin rows of the position, fp32
+constexpr int kMetaS32 = 2816;
+constexpr int kMetaC64 = 3072;  // the same rows in fp64
+constexpr int kMetaS64 = 3584;
+
+// Per-warp extra buffer (after ob): the staged-token score of each query
+// head and the staged value (fp32), for finishing a piece in place.
+constexpr int kObxFloats = 4 + kMmaD;
+constexpr int kWarpBufFloats = ((kObFloats + kObxFloats + 3) / 4) * 4;
+
+// The step's plan entries of 32 consecutive requests, one per lane, so that a
+// cursor crossing into the next request reads registers, not memory.
+struct PlanWin {
+  int base = -(1 << 30);
+  int nb = 1, slot = 0, R = 0, flags = 0, pos = 0;
+};
+struct PlanEntry {
+  int nb, slot, R, flags, pos;
+};
+
+__device__ __forceinline__ PlanEntry plan_at(const PoolDev& p, PlanWin& w, int i, int n, int lane) {
+  if (i < w.base || i >= w.base + 32) {  // warp-uniform
+    w.base = i;
+    const int k = i + lane;
+    if (k < n) {
+      w.nb = p.plan_nb[k]; w.slot = p.plan_slot[k]; w.R = p.plan_R[k];
+      w.flags = p.plan_flags[k]; w.pos = p.plan_pos[k];
+    } else {
+      w.nb = 1; w.slot = 0; w.R = 0; w.flags = 0; w.pos = 0;
+    }
+  }
+  const int src = i - w.base;
+  PlanEntry e;
+  e.nb = __shfl_sync(0xffffffffu, w.nb, src);
+  e.slot = __shfl_sync(0xffffffffu, w.slot, src);
+  e.R = __shfl_sync(0xffffffffu, w.R, src);
+  e.flags = __shfl_sync(0xffffffffu, w.flags, src);
+  e.pos = __shfl_sync(0xffffffffu, w.pos, src);
+  return e;
+}
+
+__device__ __forceinline__ void walk_next(const PoolDev& p, PlanWin& w, Cursor& c, int n, int lane) {
+  if (++c.blk == c.nb) {
+    c.blk = 0;
+    if (++c.h == p.Hk) {
+      c.h = 0;
+      if (++c.i < n) {
+        const PlanEntry e = plan_at(p, w, c.i, n, lane);
+        c.nb = e.nb;
+        c.slot = e.slot;
+      }
+    }
+  }
+}
+
 template <int G>
-__device__ __forceinline__ float fold_summary(const __nv_bfloat16* qrow0, int dim, const float* srowp,
-                                              int X, float beta, int first) {
-  float qb = __bfloat162float(qrow0[dim]);
+__device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, int h, int slot,
+                                           int pos, const __nv_bfloat16* q,
+                                           const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
+                                           uint8_t* st, uint64_t* bar) {
+  constexpr int D = kMmaD;
+  const uint32_t bytes = G * D * 2 + 2 * D * 2 + 2 * D * 4 + (p.rope ? D * 4 + D * 8 : 0);
+  mbar_expect_tx(bar, bytes);
+  bulk_g2s(st + kMetaQ, q + ((size_t)i * p.Hq + h * G) * D, G * D * 2, bar);
+  bulk_g2s(st + kMetaK, knew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
+  bulk_g2s(st + kMetaV, vnew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
+  bulk_g2s(st + kMetaS, p.summary + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * D, 2 * D * 4, bar);
+  if (p.rope) {
+    bulk_g2s(st + kMetaC32, p.cos32 + (size_t)pos * (D / 2), D * 2, bar);
+    bulk_g2s(st + kMetaS32, p.sin32 + (size_t)pos * (D / 2), D * 2, bar);
+    bulk_g2s(st + kMetaC64, p.cos64 + (size_t)pos * (D / 2), D * 4, bar);
+    bulk_g2s(st + kMetaS64, p.sin64 + (size_t)pos * (D / 2), D * 4, bar);
+  }
+}
+
+// Pointers to what a piece needs (a meta item in shared memory).
+struct PieceIn {
+  const __nv_bfloat16* q;  // [G][d]
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* s;          // [2][d] before this step
+  const float* c32;
+  const float* s32;
+  const double* c64;
+  const double* s64;
+};
+
+// fp32 fold of the step's query mean into summary X at dim di (exact order):
+// q̄ = (sum of the G heads in head order) / G; s' = fl(fl(b*s) + fl((1-b)*q̄)),
+// or q̄ on the request's first step.
+template <int G>
+__device__ __forceinline__ float fold_at(const PieceIn& in, int X, int di, float beta, int first) {
+  float qb = __bfloat162float(in.q[di]);
 #pragma unroll
-  for (int g = 1; g < G; ++g) qb = __fadd_rn(qb, __bfloat162float(qrow0[g * kMmaD + dim]));
+  for (int g = 1; g < G; ++g) qb = __fadd_rn(qb, __bfloat162float(in.q[g * kMmaD + di]));
   const float qm = __fdiv_rn(qb, (float)G);
   if (first) return qm;
-  const float a = __fsub_rn(1.0f, beta);
-  return __fadd_rn(__fmul_rn(beta, srowp[X * kMmaD + dim]), __fmul_rn(a, qm));
+  return __fadd_rn(__fmul_rn(beta, in.s[X * kMmaD + di]), __fmul_rn(__fsub_rn(1.0f, beta), qm));
 }
 
-// ---------------------------------------------------------------- prep ---
-//
-// One warp per (request i of the step, kv head h), before the attention
-// launch of the layer.  Everything here depends on the step's inputs only,
-// not on the resident keys, so it is kept off the streaming warps:
-//   1. the tensor-core operand rows of the attention kernel, laid out as the
-//      registers of lane (g = lane / 4, t = lane % 4) will hold them: rows
-//      g < G = query head g rotated to the current position, scaled by
-//      log2(e)/sqrt(d), bf16 hi (row g) + lo (row g+8); at a boundary, rows
-//      4/5 = short/long summary (after this step's fold) rotated and scaled
-//      by 1/sqrt(d), hi (rows 4/5) + mid (rows 12/13), lo in rows 6/7;
-//   2. the staged token: key rotated in fp64 and rounded once to bf16, value
-//      copied; and each query head's score against it;
-//   3. the fold of the step's query mean into both summaries.
-// Operands are written to scratch ([i][h][kk][lane] as 16-byte words).
-// bf16 pair at element `di` (even) of a row, as two floats.
-__device__ __forceinline__ float2 ld_bf2(const __nv_bfloat16* row, int di) {
-  const uint32_t w = *reinterpret_cast<const uint32_t*>(row + di);
-  return make_float2(bf16lo(w), bf16hi(w));
-}
-
+// The tensor-core operand rows of lane (g = lane / 4, t = lane % 4): rows
+// g < G = query head g rotated to the position and scaled by log2(e)/sqrt(d),
+// bf16 hi (row g) + lo (row g+8); at a boundary rows 4/5 = short/long summary
+// after this step's fold, rotated and scaled by 1/sqrt(d), hi (rows 4/5) +
+// mid (rows 12/13) with the lo parts in rows 6/7.  Other rows are zero.
 template <int G>
-__global__ void __launch_bounds__(kSmallWarps * 32)
-prep_kernel(PoolDev p, int layer, const __nv_bfloat16* __restrict__ q,
-            const __nv_bfloat16* __restrict__ knew, const __nv_bfloat16* __restrict__ vnew) {
+__device__ __forceinline__ void build_rows(const PoolDev& p, const PieceIn& in, int flags, int lane,
+                                           uint32_t (&afr)[8][4]) {
+  constexpr int D = kMmaD;
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) afr[kk][0] = afr[kk][1] = afr[kk][2] = afr[kk][3] = 0u;
+  const bool head_row = g < G;
+  const bool sum_row = (flags & kPlanScore) && g >= 4;
+  if (!(head_row || sum_row)) return;
+  const int X = g & 1, first = flags & kPlanFirst;
+  const float beta = X ? p.beta_l : p.beta_s;
+  const float sc = head_row ? 1.4426950408889634f / sqrtf((float)D)   // log2(e)/sqrt(d)
+                            : 1.0f / sqrtf((float)D);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // dims 16kk+2t+8*half, +1
+      float x[2], y[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int di = 16 * kk + 2 * t + 8 * half + u;  // < 64; partner di + 64
+        float a, b;
+        if (head_row) {
+          a = __bfloat162float(in.q[g * D + di]);
+          b = __bfloat162float(in.q[g * D + di + 64]);
+        } else {
+          a = fold_at<G>(in, X, di, beta, first);
+          b = fold_at<G>(in, X, di + 64, beta, first);
+        }
+        if (p.rope) {
+          const float c = in.c32[di], s = in.s32[di];
+          const float xa = a * c - b * s;
+          const float yb = b * c + a * s;
+          a = xa;
+          b = yb;
+        }
+        x[u] = a * sc;
+        y[u] = b * sc;
+      }
+      // registers: [0] row g, cols 2t..; [1] row g+8; [2] row g, cols 2t+8..; [3] row g+8
+      uint32_t xh[2], xl[2], yh[2], yl[2];
+      if (head_row) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          split2(x[u], xh[u], xl[u]);
+          split2(y[u], yh[u], yl[u]);
+        }
+      } else {
+        uint32_t xm[2], ym[2], xlo[2], ylo[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          split3(x[u], xh[u], xm[u], xlo[u]);
+          split3(y[u], yh[u], ym[u], ylo[u]);
+        }
+        if (g >= 6) {  // rows 6/7 carry the lo parts; rows 14/15 stay zero
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            xh[u] = xlo[u]; yh[u] = ylo[u]; xl[u] = 0u; yl[u] = 0u;
+          }
+        } else {  // rows 4/5 hi, rows 12/13 mid
+#pragma unroll
+          for (int u = 0; u < 2; ++u) { xl[u] = xm[u]; yl[u] = ym[u]; }
+        }
+      }
+      afr[kk][2 * half + 0] = pack2(xh[0], xh[1]);
+      afr[kk][2 * half + 1] = pack2(xl[0], xl[1]);
+      afr[kk + 4][2 * half + 0] = pack2(yh[0], yh[1]);
+      afr[kk + 4][2 * half + 1] = pack2(yl[0], yl[1]);
+    }
+  }
+}
+
+// Once per (request, kv head) and step, by the piece holding its first block:
+//   the staged token (key rotated in fp64 and rounded once to bf16, value)
+//   into the staging rows; each query head's score against it (log2 domain)
+//   into sstage and obx[g]; the staged value into obx[4..]; and both folded
+//   summaries into the next-summary rows (copied over the summaries by the
+//   commit kernel once every layer has been read).
+template <int G>
+__device__ void segment_duties(const PoolDev& p, int layer, int i, int h, int slot, int flags,
+                               const PieceIn& in, float* obx, int lane) {
   using Gm = Geo<__nv_bfloat16, kMmaD>;
   constexpr int D = kMmaD, NE = Gm::NE, H2 = NE / 2;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = p.plan_misc[0];
-  const int gw = blockIdx.x * kSmallWarps + warp;
-  if (gw >= n * p.Hk) return;
-  const int i = gw / p.Hk, h = gw % p.Hk;
-  const int slot = p.plan_slot[i], flags = p.plan_flags[i];
-  const int pos = p.req[slot].pos;
-  const int first = flags & kPlanFirst;
-  const bool score = (flags & kPlanScore) != 0;
+  const int sigma = lane & 7, grp = lane >> 3;
   const size_t srow = (((size_t)slot * p.L + layer) * p.Hk + h) * 2;
-  float* srowp = p.summary + srow * D;
-  const int g = lane >> 2, t = lane & 3;         // operand-row layout
-  const int sigma = lane & 7, grp = lane >> 3;   // 8 lanes per row layout
-  const bool head_row = g < G;
-  const bool sum_row = score && g >= 4;
-  const int X = g & 1;
-  // ---- loads of what was final before this step began (plan, positions,
-  // rotary tables, this layer's summaries), while the previous kernel in the
-  // stream may still run.  fd(j): operand dim 16*(j/4) + 2t + 8*((j/2)%2) + j%2.
-  float rc[16], rs[16];              // fp32 rotation at the 16 operand dims
-  float so[16], so2[16];             // old summary X at the operand dims, +64
-  double c64[H2], s64[H2];           // fp64 rotation at this lane's row dims
-  float c32r[H2], s32r[H2];          // fp32 rotation at this lane's row dims
-  float fs[4], fl[4];                // old summaries at dims 4*lane + e
+  float vraw[NE], kst[NE];
+  load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(in.k), sigma, kst);
+  load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(in.v), sigma, vraw);
+  if (p.rope) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int di = 16 * (j / 4) + 2 * t + 8 * ((j / 2) % 2) + (j % 2);
-    rc[j] = p.rope ? p.cos32[(size_t)pos * (D / 2) + di] : 1.f;
-    rs[j] = p.rope ? p.sin32[(size_t)pos * (D / 2) + di] : 0.f;
-    so[j] = sum_row ? srowp[X * D + di] : 0.f;
-    so2[j] = sum_row ? srowp[X * D + di + 64] : 0.f;
+    for (int e = 0; e < H2; ++e) {
+      const int di = dim_of<Gm>(e, sigma);
+      const double c = in.c64[di], s = in.s64[di];
+      const double x = (double)kst[e], y = (double)kst[e + H2];
+      const double ra = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, s));
+      const double rb = __dadd_rn(__dmul_rn(y, c), __dmul_rn(x, s));
+      kst[e] = __uint_as_float((uint32_t)f64_to_bf16_rne(ra) << 16);
+      kst[e + H2] = __uint_as_float((uint32_t)f64_to_bf16_rne(rb) << 16);
+    }
   }
+  if (grp == 0) {
+    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(p.staging) + srow * D;
+    store_row<__nv_bfloat16, Gm>(st, sigma, kst);  // exact: already on the bf16 grid
+    store_row<__nv_bfloat16, Gm>(st + D, sigma, vraw);
 #pragma unroll
-  for (int e = 0; e < H2; ++e) {
-    const int di = dim_of<Gm>(e, sigma);
-    c64[e] = p.rope ? p.cos64[(size_t)pos * (D / 2) + di] : 1.0;
-    s64[e] = p.rope ? p.sin64[(size_t)pos * (D / 2) + di] : 0.0;
-    c32r[e] = p.rope ? p.cos32[(size_t)pos * (D / 2) + di] : 1.f;
-    s32r[e] = p.rope ? p.sin32[(size_t)pos * (D / 2) + di] : 0.f;
+    for (int e = 0; e < NE; ++e) obx[4 + dim_of<Gm>(e, sigma)] = vraw[e];
   }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    fs[e] = srowp[lane * 4 + e];
-    fl[e] = srowp[D + lane * 4 + e];
-  }
-  // ---- the step's inputs may come from the previous kernel
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const __nv_bfloat16* q0 = q + ((size_t)i * p.Hq + h * G) * D;
-  const float bX = X ? p.beta_l : p.beta_s, aX = __fsub_rn(1.0f, bX);
-
-  // ---- 1. operand rows
   {
-    const float qscale = 1.4426950408889634f / sqrtf((float)D);  // log2(e)/sqrt(d)
-    const float sscale = 1.0f / sqrtf((float)D);
-    float a[16], b[16];
-    if (head_row) {
-#pragma unroll
-      for (int j = 0; j < 16; j += 2) {
-        const int di = 16 * (j / 4) + 2 * t + 8 * ((j / 2) % 2);
-        const float2 lo = ld_bf2(q0 + g * D, di), hi = ld_bf2(q0 + g * D, di + 64);
-        a[j] = lo.x; a[j + 1] = lo.y; b[j] = hi.x; b[j + 1] = hi.y;
-      }
-    } else if (sum_row) {
-      float qa[16], qb[16];   // head-order sums of the G heads at the operand dims
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-#pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const int di = 16 * (j / 4) + 2 * t + 8 * ((j / 2) % 2);
-          const float2 lo = ld_bf2(q0 + gg * D, di), hi = ld_bf2(q0 + gg * D, di + 64);
-          if (gg == 0) {
-            qa[j] = lo.x; qa[j + 1] = lo.y; qb[j] = hi.x; qb[j + 1] = hi.y;
-          } else {
-            qa[j] = __fadd_rn(qa[j], lo.x); qa[j + 1] = __fadd_rn(qa[j + 1], lo.y);
-            qb[j] = __fadd_rn(qb[j], hi.x); qb[j + 1] = __fadd_rn(qb[j + 1], hi.y);
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {   // the fold, as in step 3
-        const float ma = __fdiv_rn(qa[j], (float)G), mb = __fdiv_rn(qb[j], (float)G);
-        a[j] = first ? ma : __fadd_rn(__fmul_rn(bX, so[j]), __fmul_rn(aX, ma));
-        b[j] = first ? mb : __fadd_rn(__fmul_rn(bX, so2[j]), __fmul_rn(aX, mb));
-      }
-    }
-    uint32_t afr[8][4];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) afr[kk][0] = afr[kk][1] = afr[kk][2] = afr[kk][3] = 0u;
-    if (head_row || sum_row) {
-      const float sc = head_row ? qscale : sscale;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (p.rope) {
-          const float xa = a[j] * rc[j] - b[j] * rs[j];
-          const float yb = b[j] * rc[j] + a[j] * rs[j];
-          a[j] = xa;
-          b[j] = yb;
-        }
-        a[j] *= sc;
-        b[j] *= sc;
-      }
-#pragma unroll
-      for (int j = 0; j < 16; j += 2) {
-        const int kk = j / 4, half = (j / 2) % 2;
-        // registers: [0] row g, cols 2t..; [1] row g+8; [2] row g, cols 2t+8..; [3] row g+8
-        uint32_t xh[2], xl[2], yh[2], yl[2];
-        if (head_row) {
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            split2(a[j + u], xh[u], xl[u]);
-            split2(b[j + u], yh[u], yl[u]);
-          }
-        } else {
-          uint32_t xm[2], ym[2], xlo[2], ylo[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            split3(a[j + u], xh[u], xm[u], xlo[u]);
-            split3(b[j + u], yh[u], ym[u], ylo[u]);
-          }
-          if (g >= 6) {  // rows 6/7 carry the lo parts; rows 14/15 stay zero
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              xh[u] = xlo[u]; yh[u] = ylo[u]; xl[u] = 0u; yl[u] = 0u;
-            }
-          } else {  // rows 4/5 hi, rows 12/13 mid
-#pragma unroll
-            for (int u = 0; u < 2; ++u) { xl[u] = xm[u]; yl[u] = ym[u]; }
-          }
-        }
-        afr[kk][2 * half + 0] = pack2(xh[0], xh[1]);
-        afr[kk][2 * half + 1] = pack2(xl[0], xl[1]);
-        afr[kk + 4][2 * half + 0] = pack2(yh[0], yh[1]);
-        afr[kk + 4][2 * half + 1] = pack2(yl[0], yl[1]);
-      }
-    }
-    uint4* fr = p.frag + (size_t)gw * 8 * 32;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk)
-      fr[kk * 32 + lane] = make_uint4(afr[kk][0], afr[kk][1], afr[kk][2], afr[kk][3]);
-  }
-
-  // ---- 2. staged token and the query heads' scores against it
-  {
-    float vraw[NE], kst[NE];
-    load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(knew + ((size_t)i * p.Hk + h) * D),
-                                sigma, kst);
-    load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(vnew + ((size_t)i * p.Hk + h) * D),
-                                sigma, vraw);
-    float qr[NE];
-    if (grp < G)
-      load_row<__nv_bfloat16, Gm>(
-          reinterpret_cast<const uint8_t*>(q0 + (size_t)grp * D), sigma, qr);
-    if (p.rope) {
-#pragma unroll
-      for (int e = 0; e < H2; ++e) {
-        const double x = (double)kst[e], y = (double)kst[e + H2];
-        const double ra = __dsub_rn(__dmul_rn(x, c64[e]), __dmul_rn(y, s64[e]));
-        const double rb = __dadd_rn(__dmul_rn(y, c64[e]), __dmul_rn(x, s64[e]));
-        kst[e] = __uint_as_float((uint32_t)f64_to_bf16_rne(ra) << 16);
-        kst[e + H2] = __uint_as_float((uint32_t)f64_to_bf16_rne(rb) << 16);
-      }
-    }
-    if (grp == 0) {
-      __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(p.staging) + srow * D;
-      store_row<__nv_bfloat16, Gm>(st, sigma, kst);  // exact: already on the bf16 grid
-      store_row<__nv_bfloat16, Gm>(st + D, sigma, vraw);
-    }
     const float qscale = 1.4426950408889634f / sqrtf((float)D);
     float sa = 0.f;
     if (grp < G) {  // one query head per 8-lane group
+      float qr[NE];
+      load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(in.q + grp * D), sigma, qr);
       if (p.rope) {
 #pragma unroll
         for (int e = 0; e < H2; ++e) {
+          const int di = dim_of<Gm>(e, sigma);
+          const float c = in.c32[di], s = in.s32[di];
           const float x = qr[e], y = qr[e + H2];
-          qr[e] = x * c32r[e] - y * s32r[e];
-          qr[e + H2] = y * c32r[e] + x * s32r[e];
+          qr[e] = x * c - y * s;
+          qr[e + H2] = y * c + x * s;
         }
       }
 #pragma unroll
@@ -351,53 +373,33 @@ prep_kernel(PoolDev p, int layer, const __nv_bfloat16* __restrict__ q,
     sa += __shfl_xor_sync(0xffffffffu, sa, 1);
     sa += __shfl_xor_sync(0xffffffffu, sa, 2);
     sa += __shfl_xor_sync(0xffffffffu, sa, 4);
-    if (grp < G && sigma == 0) p.sstage[gw * 4 + grp] = sa;
+    if (grp < G && sigma == 0) {
+      p.sstage[(i * p.Hk + h) * 4 + grp] = sa;
+      obx[grp] = sa;
+    }
   }
-
-  // ---- 3. summaries: 4 dims per lane (old values were read before the wait)
-  {
-    const float aS = __fsub_rn(1.0f, p.beta_s), aL = __fsub_rn(1.0f, p.beta_l);
-    float qs[4];
-    {
-      const uint2 w0 = *reinterpret_cast<const uint2*>(q0 + lane * 4);
-      qs[0] = bf16lo(w0.x); qs[1] = bf16hi(w0.x); qs[2] = bf16lo(w0.y); qs[3] = bf16hi(w0.y);
-    }
+  const int first = flags & kPlanFirst;
+  float* nxt = p.summary_next + srow * D;
 #pragma unroll
-    for (int gg = 1; gg < G; ++gg) {
-      const uint2 w1 = *reinterpret_cast<const uint2*>(q0 + gg * D + lane * 4);
-      qs[0] = __fadd_rn(qs[0], bf16lo(w1.x)); qs[1] = __fadd_rn(qs[1], bf16hi(w1.x));
-      qs[2] = __fadd_rn(qs[2], bf16lo(w1.y)); qs[3] = __fadd_rn(qs[3], bf16hi(w1.y));
-    }
-    float4 ns, nl;
-    float* nsp = &ns.x;
-    float* nlp = &nl.x;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float qm = __fdiv_rn(qs[e], (float)G);
-      nsp[e] = first ? qm : __fadd_rn(__fmul_rn(p.beta_s, fs[e]), __fmul_rn(aS, qm));
-      nlp[e] = first ? qm : __fadd_rn(__fmul_rn(p.beta_l, fl[e]), __fmul_rn(aL, qm));
-    }
-    *reinterpret_cast<float4*>(srowp + lane * 4) = ns;
-    *reinterpret_cast<float4*>(srowp + D + lane * 4) = nl;
+  for (int e = 0; e < 4; ++e) {
+    const int di = lane * 4 + e;
+    nxt[di] = fold_at<G>(in, 0, di, p.beta_s, first);
+    nxt[D + di] = fold_at<G>(in, 1, di, p.beta_l, first);
   }
 }
 
-// Output of one (request, kv head) from the merged attention state in the
-// warp's buffer ob ([G][D] unnormalised output, then m[G] in the log2
-// domain, l[G]): the staged token (value from the staging rows, score from
-// the prep kernel) is merged in and the rows are normalised and stored.
+// Output of one (request, kv head) from the attention state in the warp's
+// buffer ob ([G][D] unnormalised output, then m[G] in the log2 domain, l[G])
+// and the staged token in obx: merged, normalised, stored (16-byte stores).
 template <int G>
-__device__ __forceinline__ void finish_mma(const PoolDev& p, int layer, int i, int h, int slot,
+__device__ __forceinline__ void finish_mma(const PoolDev& p, int i, int h,
                                            __nv_bfloat16* __restrict__ out, const float* ob,
-                                           int lane) {
+                                           const float* obx, int lane) {
   using Gm = Geo<__nv_bfloat16, kMmaD>;
-  constexpr int D = kMmaD, NE = Gm::NE;
+  constexpr int D = kMmaD;
   const int sigma = lane & 7, g = lane >> 3;  // one query head per 8-lane group
   if (g >= G) return;
-  const size_t srow = (((size_t)slot * p.L + layer) * p.Hk + h) * 2;
-  float vraw[NE];
-  load_row<__nv_bfloat16, Gm>(p.staging + (srow + 1) * D * sizeof(__nv_bfloat16), sigma, vraw);
-  const float a = p.sstage[(i * p.Hk + h) * 4 + g];
+  const float a = obx[g];
   const float mg = ob[G * D + g], lg = ob[G * D + G + g];
   const float mn = fmaxf(mg, a);
   const float al = (mg == -INFINITY) ? 0.f : exp2f(mg - mn);
@@ -409,9 +411,9 @@ __device__ __forceinline__ void finish_mma(const PoolDev& p, int layer, int i, i
     uint32_t wv[4];
 #pragma unroll
     for (int k2 = 0; k2 < 4; ++k2) {
-      const int e0 = c * 8 + 2 * k2;
-      const float r0 = (ob[g * D + dim_of<Gm>(e0, sigma)] * al + be * vraw[e0]) * inv;
-      const float r1 = (ob[g * D + dim_of<Gm>(e0 + 1, sigma)] * al + be * vraw[e0 + 1]) * inv;
+      const int d0 = dim_of<Gm>(c * 8 + 2 * k2, sigma);
+      const float r0 = (ob[g * D + d0] * al + be * obx[4 + d0]) * inv;
+      const float r1 = (ob[g * D + d0 + 1] * al + be * obx[4 + d0 + 1]) * inv;
       const __nv_bfloat162 pr = __floats2bfloat162_rn(r0, r1);
       wv[k2] = *reinterpret_cast<const uint32_t*>(&pr);
     }
@@ -419,10 +421,12 @@ __device__ __forceinline__ void finish_mma(const PoolDev& p, int layer, int i, i
   }
 }
 
+// ----------------------------------------------------------- attention ---
 template <int G, int S>
 __global__ void __launch_bounds__(kMmaWarps * 32)
 attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
-                __nv_bfloat16* __restrict__ out) {
+                const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ knew,
+                const __nv_bfloat16* __restrict__ vnew, __nv_bfloat16* __restrict__ out) {
   static_assert(G == 1 || G == 2 || G == 4, "G");
   constexpr int D = kMmaD;
   extern __shared__ uint8_t smem_raw[];
@@ -431,9 +435,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   uint8_t* ring = smem + (size_t)warp * S * kMmaStageB;
-  float* ob = reinterpret_cast<float*>(smem + (size_t)kMmaWarps * S * kMmaStageB) + warp * kObFloats;
+  float* ob = reinterpret_cast<float*>(smem + (size_t)kMmaWarps * S * kMmaStageB) + warp * kWarpBufFloats;
+  float* obx = ob + kObFloats;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kMmaWarps * S * kMmaStageB +
-                                               (size_t)kMmaWarps * kObFloats * 4) + warp * S;
+                                               (size_t)kMmaWarps * kWarpBufFloats * 4) + warp * S;
 
   const int n = p.plan_misc[0];
   const int64_t Tb = (int64_t)p.plan_misc[2] * p.Hk;
@@ -454,22 +459,53 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   }
   __syncwarp();
 
+  // ---- the warp's item sequence: the blocks of its range, with a meta item
+  // in front of every piece.  Item c lives in stage c % S.  Producer state:
   Cursor pc;
   cursor_start(p, w, pc);
+  PlanWin pwin, cwin;
   PageWin win;
   const int first_seg = pc.i * p.Hk + pc.h;
-  {
-    int64_t b = start;
-    for (int s = 0; s < S && b < end; ++s, ++b) {
+  const int i_first = pc.i, h_first = pc.h;
+  int64_t pblk = start;   // next block to issue
+  bool pmeta = false;     // next item is a meta item
+  int64_t pitems = 1;     // items issued (item 0, the first meta, comes after the wait)
+  auto emit = [&](bool allow_meta) -> bool {
+    if (pblk >= end && !pmeta) return false;
+    if (pmeta && !allow_meta) return false;
+    const int s = (int)(pitems % S);
+    uint8_t* st = ring + s * kMmaStageB;
+    if (pmeta) {
+      const PlanEntry e = plan_at(p, pwin, pc.i, n, lane);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue_meta<G>(p, layer, pc.i, pc.h, e.slot, e.pos, q, knew, vnew, st, &bars[s]);
+      }
+      pmeta = false;
+    } else {
       const int page = page_of(p, win, pc, lane);
-      if (lane == 0) issue_block_tma(p, &kvmap, layer, pc, page, ring + s * kMmaStageB, &bars[s]);
-      if (b + 1 < end) cursor_next(p, pc);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue_block_tma(p, &kvmap, layer, pc, page, st, &bars[s]);
+      }
+      if (++pblk < end) {
+        walk_next(p, pwin, pc, n, lane);
+        if (pc.blk == 0) pmeta = true;
+      }
     }
-  }
-  int64_t issued = start + S < end ? start + S : end;
-  // The operand rows and staged tokens (prep kernel), the split-K scratch
-  // and the outputs belong to earlier kernels: wait for them to finish.
+    ++pitems;
+    return true;
+  };
+  // prologue: blocks only (meta items read this step's inputs)
+  while (pitems < S && emit(false)) {}
+  // The step's inputs, the split-K scratch and the outputs belong to earlier
+  // kernels: wait for them.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  {
+    const PlanEntry e = plan_at(p, pwin, i_first, n, lane);
+    if (lane == 0) issue_meta<G>(p, layer, i_first, h_first, e.slot, e.pos, q, knew, vnew, ring, &bars[0]);
+  }
+  while (pitems < S && emit(true)) {}
 
   // per-lane ldmatrix row offsets (within a stage): K (non-transposed) and V
   const int mi = lane >> 3, ri = lane & 7;
@@ -478,6 +514,20 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   const uint32_t ring_u32 = smem_u32(ring);
 
   bool failed = false;
+  int64_t citems = 0;
+  auto wait_item = [&](int64_t c, int slot) -> bool {
+    const int s = (int)(c % S);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (uint32_t)((c / S) & 1),
+                                                              kWaitLimitNs));
+    if (!ok && lane == 0) set_status(p, GP_ST_TIMEOUT, slot);
+    return ok;
+  };
+  auto release_item = [&]() {
+    __syncwarp();
+    ++citems;
+    if (pitems < citems + S) emit(true);
+  };
+
   Cursor cc;
   cursor_start(p, w, cc);
   int64_t j = start;
@@ -485,18 +535,27 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     const int i = cc.i, h = cc.h, slot = cc.slot, nb = cc.nb;
     const int64_t len = ((int64_t)(nb - cc.blk) < end - j) ? (int64_t)(nb - cc.blk) : end - j;
     const bool full = (cc.blk == 0) && (len == nb);
-    const int R = p.plan_R[i];
-    const bool score = (p.plan_flags[i] & kPlanScore) != 0;
+    const PlanEntry pe = plan_at(p, cwin, i, n, lane);
+    const int R = pe.R;
+    const bool score = (pe.flags & kPlanScore) != 0;
 
-    // ---- A operand rows, prepared by prep_kernel (see there)
+    // ---- operand rows, and the once-per-(request, head) duties
     uint32_t afr[8][4];
     {
-      const uint4* fr = p.frag + (size_t)(i * p.Hk + h) * 8 * 32;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint4 v = fr[kk * 32 + lane];
-        afr[kk][0] = v.x; afr[kk][1] = v.y; afr[kk][2] = v.z; afr[kk][3] = v.w;
-      }
+      if (!wait_item(citems, slot)) { failed = true; break; }
+      const uint8_t* st = ring + (citems % S) * kMmaStageB;
+      PieceIn in;
+      in.q = reinterpret_cast<const __nv_bfloat16*>(st + kMetaQ);
+      in.k = reinterpret_cast<const __nv_bfloat16*>(st + kMetaK);
+      in.v = reinterpret_cast<const __nv_bfloat16*>(st + kMetaV);
+      in.s = reinterpret_cast<const float*>(st + kMetaS);
+      in.c32 = reinterpret_cast<const float*>(st + kMetaC32);
+      in.s32 = reinterpret_cast<const float*>(st + kMetaS32);
+      in.c64 = reinterpret_cast<const double*>(st + kMetaC64);
+      in.s64 = reinterpret_cast<const double*>(st + kMetaS64);
+      build_rows<G>(p, in, pe.flags, lane, afr);
+      if (cc.blk == 0) segment_duties<G>(p, layer, i, h, slot, pe.flags, in, obx, lane);
+      release_item();
     }
     const bool head_row = g < G;
     float* lgS = p.logits + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * p.logit_width;
@@ -508,16 +567,8 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 
     for (int64_t k = 0; k < len; ++k, ++j) {
-      const int64_t jl = j - start;
-      const int s = (int)(jl % S);
-      const bool ok = __all_sync(0xffffffffu,
-                                 mbar_wait_bounded(&bars[s], (uint32_t)((jl / S) & 1), kWaitLimitNs));
-      if (!ok) {
-        if (lane == 0) set_status(p, GP_ST_TIMEOUT, slot);
-        failed = true;
-        break;
-      }
-      const uint32_t sK = ring_u32 + s * kMmaStageB, sV = sK + 4096;
+      if (!wait_item(citems, slot)) { failed = true; break; }
+      const uint32_t sK = ring_u32 + (uint32_t)(citems % S) * kMmaStageB, sV = sK + 4096;
       // ---- scores: S[16 rows][16 tokens] = A · K^T
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -535,11 +586,11 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
       // summary scores: rows 4/5 (+ rows 12/13 in the same thread) plus the
       // lo rows 6/7 held 8 lanes up
-      {
+      if (score) {
         float other[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) other[u] = __shfl_xor_sync(0xffffffffu, sv[u], 8);
-        if (score && (g == 4 || g == 5)) {
+        if (g == 4 || g == 5) {
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             if (tok[u] < nvalid) lgX[t0 + tok[u]] = sv[u] + other[u];
@@ -585,17 +636,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
         mma_bf16(o[2 * q2], ap, b[0], b[1]);
         mma_bf16(o[2 * q2 + 1], ap, b[2], b[3]);
       }
-      // refill this stage with the block S ahead
-      __syncwarp();
-      if (issued < end) {
-        const int page = page_of(p, win, pc, lane);
-        if (lane == 0) {
-          fence_proxy_async_smem();
-          issue_block_tma(p, &kvmap, layer, pc, page, ring + s * kMmaStageB, &bars[s]);
-        }
-        if (issued + 1 < end) cursor_next(p, pc);
-        ++issued;
-      }
+      release_item();
     }
     if (failed) break;
 
@@ -615,7 +656,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     }
     __syncwarp();
     if (full) {
-      finish_mma<G>(p, layer, i, h, slot, out, ob, lane);
+      finish_mma<G>(p, i, h, out, ob, obx, lane);
     } else {
       // a cut (request, head): leave this piece's state for combine_kernel
       const int seg = i * p.Hk + h;
@@ -625,15 +666,16 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       for (int x = lane; x < G * D; x += 32) part[(x / D) * (D + 2) + (x % D)] = ob[x];
       if (lane < 2 * G) part[(lane % G) * (D + 2) + D + lane / G] = ob[G * D + lane];
     }
-    __syncwarp();  // the buffer is reused by the next piece
-    if (j < end) {
+    __syncwarp();  // the buffers are reused by the next piece
+    if (j < end) {  // next piece: block 0 of the following (request, head)
       cc.blk = cc.nb - 1;
-      cursor_next(p, cc);
+      walk_next(p, cwin, cc, n, lane);
     }
   }
   if (failed) {
-    for (int64_t jl = j - start; jl < issued - start; ++jl)
-      (void)mbar_wait_bounded(&bars[jl % S], (uint32_t)((jl / S) & 1), kWaitLimitNs);
+    // let the copies this warp has in flight land before the CTA may exit
+    for (int64_t c = citems; c < pitems; ++c)
+      (void)mbar_wait_bounded(&bars[c % S], (uint32_t)((c / S) & 1), kWaitLimitNs);
   }
 }
 
@@ -722,13 +764,13 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
 }
 
 size_t mma_smem_bytes() {
-  return (size_t)kMmaWarps * kMmaStages * kMmaStageB + (size_t)kMmaWarps * kObFloats * 4 +
+  return (size_t)kMmaWarps * kMmaStages * kMmaStageB + (size_t)kMmaWarps * kWarpBufFloats * 4 +
          (size_t)kMmaWarps * kMmaStages * 8 + 1024;
 }
 
 // Both kernels are launched as programmatic dependents of the previous
 // kernel in the stream (see griddepcontrol in the kernels): the attention
-// kernel's prologue (cursors, first K/V copies) overlaps the prep kernel.
+// kernel's prologue (cursors, first K/V copies) overlaps what runs before it.
 static cudaLaunchConfig_t pdl_config(cudaLaunchAttribute* attr, dim3 grid, dim3 block, size_t smem,
                                      cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
@@ -748,17 +790,15 @@ static cudaError_t launch_mma_t(const PoolDev& p, const CUtensorMap* map, int la
                                 const void* q, const void* k, const void* v, void* out, int grid,
                                 cudaStream_t st) {
   cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t c1 = pdl_config(attr, dim3(grid), dim3(kMmaWarps * 32), mma_smem_bytes(), st);
+  cudaError_t e = cudaLaunchKernelEx(&c1, attn_mma_kernel<G, kMmaStages>, *map, p, layer,
+                                     (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
+                                     (const __nv_bfloat16*)v, (__nv_bfloat16*)out);
+  if (e != cudaSuccess) return e;
   const int warps = n * p.Hk;
-  const dim3 sgrid((warps + kSmallWarps - 1) / kSmallWarps), sblock(kSmallWarps * 32);
-  cudaLaunchConfig_t c1 = pdl_config(attr, sgrid, sblock, 0, st);
-  cudaError_t e = cudaLaunchKernelEx(&c1, prep_kernel<G>, p, layer, (const __nv_bfloat16*)q,
-                                     (const __nv_bfloat16*)k, (const __nv_bfloat16*)v);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t c2 = pdl_config(attr, dim3(grid), dim3(kMmaWarps * 32), mma_smem_bytes(), st);
-  e = cudaLaunchKernelEx(&c2, attn_mma_kernel<G, kMmaStages>, *map, p, layer, (__nv_bfloat16*)out);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t c3 = pdl_config(attr, sgrid, sblock, 0, st);
-  return cudaLaunchKernelEx(&c3, combine_kernel<G>, p, layer, (__nv_bfloat16*)out);
+  cudaLaunchConfig_t c2 = pdl_config(attr, dim3((warps + kSmallWarps - 1) / kSmallWarps),
+                                     dim3(kSmallWarps * 32), 0, st);
+  return cudaLaunchKernelEx(&c2, combine_kernel<G>, p, layer, (__nv_bfloat16*)out);
 }
 
 template <int G>
@@ -772,7 +812,7 @@ static cudaError_t occupancy_mma_t(int* blocks) {
 
 int mma_warps_per_cta() { return kMmaWarps; }
 
-// Three launches: prep_kernel, attn_mma_kernel, combine_kernel.
+// Two launches: attn_mma_kernel, then combine_kernel.
 cudaError_t launch_attention_mma(const PoolDev& p, const CUtensorMap* map, int layer, int n,
                                  const void* q, const void* k, const void* v, void* out, int grid,
                                  cudaStream_t st) {

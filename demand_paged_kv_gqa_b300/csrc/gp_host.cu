@@ -133,12 +133,12 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   l->prefix_pages = take((uint64_t)c->max_prefixes * l->max_prefix_pages * 4);
   l->rope = take((uint64_t)c->max_seq_len * (D / 2) * (8 + 8 + 4 + 4));
   l->scratch = off;
-  for (int k = 0; k < 10; ++k) take((R + 1) * 4);             // plan arrays
+  for (int k = 0; k < 11; ++k) take((R + 1) * 4);             // plan arrays
   take(R * 8);                                                 // plan_delta
   take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 2) * 4);  // partials
   take(R * Hk * 4);                                            // seg_count
   take((uint64_t)gp::kMaxWorkersBound * 16);                   // wstart
-  take(R * Hk * 8 * 32 * 16);                                  // frag
+  take(R * L * Hk * 2 * D * 4);                                // summary_next
   take(R * Hk * 4 * 4);                                        // sstage
   take(R * L * Hk * P * 2 * 4);                                // moves
   take(R * L * Hk * 4);                                        // moves_n
@@ -194,11 +194,12 @@ void fill_dev(gp_pool* p) {
   d.plan_dec = (int32_t*)take((R + 1) * 4);
   d.plan_bnd = (int32_t*)take((R + 1) * 4);
   d.plan_misc = (int32_t*)take((R + 1) * 4);
+  d.plan_pos = (int32_t*)take((R + 1) * 4);
   d.plan_delta = (long long*)take(R * 8);
   d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 2) * 4);
   d.seg_count = (int32_t*)take(R * c.num_kv_heads * 4);
   d.wstart = (int4*)take((uint64_t)gp::kMaxWorkersBound * 16);
-  d.frag = (uint4*)take(R * c.num_kv_heads * 8 * 32 * 16);
+  d.summary_next = (float*)take(R * c.num_layers * c.num_kv_heads * 2 * c.head_dim * 4);
   d.sstage = (float*)take(R * c.num_kv_heads * 4 * 4);
   d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 2 * 4);
   d.moves_n = (int32_t*)take(R * c.num_layers * c.num_kv_heads * 4);
@@ -301,6 +302,7 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   p->launches += 1;
   p->use_mma = cfg->dtype == GP_DTYPE_BF16 && cfg->head_dim == 128;
+  p->dev.summary_via_next = p->use_mma ? 1 : 0;
   if (p->use_mma) {
     // The pool's K/V pages viewed as one 2-D bf16 tensor [rows][d], rows =
     // ((page * L + layer) * Hk + head) * 2 * P + kv * P + token; boxes of
@@ -449,6 +451,8 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
   if (n < 0 || n > c.max_requests) return fail(pool, GP_ERR_INVALID, "n out of range");
   if (n > 0 && (!slots_dev || !q || !k_new || !v_new || !out))
     return fail(pool, GP_ERR_INVALID, "null tensor");
+  if (((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)out) % 16)
+    return fail(pool, GP_ERR_INVALID, "q, k_new, v_new and out must be 16-byte aligned");
   if (layer == 0) {
     GP_LAUNCH(pool, gp::launch_plan(pool->dev, n, slots_dev, 1, pool->stream));
     pool->step_n = n;
@@ -460,7 +464,7 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
     if (pool->use_mma) {
       GP_LAUNCH(pool, gp::launch_attention_mma(pool->dev, &pool->kvmap, layer, n, q, k_new, v_new,
                                                out, pool->attn_grid, pool->stream));
-      pool->launches += 2;  // prep, attention and combine kernels
+      pool->launches += 1;  // attention and combine kernels
     }
     else
       GP_LAUNCH(pool, gp::launch_attention(pool->dev, layer, q, k_new, v_new, out, pool->attn_grid,

@@ -61,15 +61,18 @@ struct PoolDev {
   int32_t* plan_cpos;     // [max_req] its position
   int32_t* plan_dec;      // [max_req] decision of this step
   int32_t* plan_bnd;      // [max_req] indices i of scoring boundaries
+  int32_t* plan_pos;      // [max_req] position of the step's token
   int32_t* plan_misc;     // [0] n, [1] n scoring boundaries, [2] total blocks/Hk
   long long* plan_delta;  // [max_req] Delta accumulators
   // scratch: attention split-K
   float* partials;        // [num_workers][2][G][D + 2]
   int32_t* seg_count;     // [max_req][Hk]
-  uint4* frag;            // [max_req][Hk][8][32] bf16 tensor-core operand rows per
-                          // (request, kv head) as held by each lane (prep kernel)
+  float* summary_next;    // [max_req][L][Hk][2][d] this step's folded summaries
+                          // (bf16 attention path), copied over `summary` by the
+                          // commit kernel once every layer has been read
   float* sstage;          // [max_req][Hk][4] each query head's score against the
-                          // staged token (log2 domain, prep kernel)
+                          // staged token (log2 domain)
+  int32_t summary_via_next;  // 1: the attention kernel writes summary_next
   int4* wstart;           // [kMaxWorkersBound] first block of each attention worker:
                           // request index, (head << 20) | block, blocks of the
                           // segment, slot (written by the plan kernel)

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
         s_bad = 1;
         set_status(p, GP_ST_BAD_SLOTS, i);
         p.plan_slot[i] = 0; p.plan_R[i] = 0; p.plan_nb[i] = 1; p.plan_flags[i] = 0;
+        p.plan_pos[i] = 0;
         nb = 1;
       } else {
         const gp_req_meta m = p.req[slot];
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
         if (at_b && p.mode == GP_MODE_GROWPAGE) flags |= kPlanScore;
         isb = (flags & kPlanScore) ? 1 : 0;
         p.plan_slot[i] = slot; p.plan_R[i] = R; p.plan_nb[i] = nb; p.plan_flags[i] = flags;
+        p.plan_pos[i] = m.pos;
         p.plan_delta[i] = 0;
         atomicAdd(&s_tok, (unsigned long long)R);
         if (at_b) atomicAdd(&s_btok, (unsigned long long)R);
@@ -566,6 +568,11 @@ __global__ void __launch_bounds__(256) commit_kernel(PoolDev p) {
     const int npre = p.req[slot].n_pre_pages;
     const int32_t* bt = p.block + (size_t)slot * p.block_width + npre;
     const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
+    if (p.summary_via_next) {  // this step's folded summaries become current
+      const float4* src = reinterpret_cast<const float4*>(p.summary_next + row * 2 * p.D);
+      float4* dst = reinterpret_cast<float4*>(p.summary + row * 2 * p.D);
+      for (int c = lane; c < 2 * p.D / 4; c += 32) dst[c] = src[c];
+    }
     if (dec == kCompact || dec == kCompactDenied) {
       const int nm = p.moves_n[row];
       const int32_t* mv = p.moves + row * p.P * 2;
