@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -515,6 +516,80 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
   const int grid = (pool->dev.num_workers + wpc - 1) / wpc;
   for (int l = layer0; l < layer0 + count; ++l)
     GP_LAUNCH(pool, gp::launch_kv_read(pool->dev, &pool->kvmap, l, mode, sink_dev, grid, pool->stream));
+  return GP_OK;
+}
+
+}  // extern "C"
+
+// ---- read ceiling without caller scratch -------------------------------
+//
+// Scratch of gp_kv_read_ceiling_static: the step plan (eleven arrays of
+// kStaticMaxRequests + 1 ints, the Delta accumulators) and the per-worker
+// start cursors.  It is a file-scope device array, so every GPU that loads
+// the library holds these bytes until the process exits.
+namespace {
+constexpr int kStaticMaxRequests = 1024;
+constexpr size_t kStaticPlanArrayBytes = ((size_t)(kStaticMaxRequests + 1) * 4 + 255) / 256 * 256;
+constexpr size_t kStaticDeltaBytes = (size_t)kStaticMaxRequests * 8;
+constexpr size_t kStaticBytes =
+    11 * kStaticPlanArrayBytes + kStaticDeltaBytes + (size_t)gp::kMaxWorkersBound * 16;
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+uint8_t* g_static_addr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device (set up once per
+// device; the host-side name of the array is not a device address).
+cudaError_t static_scratch(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_addr[dev] = static_cast<uint8_t*>(ptr);
+  }
+  *out = g_static_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
+extern "C" {
+
+int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int32_t mode,
+                              int32_t n, const int32_t* slots_dev, uint32_t* sink_dev) {
+  if (!pool) return GP_ERR_INVALID;
+  if (!pool->use_mma) return fail(pool, GP_ERR_INVALID, "read ceiling needs bf16 pages with head_dim 128");
+  if (layer0 < 0 || count < 1 || layer0 + count > pool->cfg.num_layers || mode < 0 || mode > 2 ||
+      n < 0 || n > pool->cfg.max_requests || !sink_dev || (n > 0 && !slots_dev))
+    return fail(pool, GP_ERR_INVALID, "bad read-ceiling arguments");
+  if (n > kStaticMaxRequests)
+    return fail(pool, GP_ERR_INVALID, "gp_kv_read_ceiling_static: n exceeds the static scratch limit of 1024 requests");
+  if (pool->dev.num_workers > gp::kMaxWorkersBound)
+    return fail(pool, GP_ERR_INVALID, "gp_kv_read_ceiling_static: too many attention workers");
+  uint8_t* base = nullptr;
+  cudaError_t e = static_scratch(&base);
+  if (e != cudaSuccess) return cuda_fail(pool, e, "cudaGetSymbolAddress(g_static_scratch)");
+  // the pool's view with its per-call scratch moved into the static array
+  gp::PoolDev d = pool->dev;
+  int32_t** arrays[11] = {&d.plan_slot, &d.plan_R,    &d.plan_nb,  &d.plan_cum,
+                          &d.plan_flags, &d.plan_commit, &d.plan_cpos, &d.plan_dec,
+                          &d.plan_bnd,  &d.plan_misc, &d.plan_pos};
+  for (int k = 0; k < 11; ++k) *arrays[k] = (int32_t*)(base + k * kStaticPlanArrayBytes);
+  d.plan_delta = (long long*)(base + 11 * kStaticPlanArrayBytes);
+  d.wstart = (int4*)(base + 11 * kStaticPlanArrayBytes + kStaticDeltaBytes);
+  GP_LAUNCH(pool, gp::launch_plan(d, n, slots_dev, 0, pool->stream));
+  const int wpc = gp::ceiling_warps_per_cta();
+  const int grid = (d.num_workers + wpc - 1) / wpc;
+  for (int l = layer0; l < layer0 + count; ++l)
+    GP_LAUNCH(pool, gp::launch_kv_read(d, &pool->kvmap, l, mode, sink_dev, grid, pool->stream));
   return GP_OK;
 }
 

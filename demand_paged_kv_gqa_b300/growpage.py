@@ -87,6 +87,7 @@ def _load():
         "gp_get_request": (ctypes.c_int, [P, I32, ctypes.POINTER(gp_req_meta),
                                           ctypes.POINTER(I32), I32]),
         "gp_kv_read_ceiling": (ctypes.c_int, [P, I32, I32, I32, I32, P, P]),
+        "gp_kv_read_ceiling_static": (ctypes.c_int, [P, I32, I32, I32, I32, P, P]),
         "gp_last_error": (ctypes.c_char_p, [P]),
         "gp_launch_count": (I64, [P]),
     }
@@ -220,6 +221,12 @@ class Pool:
         """Read-only streaming of layers' resident K/V (a bandwidth ceiling)."""
         self._check(lib.gp_kv_read_ceiling(self.h, layer0, count, mode, slots.numel(),
                                            _ptr(slots), _ptr(sink)))
+
+    def kv_read_ceiling_static(self, layer0: int, count: int, mode: int, slots: torch.Tensor,
+                               sink: torch.Tensor):
+        """The same read, with its scratch in the library's static device array."""
+        self._check(lib.gp_kv_read_ceiling_static(self.h, layer0, count, mode, slots.numel(),
+                                                  _ptr(slots), _ptr(sink)))
 
     def launch_count(self) -> int:
         return int(lib.gp_launch_count(self.h))

@@ -266,6 +266,29 @@ int gp_free(gp_pool* pool, int32_t slot);
 int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mode, int32_t n,
                        const int32_t* slots_dev, uint32_t* sink_dev);
 
+/* gp_kv_read_ceiling without caller scratch.  No counterpart in the paper:
+ * it is a convenience of this library for callers that cannot allocate device
+ * memory when they call it -- code running inside a memory arena sized
+ * once at start-up, or a runtime whose allocator must not be entered at that
+ * point -- and for callers that must not disturb the pool's own scratch,
+ * which gp_kv_read_ceiling overwrites (so that one may only run between
+ * steps).  Same arguments, result and rules as gp_kv_read_ceiling, except:
+ *   - the per-call scratch (the step plan of the n requests and the start
+ *     cursor of every attention worker) lives in a file-scope device array
+ *     of this library, about 135 KB, which every GPU that loads the library
+ *     keeps until the process exits; nothing of it needs clearing, as each
+ *     call writes all the scratch it reads;
+ *   - n may not exceed 1024 (GP_ERR_INVALID with a message otherwise);
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture;
+ *   - all calls share the array: two calls whose work overlaps on the GPU
+ *     (different streams, or different pools on one device) race.
+ * It calls no cudaMalloc, cudaFree or allocating library routine.
+ * Asynchronous. */
+int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int32_t mode,
+                              int32_t n, const int32_t* slots_dev, uint32_t* sink_dev);
+
 /* Wait for the stream; GP_ERR_DEVICE if the device status word is set.
  * SYNC. */
 int gp_sync(gp_pool* pool);
