@@ -729,24 +729,37 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
     lsum[g] = 0.f;
     acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
   }
-  // online merge over the parts: every lane holds dims lane + 32e of each head
-  for (int k = 0; k < nparts; ++k) {
-    const float* pk = part_of(k);
+  // online merge over the parts, four at a time with all their loads issued
+  // first: every lane holds dims lane + 32e of each head
+  constexpr int CH = 4;
+  for (int base = 0; base < nparts; base += CH) {
+    float mv[CH][G], lv[CH][G], ov[CH][G][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mk = __ldcg(pk + g * (D + 2) + D);
-      const float lk = __ldcg(pk + g * (D + 2) + D + 1);
-      float ov[4];
+    for (int u = 0; u < CH; ++u) {
+      const bool ok = base + u < nparts;
+      const float* pk = part_of(ok ? base + u : base);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) ov[e] = __ldcg(pk + g * (D + 2) + lane + 32 * e);
-      if (mk == -INFINITY) continue;
-      const float mn = fmaxf(mmax[g], mk);
-      const float al = (mmax[g] == -INFINITY) ? 0.f : exp2f(mmax[g] - mn);
-      const float be = exp2f(mk - mn);
-      lsum[g] = lsum[g] * al + lk * be;
+      for (int g = 0; g < G; ++g) {
+        mv[u][g] = ok ? __ldcg(pk + g * (D + 2) + D) : -INFINITY;
+        lv[u][g] = ok ? __ldcg(pk + g * (D + 2) + D + 1) : 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[g][e] = acc[g][e] * al + ov[e] * be;
-      mmax[g] = mn;
+        for (int e = 0; e < 4; ++e) ov[u][g][e] = ok ? __ldcg(pk + g * (D + 2) + lane + 32 * e) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < CH; ++u) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float mk = mv[u][g];
+        if (mk == -INFINITY) continue;
+        const float mn = fmaxf(mmax[g], mk);
+        const float al = (mmax[g] == -INFINITY) ? 0.f : exp2f(mmax[g] - mn);
+        const float be = exp2f(mk - mn);
+        lsum[g] = lsum[g] * al + lv[u][g] * be;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[g][e] = acc[g][e] * al + ov[u][g][e] * be;
+        mmax[g] = mn;
+      }
     }
   }
   // the staged token, normalisation, store

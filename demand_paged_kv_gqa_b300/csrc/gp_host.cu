@@ -30,6 +30,7 @@ int ceiling_warps_per_cta();
 cudaError_t launch_kv_read(const PoolDev& p, const CUtensorMap* map, int layer, int mode,
                            uint32_t* sink, int grid, cudaStream_t st);
 cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st);
+cudaError_t select_setup();
 cudaError_t launch_decide(const PoolDev& p, cudaStream_t st);
 cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st);
 cudaError_t launch_init(const PoolDev& p, cudaStream_t st);
@@ -299,6 +300,7 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
     if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
     if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   }
+  if (gp::select_setup() != cudaSuccess) return bail(GP_ERR_CUDA);
   e = gp::launch_init(p->dev, p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   p->launches += 1;

@@ -224,10 +224,41 @@ struct SelShared {
   int done;
 };
 
+// Sources of e_j = exp(u_j - max) for one summary's scores: computed from the
+// scores in global memory, or read from shared memory where the kernel has
+// staged them once (rows of up to kSelSmemTok tokens).  Both give the same
+// value for every j.
+struct EGlobal {
+  const float* u;
+  float mx;
+  __device__ __forceinline__ float operator()(int j) const { return expf(u[j] - mx); }
+};
+struct ESmem {
+  const float* e;
+  __device__ __forceinline__ float operator()(int j) const { return e[j]; }
+};
+// Absolute position of private slot s: gathered through the block table, or
+// staged in shared memory.
+struct PosGlobal {
+  const int32_t* bt;
+  const int32_t* tok_pos;
+  int P, L, Hk, layer, h, num_pages;
+  __device__ __forceinline__ int operator()(int s) const {
+    int page = bt[s / P];
+    if ((unsigned)page >= (unsigned)num_pages) page = 0;
+    return tok_pos[(((size_t)page * L + layer) * Hk + h) * P + (s % P)];
+  }
+};
+struct PosSmem {
+  const int* pos;
+  __device__ __forceinline__ int operator()(int s) const { return pos[s]; }
+};
+
 // Top-p working-set size: smallest k with (mass of the k largest) >= thr,
 // by a 4-pass radix select (8 bits per pass, most significant first) on the
-// fp32 bit patterns of e_j = exp(u_j - max), weighting each by its mass.
-__device__ int topp_radix(const float* u, int R, float mx, unsigned long long thr, SelShared& sh) {
+// fp32 bit patterns of e_j, weighting each by its fixed-point mass.
+template <class EF>
+__device__ int topp_radix(EF e_at, int R, unsigned long long thr, SelShared& sh) {
   uint32_t prefix = 0u, pmask = 0u;
   unsigned long long mass_above = 0ull, cnt_above = 0ull;
   for (int pass = 0; pass < 4; ++pass) {
@@ -236,7 +267,7 @@ __device__ int topp_radix(const float* u, int R, float mx, unsigned long long th
     if (threadIdx.x == 0) { sh.pick_d = 0u; sh.pick_a = 0ull; sh.pick_b = 0ull; }
     __syncthreads();
     for (int j = threadIdx.x; j < R; j += blockDim.x) {
-      const float e = expf(u[j] - mx);
+      const float e = e_at(j);
       const uint32_t bits = __float_as_uint(e);
       if ((bits & pmask) == prefix) {
         const int d = (bits >> shift) & 255;
@@ -293,32 +324,28 @@ __device__ int topp_radix(const float* u, int R, float mx, unsigned long long th
   return (int)(cnt_above + (k ? k : 1ull));
 }
 
-struct SelCtx {
-  const float* uS;
-  const float* uL;
-  float mS, mL, invS, invL;
-  int npre;           // prefix tokens (logical index of private slot 0)
-  int cut_pos;        // positions below this are compaction candidates
-  const int32_t* bt;  // private block-table row
-  const int32_t* tok_pos;
-  int P, L, Hk, layer, h, num_pages;
+// Compaction key of private slot s: (importance bits << 32 | position), with
+// importance = max(p_S, p_L); *cand: the token is older than the window.
+template <class ES, class EL, class PF>
+struct KeyOf {
+  ES eS;
+  EL eL;
+  PF posf;
+  float invS, invL;
+  int npre, cut_pos;
+  __device__ __forceinline__ unsigned long long operator()(int s, bool* cand) const {
+    const int pos = posf(s);
+    *cand = pos < cut_pos;
+    const float I = fmaxf(eS(npre + s) * invS, eL(npre + s) * invL);
+    return ((unsigned long long)__float_as_uint(I) << 32) | (unsigned long long)(uint32_t)pos;
+  }
 };
-
-__device__ __forceinline__ unsigned long long key_of(const SelCtx& c, int s, bool* cand) {
-  int page = c.bt[s / c.P];
-  if ((unsigned)page >= (unsigned)c.num_pages) page = 0;
-  const int pos = c.tok_pos[(((size_t)page * c.L + c.layer) * c.Hk + c.h) * c.P + (s % c.P)];
-  *cand = pos < c.cut_pos;
-  const float eS = expf(c.uS[c.npre + s] - c.mS);
-  const float eL = expf(c.uL[c.npre + s] - c.mL);
-  const float I = fmaxf(eS * c.invS, eL * c.invL);
-  return ((unsigned long long)__float_as_uint(I) << 32) | (unsigned long long)(uint32_t)pos;
-}
 
 // Threshold key such that exactly `k` candidates have key <= threshold (keys
 // are distinct: they end with the token position).  Radix select, 8 bits per
 // pass from the top, stopping as soon as the chosen bucket is taken whole.
-__device__ unsigned long long kth_smallest(const SelCtx& c, int C, int k, SelShared& sh) {
+template <class KF>
+__device__ unsigned long long kth_smallest(const KF& key_of, int C, int k, SelShared& sh) {
   unsigned long long prefix = 0ull, pmask = 0ull;
   unsigned int below = 0u;
   for (int pass = 0; pass < 8; ++pass) {
@@ -327,7 +354,7 @@ __device__ unsigned long long kth_smallest(const SelCtx& c, int C, int k, SelSha
     __syncthreads();
     for (int s = threadIdx.x; s < C; s += blockDim.x) {
       bool cand;
-      const unsigned long long key = key_of(c, s, &cand);
+      const unsigned long long key = key_of(s, &cand);
       if (cand && (key & pmask) == prefix) atomicAdd(&sh.cnt[(key >> shift) & 255], 1u);
     }
     __syncthreads();
@@ -354,8 +381,91 @@ __device__ unsigned long long kth_smallest(const SelCtx& c, int C, int k, SelSha
   return prefix;
 }
 
+// Working sets, Delta and the compaction plan of one (request, layer, head).
+template <class ES, class EL, class PF>
+__device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const gp_req_meta& m,
+                            int R, ES eS, EL eL, float mS, float mL, PF posf, SelShared& sh) {
+  // fixed-point masses, Top-p counts
+  float inv[2];
+  int W[2];
+  for (int X = 0; X < 2; ++X) {
+    unsigned long long s = 0ull;
+    for (int j = threadIdx.x; j < R; j += blockDim.x) s += mass_q(X ? eL(j) : eS(j));
+    const unsigned long long T = block_sum_ull(s, sh.red);
+    const unsigned long long thr = ceil_mul(p.top_p, T);
+    W[X] = X ? topp_radix(eL, R, thr, sh) : topp_radix(eS, R, thr, sh);
+    inv[X] = (float)(0x1p40 / (double)(T ? T : 1ull));
+  }
+  if (threadIdx.x == 0) {
+    p.wset[row * 2 + 0] = W[0];
+    p.wset[row * 2 + 1] = W[1];
+    atomicAdd((unsigned long long*)&p.plan_delta[i], (unsigned long long)(long long)(W[0] - W[1]));
+  }
+  // compaction plan: drop the P lowest (importance, position) candidates
+  const int C = m.n_pages * p.P;
+  const int weff = min(p.recent_window, C - p.P);
+  KeyOf<ES, EL, PF> key_of{eS, eL, posf, inv[0], inv[1], m.n_pre_pages * p.P, m.pos - weff};
+  const unsigned long long thr_key = kth_smallest(key_of, C, p.P, sh);
+  // holes below C-P and survivors of the last page, both ascending
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int nh = 0;
+    for (int base = 0; base < C - p.P; base += 32) {
+      const int s = base + lane;
+      bool dropped = false;
+      if (s < C - p.P) {
+        bool cand;
+        const unsigned long long key = key_of(s, &cand);
+        dropped = cand && key <= thr_key;
+      }
+      const unsigned int bal = __ballot_sync(0xffffffffu, dropped);
+      if (dropped) {
+        const int r = nh + __popc(bal & ((1u << lane) - 1u));
+        if (r < 256) sh.holes[r] = s;
+      }
+      nh += __popc(bal);
+    }
+    int ns = 0;
+    for (int base = C - p.P; base < C; base += 32) {
+      const int s = base + lane;
+      bool kept = false;
+      if (s < C) {
+        bool cand;
+        const unsigned long long key = key_of(s, &cand);
+        kept = !(cand && key <= thr_key);
+      }
+      const unsigned int bal = __ballot_sync(0xffffffffu, kept);
+      if (kept) {
+        const int r = ns + __popc(bal & ((1u << lane) - 1u));
+        if (r < 256) sh.srcs[r] = s;
+      }
+      ns += __popc(bal);
+    }
+    if (nh != ns || nh > p.P) {
+      if (lane == 0) set_status(p, GP_ST_BAD_PLAN, slot);
+      nh = 0;
+    }
+    int32_t* mv = p.moves + row * p.P * 2;
+    for (int t = lane; t < nh; t += 32) {
+      mv[2 * t] = sh.holes[t];
+      mv[2 * t + 1] = sh.srcs[t];
+    }
+    if (lane == 0) p.moves_n[row] = nh;
+  }
+  __syncthreads();
+}
+
+// Rows of up to this many tokens are staged in shared memory: both
+// summaries' e_j and the private slots' positions (48 KiB).
+constexpr int kSelSmemTok = 4096;
+constexpr size_t kSelSmemBytes = (size_t)kSelSmemTok * (4 + 4 + 4);
+
 __global__ void __launch_bounds__(kSelThreads) select_kernel(PoolDev p) {
   __shared__ SelShared sh;
+  extern __shared__ float sel_dyn[];
+  float* eSs = sel_dyn;
+  float* eLs = sel_dyn + kSelSmemTok;
+  int* poss = reinterpret_cast<int*>(sel_dyn + 2 * kSelSmemTok);
   const int nb = p.plan_misc[1];
   const int items = nb * p.L * p.Hk;
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
@@ -366,88 +476,30 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(PoolDev p) {
     const int slot = p.plan_slot[i];
     const int R = p.plan_R[i];
     const gp_req_meta m = p.req[slot];
-    const int npre = m.n_pre_pages * p.P;
     const int C = m.n_pages * p.P;
     const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
     const float* uS = p.logits + row * 2 * p.logit_width;
     const float* uL = uS + p.logit_width;
-    float mx[2], inv[2];
-    int W[2];
+    float mx[2];
     for (int X = 0; X < 2; ++X) {
       const float* u = X ? uL : uS;
       float v = -INFINITY;
       for (int j = threadIdx.x; j < R; j += blockDim.x) v = fmaxf(v, u[j]);
       mx[X] = block_max_f(v, sh.redf);
-      unsigned long long s = 0ull;
-      for (int j = threadIdx.x; j < R; j += blockDim.x) s += mass_q(expf(u[j] - mx[X]));
-      const unsigned long long T = block_sum_ull(s, sh.red);
-      const unsigned long long thr = ceil_mul(p.top_p, T);
-      W[X] = topp_radix(u, R, mx[X], thr, sh);
-      inv[X] = (float)(0x1p40 / (double)(T ? T : 1ull));
     }
-    if (threadIdx.x == 0) {
-      p.wset[row * 2 + 0] = W[0];
-      p.wset[row * 2 + 1] = W[1];
-      atomicAdd((unsigned long long*)&p.plan_delta[i],
-                (unsigned long long)(long long)(W[0] - W[1]));
+    PosGlobal pg{p.block + (size_t)slot * p.block_width + m.n_pre_pages, p.tok_pos, p.P, p.L, p.Hk,
+                 layer, h, p.num_pages};
+    if (R <= kSelSmemTok && C <= kSelSmemTok) {
+      for (int j = threadIdx.x; j < R; j += blockDim.x) {
+        eSs[j] = expf(uS[j] - mx[0]);
+        eLs[j] = expf(uL[j] - mx[1]);
+      }
+      for (int s = threadIdx.x; s < C; s += blockDim.x) poss[s] = pg(s);
+      __syncthreads();
+      select_item(p, i, slot, row, m, R, ESmem{eSs}, ESmem{eLs}, mx[0], mx[1], PosSmem{poss}, sh);
+    } else {
+      select_item(p, i, slot, row, m, R, EGlobal{uS, mx[0]}, EGlobal{uL, mx[1]}, mx[0], mx[1], pg, sh);
     }
-    // compaction plan: drop the P lowest (importance, position) candidates
-    SelCtx c;
-    c.uS = uS; c.uL = uL; c.mS = mx[0]; c.mL = mx[1]; c.invS = inv[0]; c.invL = inv[1];
-    c.npre = npre;
-    const int weff = min(p.recent_window, C - p.P);
-    c.cut_pos = m.pos - weff;
-    c.bt = p.block + (size_t)slot * p.block_width + m.n_pre_pages;
-    c.tok_pos = p.tok_pos;
-    c.P = p.P; c.L = p.L; c.Hk = p.Hk; c.layer = layer; c.h = h; c.num_pages = p.num_pages;
-    const unsigned long long thr_key = kth_smallest(c, C, p.P, sh);
-    // holes below C-P and survivors of the last page, both ascending
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      int nh = 0;
-      for (int base = 0; base < C - p.P; base += 32) {
-        const int s = base + lane;
-        bool dropped = false;
-        if (s < C - p.P) {
-          bool cand;
-          const unsigned long long key = key_of(c, s, &cand);
-          dropped = cand && key <= thr_key;
-        }
-        const unsigned int bal = __ballot_sync(0xffffffffu, dropped);
-        if (dropped) {
-          const int r = nh + __popc(bal & ((1u << lane) - 1u));
-          if (r < 256) sh.holes[r] = s;
-        }
-        nh += __popc(bal);
-      }
-      int ns = 0;
-      for (int base = C - p.P; base < C; base += 32) {
-        const int s = base + lane;
-        bool kept = false;
-        if (s < C) {
-          bool cand;
-          const unsigned long long key = key_of(c, s, &cand);
-          kept = !(cand && key <= thr_key);
-        }
-        const unsigned int bal = __ballot_sync(0xffffffffu, kept);
-        if (kept) {
-          const int r = ns + __popc(bal & ((1u << lane) - 1u));
-          if (r < 256) sh.srcs[r] = s;
-        }
-        ns += __popc(bal);
-      }
-      if (nh != ns || nh > p.P) {
-        if (lane == 0) set_status(p, GP_ST_BAD_PLAN, slot);
-        nh = 0;
-      }
-      int32_t* mv = p.moves + row * p.P * 2;
-      for (int t = lane; t < nh; t += 32) {
-        mv[2 * t] = sh.holes[t];
-        mv[2 * t + 1] = sh.srcs[t];
-      }
-      if (lane == 0) p.moves_n[row] = nh;
-    }
-    __syncthreads();
   }
 }
 
@@ -739,8 +791,12 @@ cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count
   plan_kernel<<<1, 1024, 0, st>>>(p, n, slots, count);
   return cudaGetLastError();
 }
+cudaError_t select_setup() {
+  return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSelSmemBytes);
+}
 cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st) {
-  select_kernel<<<grid, kSelThreads, 0, st>>>(p);
+  select_kernel<<<grid, kSelThreads, kSelSmemBytes, st>>>(p);
   return cudaGetLastError();
 }
 cudaError_t launch_decide(const PoolDev& p, cudaStream_t st) {
