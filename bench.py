@@ -137,6 +137,21 @@ class ClockSampler:
         return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_over_ranks(t_ms, tokens, device):
+    """Max over ranks of the timed milliseconds and sum of the tokens.
+
+    Replicas share nothing on the data path (requests are independent); this
+    host-side reduction of the timing is the only cross-rank step."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(t_ms), float(tokens)
+    tt = torch.tensor([float(t_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    nn = torch.tensor([float(tokens)], dtype=torch.float64, device=device)
+    dist.all_reduce(nn)
+    return float(tt.item()), float(nn.item())
+
+
 # ------------------------------------------------------------ byte counts
 
 def attention_bytes(w, tok, req_steps, btok):
@@ -315,14 +330,7 @@ def run_ours(args, ws, rank, local):
     fk_res = None if args.no_full_kv else measure(gpb.GP_MODE_FULL_KV, "full_kv")
 
     # max over ranks of the time, sum of tokens
-    t_ms = gp_res["step_ms"]
-    tokens = gp_res["tokens"]
-    if ws > 1:
-        tt = torch.tensor([t_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        nn = torch.tensor([tokens], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(nn)
-        t_ms, tokens = float(tt.item()), float(nn.item())
+    t_ms, tokens = reduce_over_ranks(gp_res["step_ms"], gp_res["tokens"], dev)
     if rank != 0:
         return None
     value = tokens / (t_ms * 1e-3)

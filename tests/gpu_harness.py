@@ -74,11 +74,20 @@ class _Arbiter:
         return gd
 
 
-def _private_positions(tok_pos: np.ndarray, bt_priv: List[int], n: int, L: int, hk: int, P: int):
-    """[L][Hk][n] positions of the first n private slots (block-table order)."""
+def _private_positions(tok_pos, bt_priv: List[int], n: int, L: int, hk: int, P: int):
+    """[L][Hk][n] positions of the first n private slots (block-table order).
+
+    ``tok_pos`` is the host copy of the whole region, or the device tensor
+    itself, in which case only the request's own pages are copied."""
+    npg = -(-n // P)
+    if isinstance(tok_pos, torch.Tensor):
+        idx = torch.tensor(bt_priv[:npg], dtype=torch.long, device=tok_pos.device)
+        rows = tok_pos.index_select(0, idx).cpu().numpy()        # [npg][L][Hk][P]
+    else:
+        rows = tok_pos[bt_priv[:npg]]
     out = np.zeros((L, hk, n), np.int64)
     for s in range(n):
-        out[:, :, s] = tok_pos[bt_priv[s // P], :, :, s % P]
+        out[:, :, s] = rows[s // P, :, :, s % P]
     return out
 
 
@@ -231,3 +240,174 @@ class Harness:
             if self.rep.failures:
                 break
         return self.rep
+
+
+class Scenario:
+    """A GPU pool and the oracle driven through admissions, steps and frees.
+
+    ``compare_all``: the oracle holds every request and the same pool, so
+    block tables are compared exactly.  Otherwise only the requests admitted
+    with ``compare=True`` are simulated (each needs nothing from the others
+    as long as the GPU pool never runs short of pages, which is checked), and
+    page counts, positions and kept-token sets are compared instead of page
+    ids.  Inputs come from ``synth.RequestStream`` on ``gen_device``.
+    """
+
+    def __init__(self, w, max_requests, num_pages, mode=gpb.GP_MODE_GROWPAGE, compare_all=True,
+                 gen_device="cpu", max_seq_len=None, max_prefixes=0, tol=None, oracle_pages=None):
+        self.w = w
+        self.full_kv = mode == gpb.GP_MODE_FULL_KV
+        self.cfg = gpb.config_for(w, mode=mode, max_requests=max_requests, num_pages=num_pages,
+                                  max_seq_len=max_seq_len, max_prefixes=max_prefixes)
+        self.pool = gpb.Pool(self.cfg)
+        self.compare_all = compare_all
+        opages = num_pages if compare_all else (oracle_pages or num_pages)
+        self.ora = OraclePool(OracleConfig.from_workload(w, full_kv=self.full_kv, num_pages=opages))
+        self.tol = tol if tol is not None else (1e-4 if w.dtype == "f32" else 2e-2)
+        self.rep = Report()
+        self.arb = _Arbiter(self.rep)
+        self.gen = torch.device(gen_device)
+        self.dev = torch.device("cuda")
+        self.active = {}          # slot -> RequestStream
+        self.cmp = set()          # compared slots
+        self.gpid, self.opid = {}, {}
+        self.prev_nb = {}
+
+    def add_prefix(self, index, compare=True):
+        k, v = synth.prefix_tensors(self.w, index, device=self.gen)
+        self.gpid[index] = self.pool.add_prefix(k.to(self.dev).contiguous(), v.to(self.dev).contiguous())
+        if compare:
+            self.opid[index] = self.ora.add_prefix(k.double().cpu().numpy(), v.double().cpu().numpy())
+        return self.gpid[index]
+
+    def release_prefix(self, index):
+        self.pool.release_prefix(self.gpid.pop(index))
+        if index in self.opid:
+            self.ora.release_prefix(self.opid.pop(index))
+
+    def admit(self, slot, rid, compare=True, prefix=None, budget_pages=None):
+        w = self.w
+        pl, T = synth.draw_lengths(w, 1, rid)[0]
+        st = synth.RequestStream(w, rid, T, device=self.gen)
+        k, v = st.prompt(pl)
+        budget = budget_pages or max(w.budget_pages, -(-pl // w.page_size))
+        gp = self.gpid[prefix] if prefix is not None else -1
+        self.pool.add_request(slot, k.to(self.dev).contiguous() if pl else None,
+                              v.to(self.dev).contiguous() if pl else None, budget, gp)
+        if compare:
+            op = self.opid[prefix] if prefix is not None else -1
+            self.ora.add_request(slot, k.double().cpu().numpy(), v.double().cpu().numpy(), budget, op)
+            self.cmp.add(slot)
+        self.active[slot] = st
+        self.prev_nb[slot] = 0
+        return T
+
+    def free(self, slot):
+        self.pool.free(slot)
+        del self.active[slot]
+        if slot in self.cmp:
+            self.ora.free_request(slot)
+            self.cmp.discard(slot)
+
+    def step(self, check=True):
+        w, rep = self.w, self.rep
+        L, hk, hq, d, P = w.num_layers, w.num_kv_heads, w.num_q_heads, w.head_dim, w.page_size
+        slots = sorted(self.active)
+        qs, ks, vs = [], [], []
+        for s in slots:
+            q, k, v = self.active[s].next_step()
+            qs.append(q); ks.append(k); vs.append(v)
+        q = torch.stack(qs).to(self.dev)
+        k = torch.stack(ks).to(self.dev)
+        v = torch.stack(vs).to(self.dev)
+        slots_dev = torch.tensor(slots, dtype=torch.int32, device=self.dev)
+        outs = []
+        for l in range(L):
+            o = torch.empty(len(slots), hq, d, dtype=w.torch_dtype, device=self.dev)
+            self.pool.decode_step(l, slots_dev, q[:, l].contiguous(), k[:, l].contiguous(),
+                                  v[:, l].contiguous(), o)
+            outs.append(o)
+        self.pool.boundary(slots_dev)
+        self.pool.sync()
+        cslots = sorted(self.cmp)
+        idx = [slots.index(s) for s in cslots]
+        metas, bts = {}, {}
+        for s in cslots:
+            metas[s], bts[s] = self.pool.request(s)
+        st = self.pool.stats()
+        if not self.compare_all and st.denied:
+            rep.fail("the GPU pool ran short of pages: sampled comparison no longer valid")
+        tok_pos = None
+        self.arb.gpu_dec, self.arb.gpu_kept = {}, {}
+        for s in cslots:
+            m = metas[s]
+            if m.n_boundaries > self.prev_nb[s]:
+                self.arb.gpu_dec[s] = m.last_decision
+                if m.last_decision in (COMPACT, COMPACT_DENIED):
+                    tok_pos = self.pool.region("tok_pos")
+                    pos = _private_positions(tok_pos, bts[s][m.n_pre_pages:], m.seq_priv - 1, L, hk, P)
+                    self.arb.gpu_kept[s] = [[set(pos[l, h].tolist()) for h in range(hk)] for l in range(L)]
+        if cslots:
+            qc = q[idx].double().cpu().numpy()
+            kc = k[idx].double().cpu().numpy()
+            vc = v[idx].double().cpu().numpy()
+            res = self.ora.step(cslots, qc, kc, vc, arbiter=self.arb)
+            rep.steps += 1
+            if check:
+                out_g = torch.stack([o[idx].float().cpu() for o in outs], 1).double().numpy()
+                self._compare(res, cslots, out_g, metas, bts, tok_pos)
+        for s in cslots:
+            self.prev_nb[s] = metas[s].n_boundaries
+
+    def _compare(self, res, cslots, out_g, metas, bts, tok_pos):
+        w, rep = self.w, self.rep
+        L, hk, P = w.num_layers, w.num_kv_heads, w.page_size
+        t = rep.steps
+        for ci, s in enumerate(cslots):
+            for l in range(L):
+                ref = res["out"][ci, l]
+                err = np.max(np.abs(out_g[ci, l] - ref)) / max(np.max(np.abs(ref)), 1e-30)
+                rep.max_out_err = max(rep.max_out_err, float(err))
+                if not err <= self.tol:
+                    rep.fail(f"step {t} slot {s} layer {l}: output rel err {err:.3g} > {self.tol}")
+        summ = self.pool.region("summary")[cslots].cpu().numpy()
+        if not np.array_equal(summ, res["summaries"]):
+            rep.fail(f"step {t}: summaries differ")
+        stg = self.pool.region("staging")[cslots][:, :, :, 0].float().cpu().double().numpy()
+        if not np.array_equal(stg, res["staged_k"]):
+            rep.fail(f"step {t}: staged keys differ")
+        wset = None
+        for s in cslots:
+            m, r = metas[s], self.ora.req[s]
+            if m.pos != r.pos or m.n_pages != len(r.pages) or m.seq_priv != r.toks.n:
+                rep.fail(f"step {t} slot {s}: pos/pages/seq {m.pos},{m.n_pages},{m.seq_priv} "
+                         f"vs {r.pos},{len(r.pages)},{r.toks.n}")
+            if self.compare_all and bts[s] != self.ora.block_table(s):
+                rep.fail(f"step {t} slot {s}: block table {bts[s]} vs {self.ora.block_table(s)}")
+            rec = res["records"].get(s)
+            if rec is None:
+                continue
+            rep.boundaries += 1
+            if m.last_decision != rec.decision:
+                rep.fail(f"step {t} slot {s}: decision {m.last_decision} vs {rec.decision}")
+            if rec.decision == GROW:
+                rep.grows += 1
+            elif rec.decision in (COMPACT, COMPACT_DENIED):
+                rep.compacts += 1
+            if self.full_kv:
+                continue
+            if wset is None:
+                wset = self.pool.region("wset").cpu().numpy()
+            wg = wset[s]
+            wo = np.stack([rec.w_short, rec.w_long], -1)
+            near = rec.w_near_tie
+            if not np.array_equal(wg[~near], wo[~near]):
+                rep.fail(f"step {t} slot {s}: W differs outside near-ties")
+            rep.w_in_band += int(np.sum(near & (wg != wo)))
+            if not near.any() and m.delta != rec.delta:
+                rep.fail(f"step {t} slot {s}: delta {m.delta} vs {rec.delta}")
+            if rec.decision in (COMPACT, COMPACT_DENIED):
+                pos = _private_positions(self.pool.region("tok_pos"), bts[s][m.n_pre_pages:],
+                                         m.seq_priv, L, hk, P)
+                if not np.array_equal(np.sort(pos, axis=-1), self.ora.kept_positions(s)):
+                    rep.fail(f"step {t} slot {s}: kept positions differ")

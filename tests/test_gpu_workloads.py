@@ -1,0 +1,159 @@
+"""CUDA path vs the oracle on the larger workloads.
+
+* Continuous batching with shared, refcounted prefixes (the 36-layer
+  Qwen3-shaped workload's features at reduced size): requests join and leave
+  mid-run, slots are reused, prefixes are released; every request and every
+  block table is compared.
+* The three large workloads at their full sizes and in the launch
+  configuration bench.py times (32-layer stack with a 40 GB pool and 64
+  requests; 36-layer stack with shared 2048-token prefixes and 128 request
+  slots; 256 requests all at a boundary in the same step with a 120 GB pool):
+  two sampled requests are simulated by the oracle and compared step by step.
+"""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from tests import gpu_harness
+    from demand_paged_kv_gqa_b300 import growpage, synth
+    return gpu_harness, growpage, synth
+
+
+def _check(rep):
+    assert not rep.failures, "\n".join(rep.failures)
+
+
+def _cb_workload(synth):
+    # Qwen3-8B-shaped heads (32q/8kv, d=128, bf16, RoPE 1e6), 2 layers,
+    # 64-token prefixes shared by groups of 4, prompt = the prefix only,
+    # 2-page initial budget, short lognormal outputs.
+    return synth.WORKLOADS["qwen3_8b_36layer_cb"].replace(
+        num_layers=2, prefix_len=64, prefix_group=4, budget_pages=2, out_median=120,
+        out_min=70, out_max=220, max_pages_per_req=64, top_p=0.9)
+
+
+@pytest.mark.parametrize("full_kv", [False, True])
+def test_continuous_batching_with_shared_prefixes(env, full_kv):
+    H, gp, synth = env
+    w = _cb_workload(synth)
+    mode = gp.GP_MODE_FULL_KV if full_kv else gp.GP_MODE_GROWPAGE
+    sc = H.Scenario(w, max_requests=8, num_pages=400, mode=mode, max_prefixes=16,
+                    max_seq_len=64 + 256 + 16)
+    remaining = {}
+    next_rid = 0
+    users = {}
+
+    def admit(slot, prefix):
+        nonlocal next_rid
+        remaining[slot] = sc.admit(slot, next_rid, prefix=prefix)
+        users[prefix] = users.get(prefix, 0) + 1
+        next_rid += 1
+
+    sc.add_prefix(0)
+    for s in range(4):
+        admit(s, 0)
+    sc.release_prefix(0)            # the creator lets go; requests keep it alive
+    prefix_of = {s: 0 for s in range(4)}
+    next_prefix = 1
+    for t in range(260):
+        if t == 30:                 # a second group arrives
+            sc.add_prefix(next_prefix)
+            for s in range(4, 8):
+                admit(s, next_prefix)
+                prefix_of[s] = next_prefix
+            sc.release_prefix(next_prefix)
+            next_prefix += 1
+        sc.step()
+        if sc.rep.failures:
+            break
+        for s in list(remaining):
+            remaining[s] -= 1
+            if remaining[s] == 0:   # leaves; its slot is reused by a new group
+                sc.free(s)
+                del remaining[s]
+                users[prefix_of[s]] -= 1
+                if t < 200:
+                    if next_prefix not in sc.gpid:
+                        sc.add_prefix(next_prefix)
+                    admit(s, next_prefix)
+                    prefix_of[s] = next_prefix
+                    if users[next_prefix] == 2:
+                        sc.release_prefix(next_prefix)
+                        next_prefix += 1
+        sc.ora.check_invariants()
+    _check(sc.rep)
+    assert sc.rep.boundaries > 20
+    if full_kv:
+        assert sc.rep.compacts == 0
+    else:
+        assert sc.rep.compacts > 0
+
+
+def _run_sampled(sc, steps):
+    try:
+        for _ in range(steps):
+            sc.step()
+            if sc.rep.failures:
+                break
+        _check(sc.rep)
+    finally:
+        torch.cuda.synchronize()
+
+
+def test_llama8b_32layer_full_size_sampled(env):
+    # 32 layers, batch 64, 40 GB pool (19073 pages), the bench's launch shape.
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_32layer"]
+    sc = H.Scenario(w, max_requests=w.batch, num_pages=w.num_pages, compare_all=False,
+                    gen_device="cuda", oracle_pages=256)
+    lens = synth.draw_lengths(w, w.batch)
+    # the two requests with the longest prompts reach their first boundary soonest
+    sampled = sorted(range(w.batch), key=lambda r: -lens[r][0])[:2]
+    for rid in range(w.batch):
+        sc.admit(rid, rid, compare=rid in sampled)
+    need = 1024 - max(lens[r][0] for r in sampled)
+    _run_sampled(sc, min(need + 70, 200))
+    assert sc.rep.boundaries >= 3
+    del sc
+    torch.cuda.empty_cache()
+
+
+def test_qwen3_36layer_full_size_sampled(env):
+    # 36 layers, 128 request slots, 40 GB pool (16954 pages), 2048-token
+    # prefixes shared by groups of 8; initial budget cut to 4 pages so that
+    # the sampled requests reach boundaries within the window.
+    H, gp, synth = env
+    w = synth.WORKLOADS["qwen3_8b_36layer_cb"].replace(budget_pages=4)
+    sc = H.Scenario(w, max_requests=w.batch, num_pages=w.num_pages, compare_all=False,
+                    gen_device="cuda", oracle_pages=512, max_prefixes=8)
+    sc.add_prefix(0, compare=True)
+    sc.add_prefix(1, compare=False)
+    for rid in range(16):
+        sc.admit(rid, rid, compare=rid in (0, 5), prefix=rid // 8)
+    _run_sampled(sc, 100)
+    assert sc.rep.boundaries >= 4
+    del sc
+    torch.cuda.empty_cache()
+
+
+def test_stress_burst_full_size_sampled(env):
+    # 256 requests, prompts of exactly the initial budget: all at a boundary
+    # on the first step and every 16th after it; 120 GB pool (57220 pages).
+    H, gp, synth = env
+    w = synth.WORKLOADS["stress_burst"]
+    sc = H.Scenario(w, max_requests=w.batch, num_pages=w.num_pages, compare_all=False,
+                    gen_device="cuda", oracle_pages=256)
+    for rid in range(w.batch):
+        sc.admit(rid, rid, compare=rid in (3, 200))
+    _run_sampled(sc, 34)
+    assert sc.rep.boundaries == 2 * 3
+    st = sc.pool.stats()
+    assert st.boundaries == 256 * 3
+    del sc
+    torch.cuda.empty_cache()
