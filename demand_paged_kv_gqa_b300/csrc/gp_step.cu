@@ -266,13 +266,26 @@ __device__ int topp_radix(EF e_at, int R, unsigned long long thr, SelShared& sh)
     for (int d = threadIdx.x; d < 256; d += blockDim.x) { sh.cnt[d] = 0u; sh.mass[d] = 0ull; }
     if (threadIdx.x == 0) { sh.pick_d = 0u; sh.pick_a = 0ull; sh.pick_b = 0ull; }
     __syncthreads();
-    for (int j = threadIdx.x; j < R; j += blockDim.x) {
-      const float e = e_at(j);
-      const uint32_t bits = __float_as_uint(e);
-      if ((bits & pmask) == prefix) {
-        const int d = (bits >> shift) & 255;
-        atomicAdd(&sh.cnt[d], 1u);
-        atomicAdd(&sh.mass[d], mass_q(e));
+    // Most weights share their top digits, so lanes with the same digit are
+    // combined inside the warp first and one lane per digit does the atomics.
+    for (int base = 0; base < R; base += blockDim.x) {
+      const int j = base + threadIdx.x;
+      int d = 256;  // "no digit"
+      unsigned long long mq = 0ull;
+      if (j < R) {
+        const float e = e_at(j);
+        const uint32_t bits = __float_as_uint(e);
+        if ((bits & pmask) == prefix) {
+          d = (bits >> shift) & 255;
+          mq = mass_q(e);
+        }
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, d);
+      const unsigned int hi = __reduce_add_sync(peers, (unsigned int)(mq >> 20));
+      const unsigned int lo = __reduce_add_sync(peers, (unsigned int)(mq & 0xfffffull));
+      if (d < 256 && (threadIdx.x & 31) == __ffs(peers) - 1) {
+        atomicAdd(&sh.cnt[d], (unsigned int)__popc(peers));
+        atomicAdd(&sh.mass[d], ((unsigned long long)hi << 20) + (unsigned long long)lo);
       }
     }
     __syncthreads();
@@ -352,10 +365,17 @@ __device__ unsigned long long kth_smallest(const KF& key_of, int C, int k, SelSh
     const int shift = 56 - 8 * pass;
     for (int d = threadIdx.x; d < 256; d += blockDim.x) sh.cnt[d] = 0u;
     __syncthreads();
-    for (int s = threadIdx.x; s < C; s += blockDim.x) {
-      bool cand;
-      const unsigned long long key = key_of(s, &cand);
-      if (cand && (key & pmask) == prefix) atomicAdd(&sh.cnt[(key >> shift) & 255], 1u);
+    for (int base = 0; base < C; base += blockDim.x) {
+      const int s = base + threadIdx.x;
+      int d = 256;
+      if (s < C) {
+        bool cand;
+        const unsigned long long key = key_of(s, &cand);
+        if (cand && (key & pmask) == prefix) d = (int)((key >> shift) & 255);
+      }
+      const unsigned int peers = __match_any_sync(0xffffffffu, d);
+      if (d < 256 && (threadIdx.x & 31) == __ffs(peers) - 1)
+        atomicAdd(&sh.cnt[d], (unsigned int)__popc(peers));
     }
     __syncthreads();
     if (threadIdx.x == 0) {
