@@ -95,7 +95,9 @@ const char* check_config(const gp_config* c) {
   if (c->max_prefixes < 0 || c->max_prefix_len < 0 || c->max_prefix_len % c->page_size)
     return "max_prefix_len must be a non-negative multiple of page_size";
   if (c->max_seq_len < 1) return "bad max_seq_len";
-  if (c->mode != GP_MODE_GROWPAGE && c->mode != GP_MODE_FULL_KV) return "unknown mode";
+  if (c->mode < GP_MODE_GROWPAGE || c->mode > GP_MODE_RANDOM) return "unknown mode";
+  if (c->mode == GP_MODE_RANDOM && !(c->random_grow_rate >= 0.f && c->random_grow_rate <= 1.f))
+    return "random_grow_rate must be in [0, 1]";
   if (c->recent_window < 0) return "recent_window < 0";
   if (!(c->beta_s >= 0.f && c->beta_s < 1.f && c->beta_l >= 0.f && c->beta_l < 1.f))
     return "betas must be in [0, 1)";
@@ -127,7 +129,7 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   l->req = take(R * sizeof(gp_req_meta));
   l->summary = take(R * L * Hk * 2 * D * 4);
   l->staging = take(R * L * Hk * 2 * D * eb);
-  l->logits = take(c->mode == GP_MODE_GROWPAGE ? R * L * Hk * 2 * (uint64_t)l->logit_width * 4 : 0);
+  l->logits = take(c->mode != GP_MODE_FULL_KV ? R * L * Hk * 2 * (uint64_t)l->logit_width * 4 : 0);
   l->wset = take(R * L * Hk * 2 * 4);
   l->free_stack = take((uint64_t)c->num_pages * 4);
   l->ctrl = take(sizeof(gp_ctrl));
@@ -159,6 +161,7 @@ void fill_dev(gp_pool* p) {
   d.block_width = l.block_width; d.logit_width = l.logit_width; d.max_seq_len = c.max_seq_len;
   d.dtype = c.dtype; d.mode = c.mode; d.recent_window = c.recent_window;
   d.beta_s = c.beta_s; d.beta_l = c.beta_l; d.top_p = c.top_p; d.tau = c.tau;
+  d.random_grow_rate = c.random_grow_rate;
   d.rope = c.rope_theta != 0.0 ? 1 : 0;
   d.elem_bytes = c.dtype == GP_DTYPE_BF16 ? 2 : 4;
   d.half_bytes = (uint64_t)c.page_size * c.head_dim * d.elem_bytes;
@@ -485,7 +488,7 @@ int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev) {
     return fail(pool, GP_ERR_INVALID, "gp_boundary must get the step's slot list");
   pool->next_layer = 0;
   if (n == 0) return GP_OK;
-  if (pool->cfg.mode == GP_MODE_GROWPAGE)
+  if (pool->cfg.mode != GP_MODE_FULL_KV)
     GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, pool->stream));
   GP_LAUNCH(pool, gp::launch_decide(pool->dev, pool->stream));
   GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, pool->stream));

@@ -31,6 +31,7 @@ struct PoolDev {
   int32_t block_width, logit_width, max_seq_len, dtype, mode, recent_window;
   int32_t num_workers;
   float beta_s, beta_l, top_p, tau;
+  float random_grow_rate;
   int32_t rope;  // 1: rotary embedding on
   int32_t elem_bytes;
   uint64_t page_bytes, layer_bytes, head_bytes, half_bytes;  // kv strides

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
         int flags = 0;
         if (at_b) flags |= kPlanBoundary;
         if (m.steps == 0) flags |= kPlanFirst;
-        if (at_b && p.mode == GP_MODE_GROWPAGE) flags |= kPlanScore;
+        if (at_b && p.mode != GP_MODE_FULL_KV) flags |= kPlanScore;
         isb = (flags & kPlanScore) ? 1 : 0;
         p.plan_slot[i] = slot; p.plan_R[i] = R; p.plan_nb[i] = nb; p.plan_flags[i] = flags;
         p.plan_pos[i] = m.pos;
@@ -525,6 +525,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(PoolDev p) {
 
 // -------------------------------------------------------------- decide ---
 
+// SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+// generators", 2014): the output for state x.
+__device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
 __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
   __shared__ int s_warp[33];
   __shared__ int s_avail;
@@ -544,9 +553,17 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
       m = p.req[slot];
       at_b = (p.plan_flags[i] & kPlanBoundary) != 0;
       if (at_b) {
-        want = (p.mode == GP_MODE_GROWPAGE)
-                   ? ((double)p.plan_delta[i] > (double)p.tau ? 1 : 0)
-                   : 1;
+        const double delta = (double)p.plan_delta[i];
+        switch (p.mode) {
+          case GP_MODE_GROWPAGE: want = delta > (double)p.tau; break;
+          case GP_MODE_FULL_KV: want = 1; break;
+          case GP_MODE_FIXED: want = 0; break;
+          case GP_MODE_INVERSE: want = -delta > (double)p.tau; break;
+          default: {  // GP_MODE_RANDOM
+            const uint64_t x = ((uint64_t)(uint32_t)slot << 32) | (uint32_t)m.n_boundaries;
+            want = (double)(splitmix64(x) >> 11) * 0x1p-53 < (double)p.random_grow_rate;
+          }
+        }
         wg = (want && m.n_pages < p.max_pages_per_req) ? 1 : 0;
       }
     }
@@ -563,7 +580,7 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
         m.n_grows += 1;
         atomicAdd(&s_cnt[1], 1ull);
       } else if (at_b) {
-        if (p.mode == GP_MODE_GROWPAGE) {
+        if (p.mode != GP_MODE_FULL_KV) {
           dec = want ? kCompactDenied : kCompact;
           commit = C - p.P;
           m.n_compacts += 1;

@@ -165,7 +165,8 @@ class Engine:
         return self._slots_dev
 
     def step(self, timed=False, before_step: Optional[Callable] = None,
-             after_layer: Optional[Callable] = None, after_step: Optional[Callable] = None):
+             after_layer: Optional[Callable] = None, after_step: Optional[Callable] = None,
+             before_layer: Optional[Callable] = None):
         """One decode step for the active slots; returns the number of tokens."""
         if self.full_kv:
             self._preempt_for_step()
@@ -183,6 +184,8 @@ class Engine:
         if before_step:
             before_step()
         for l in range(L):
+            if before_layer:
+                before_layer(l)
             self.pool.decode_step(l, slots_dev, q[l], k[l], v[l], self.out[l, :n])
             if after_layer:
                 after_layer(l)

@@ -20,7 +20,7 @@ LIB_PATH = os.environ.get("GROWPAGE_LIB") or os.path.join(_HERE, "libgrowpage.so
 
 GP_OK, GP_ERR_INVALID, GP_ERR_NO_PAGES, GP_ERR_CUDA, GP_ERR_DEVICE = 0, 1, 2, 3, 4
 GP_DTYPE_F32, GP_DTYPE_BF16 = 0, 1
-GP_MODE_GROWPAGE, GP_MODE_FULL_KV = 0, 1
+GP_MODE_GROWPAGE, GP_MODE_FULL_KV, GP_MODE_FIXED, GP_MODE_INVERSE, GP_MODE_RANDOM = 0, 1, 2, 3, 4
 DEC_NONE, DEC_GROW, DEC_COMPACT, DEC_COMPACT_DENIED, DEC_STARVED = 0, 1, 2, 3, 4
 
 
@@ -32,7 +32,7 @@ class gp_config(ctypes.Structure):
         ("beta_s", ctypes.c_float), ("beta_l", ctypes.c_float),
         ("top_p", ctypes.c_float), ("tau", ctypes.c_float),
         ("rope_theta", ctypes.c_double), ("flags", ctypes.c_int32),
-        ("reserved", ctypes.c_int32)]
+        ("random_grow_rate", ctypes.c_float)]
 
 
 class gp_layout(ctypes.Structure):
@@ -125,7 +125,7 @@ def make_config(*, num_layers, num_q_heads, num_kv_heads, head_dim, page_size,
                 num_pages, max_requests, max_pages_per_req, dtype, max_seq_len,
                 max_prefixes=0, max_prefix_len=0, mode=GP_MODE_GROWPAGE,
                 recent_window=64, beta_s=0.9, beta_l=0.999, top_p=0.9, tau=0.0,
-                rope_theta=0.0) -> gp_config:
+                rope_theta=0.0, random_grow_rate=0.0) -> gp_config:
     c = gp_config()
     c.num_layers, c.num_q_heads, c.num_kv_heads = num_layers, num_q_heads, num_kv_heads
     c.head_dim, c.page_size, c.num_pages = head_dim, page_size, num_pages
@@ -135,6 +135,7 @@ def make_config(*, num_layers, num_q_heads, num_kv_heads, head_dim, page_size,
     c.mode, c.recent_window = mode, recent_window
     c.beta_s, c.beta_l, c.top_p, c.tau = beta_s, beta_l, top_p, tau
     c.rope_theta, c.flags = rope_theta, 0
+    c.random_grow_rate = random_grow_rate
     return c
 
 
@@ -262,7 +263,7 @@ class Pool:
 
 
 def config_for(w, mode=GP_MODE_GROWPAGE, max_requests=None, num_pages=None,
-               max_seq_len=None, max_prefixes=None) -> gp_config:
+               max_seq_len=None, max_prefixes=None, random_grow_rate=0.0) -> gp_config:
     """gp_config for a synth.Workload."""
     max_out = max(w.decode_steps, w.out_max)
     seq = max_seq_len or (w.prefix_len + w.prompt_max + max_out + 16)
@@ -279,4 +280,4 @@ def config_for(w, mode=GP_MODE_GROWPAGE, max_requests=None, num_pages=None,
         dtype=GP_DTYPE_F32 if w.dtype == "f32" else GP_DTYPE_BF16, max_seq_len=seq,
         max_prefixes=max_prefixes, max_prefix_len=w.prefix_len, mode=mode,
         recent_window=w.recent_window, beta_s=w.beta_s, beta_l=w.beta_l, top_p=w.top_p,
-        tau=w.tau, rope_theta=w.rope_theta)
+        tau=w.tau, rope_theta=w.rope_theta, random_grow_rate=random_grow_rate)

@@ -68,6 +68,17 @@ extern "C" {
 
 #define GP_MODE_GROWPAGE 0 /* grow or compact at each boundary            */
 #define GP_MODE_FULL_KV  1 /* every boundary grows; no scoring, no compaction */
+/* Ablation policies on the same kernels ("GrowPage: On-Demand KV Budgeting
+ * for Efficient LLM Reasoning Serving", evolve.pub review: the frequency-
+ * matched random policy and the inverted signal of Tables 8-9, and the
+ * fixed-budget compressed-paging baseline it compares against).  Scoring,
+ * Top-p counts and compaction are those of GP_MODE_GROWPAGE; only the grow
+ * decision differs. */
+#define GP_MODE_FIXED    2 /* never grow: every boundary compacts          */
+#define GP_MODE_INVERSE  3 /* grow iff -Delta > tau (the signal reversed)  */
+#define GP_MODE_RANDOM   4 /* grow iff u < random_grow_rate, u uniform in [0,1)
+                              from SplitMix64 of (slot << 32 | boundaries
+                              seen so far by the request), top 53 bits */
 
 typedef struct gp_config {
   int32_t num_layers;        /* L */
@@ -90,7 +101,7 @@ typedef struct gp_config {
   float tau;                 /* grow iff Delta > tau */
   double rope_theta;         /* 0: no rotary embedding */
   int32_t flags;             /* reserved, must be 0 */
-  int32_t reserved;
+  float random_grow_rate;    /* GP_MODE_RANDOM: grow probability in [0, 1] */
 } gp_config;
 
 /* ---- device layout of the pool buffer -------------------------------- */

@@ -101,3 +101,27 @@ def compaction_plan(imp_priv: np.ndarray, pos_priv: np.ndarray, pos_now: int,
         b = imp_priv[cand[order[n_drop]]]       # smallest kept
         gap = abs(b - a) / max(b, 1e-300)
     return dropped, gap
+
+
+MASK64 = (1 << 64) - 1
+
+
+def splitmix64(x: int) -> int:
+    """SplitMix64 output for state x (Steele, Lea and Flood, "Fast splittable
+    pseudorandom number generators", OOPSLA 2014), in exact integer arithmetic."""
+    z = (x + 0x9E3779B97F4A7C15) & MASK64
+    z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+    z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+    return z ^ (z >> 31)
+
+
+def random_grow(slot: int, boundaries_seen: int, rate: float) -> bool:
+    """Frequency-matched random policy: grow iff u < rate, u = the top 53
+    bits of SplitMix64(slot << 32 | boundaries seen so far) scaled to [0, 1).
+
+    Reading: the review's GROWPAGE-RANDOM (Tables 8-9) draws decisions at the
+    measured grow frequency; the pages do not say how, so a counter-based
+    generator keyed by the request and its boundary count is used."""
+    x = ((slot & 0xFFFFFFFF) << 32) | (boundaries_seen & 0xFFFFFFFF)
+    u = (splitmix64(x) >> 11) * 2.0 ** -53
+    return u < float(rate)

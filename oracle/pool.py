@@ -70,13 +70,17 @@ class OracleConfig:
     beta_l: float = 0.999
     tau: float = 0.0
     full_kv: bool = False
+    # grow decision at a boundary: "growpage" (Delta > tau), "fixed" (never),
+    # "inverse" (-Delta > tau) or "random" (see policy.random_grow)
+    policy: str = "growpage"
+    random_grow_rate: float = 0.0
 
     @property
     def group(self):
         return self.num_q_heads // self.num_kv_heads
 
     @staticmethod
-    def from_workload(w, full_kv=False, **over):
+    def from_workload(w, full_kv=False, **over):  # noqa: D401
         kw = dict(num_layers=w.num_layers, num_q_heads=w.num_q_heads,
                   num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                   page_size=w.page_size, num_pages=w.num_pages,
@@ -123,6 +127,7 @@ class OracleRequest:
     toks: _Grow
     s_short: np.ndarray     # fp32 [L][Hk][d]
     s_long: np.ndarray
+    boundaries: int = 0     # capacity boundaries met so far
 
 
 @dataclasses.dataclass
@@ -331,10 +336,22 @@ class OraclePool:
                         W[l, g] = pol.topp_count(pr, c.top_p)
                         band[l, g, X] = pol.topp_range(pr, c.top_p)
             delta = pol.demand_delta(ws, wl)
-            want = pol.wants_grow(delta, c.tau)
             dmin = int(np.sum(band[:, :, 0, 0] - band[:, :, 1, 1]))
             dmax = int(np.sum(band[:, :, 0, 1] - band[:, :, 1, 0]))
-            exempt = pol.wants_grow(dmin, c.tau) != pol.wants_grow(dmax, c.tau)
+            if c.policy == "growpage":
+                want = pol.wants_grow(delta, c.tau)
+                exempt = pol.wants_grow(dmin, c.tau) != pol.wants_grow(dmax, c.tau)
+            elif c.policy == "inverse":
+                want = pol.wants_grow(-delta, c.tau)
+                exempt = pol.wants_grow(-dmin, c.tau) != pol.wants_grow(-dmax, c.tau)
+            elif c.policy == "fixed":
+                want, exempt = False, False
+            elif c.policy == "random":
+                want = pol.random_grow(slot, r.boundaries, c.random_grow_rate)
+                exempt = False
+            else:
+                raise ValueError(c.policy)
+            r.boundaries += 1
             can = len(r.pages) < c.max_pages_per_req
             if arbiter is not None and exempt:
                 # near-tie: the checker may adopt the other side of the rule

@@ -74,6 +74,15 @@ class _Arbiter:
         return gd
 
 
+def oracle_config(w, mode, num_pages, random_grow_rate=0.0):
+    """The oracle's configuration for a GPU pool mode."""
+    policy = {gpb.GP_MODE_GROWPAGE: "growpage", gpb.GP_MODE_FULL_KV: "growpage",
+              gpb.GP_MODE_FIXED: "fixed", gpb.GP_MODE_INVERSE: "inverse",
+              gpb.GP_MODE_RANDOM: "random"}[mode]
+    return OracleConfig.from_workload(w, full_kv=mode == gpb.GP_MODE_FULL_KV, num_pages=num_pages,
+                                      policy=policy, random_grow_rate=random_grow_rate)
+
+
 def _private_positions(tok_pos, bt_priv: List[int], n: int, L: int, hk: int, P: int):
     """[L][Hk][n] positions of the first n private slots (block-table order).
 
@@ -94,15 +103,16 @@ def _private_positions(tok_pos, bt_priv: List[int], n: int, L: int, hk: int, P: 
 class Harness:
     def __init__(self, w: synth.Workload, n_req: int, mode=gpb.GP_MODE_GROWPAGE,
                  num_pages: Optional[int] = None, max_seq_len: Optional[int] = None,
-                 tol: Optional[float] = None, budget_pages: Optional[int] = None):
+                 tol: Optional[float] = None, budget_pages: Optional[int] = None,
+                 random_grow_rate: float = 0.0):
         self.w = w
         self.n = n_req
         self.full_kv = mode == gpb.GP_MODE_FULL_KV
         npages = num_pages or w.num_pages
         self.cfg = gpb.config_for(w, mode=mode, max_requests=n_req, num_pages=npages,
-                                  max_seq_len=max_seq_len)
+                                  max_seq_len=max_seq_len, random_grow_rate=random_grow_rate)
         self.pool = gpb.Pool(self.cfg)
-        self.ora = OraclePool(OracleConfig.from_workload(w, full_kv=self.full_kv, num_pages=npages))
+        self.ora = OraclePool(oracle_config(w, mode, npages, random_grow_rate))
         self.tol = tol if tol is not None else (1e-4 if w.dtype == "f32" else 2e-2)
         self.rep = Report()
         self.arb = _Arbiter(self.rep)

@@ -104,3 +104,35 @@ def test_pool_exhaustion_compacts_instead(env):
     rep = h.run(100)
     _check(rep)
     assert rep.grows == 2 and rep.compacts >= 4
+
+
+@pytest.mark.parametrize("mode_name,rate", [("FIXED", 0.0), ("INVERSE", 0.0), ("RANDOM", 0.3)])
+def test_ablation_policies(env, mode_name, rate):
+    # the review's ablation policies on the same kernels: fixed budget,
+    # inverted signal, frequency-matched random decisions
+    H, gp, synth = env
+    mode = getattr(gp, "GP_MODE_" + mode_name)
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=100, prompt_max=128, budget_pages=8,
+                                                  max_pages_per_req=20)
+    h = H.Harness(w, 6, mode=mode, budget_pages=8, random_grow_rate=rate)
+    rep = h.run(260)
+    _check(rep)
+    assert rep.boundaries > 30
+    if mode_name == "FIXED":
+        assert rep.grows == 0
+    else:
+        assert rep.grows > 0 and rep.compacts > 0
+    t = H.Harness(synth.WORKLOADS["tiny"], 1, mode=mode, random_grow_rate=rate)
+    _check(t.run(200))
+
+
+def test_review_hyperparameters_page_256(env):
+    # the authors' settings: KV block 256 tokens, Top-p 0.99, retention 64
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(page_size=256, top_p=0.99, recent_window=64,
+                                                  prompt_min=480, prompt_max=512, budget_pages=2,
+                                                  num_pages=64, max_pages_per_req=8)
+    h = H.Harness(w, 6, budget_pages=2)
+    rep = h.run(300)
+    _check(rep)
+    assert rep.boundaries >= 12

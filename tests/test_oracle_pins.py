@@ -402,3 +402,52 @@ def test_pool_summaries_follow_closed_form_of_group_means():
         ref = _closed_form(qs, float(np.float32(beta)))
         got = res["summaries"][0, 0, :, X]
         assert np.max(np.abs(got - ref)) < 2e-5 * np.max(np.abs(ref))
+
+
+# ----------------------------------------------------- ablation policies ----
+
+def test_splitmix64_published_outputs():
+    with open(os.path.join(HERE, "golden", "splitmix64.json")) as f:
+        g = json.load(f)
+    golden = 0x9E3779B97F4A7C15
+    for k, want in enumerate(g["outputs_from_state_0"]):
+        # next() advances the state by the golden gamma, then mixes
+        assert pol.splitmix64((k * golden) & pol.MASK64) == int(want, 16)
+
+
+def test_random_policy_frequency():
+    for rate in (0.0, 0.3, 1.0):
+        n = 20000
+        grows = sum(pol.random_grow(s, b, rate) for s in range(40) for b in range(n // 40))
+        if rate in (0.0, 1.0):
+            assert grows == int(rate * n)
+        else:
+            assert abs(grows / n - rate) < 4 * math.sqrt(rate * (1 - rate) / n)
+
+
+def _first_decision(policy, seed=21, **kw):
+    cfg = _small_cfg(num_pages=40, policy=policy, **kw)
+    rng = np.random.default_rng(seed)
+    pool = OraclePool(cfg)
+    L, hk, hq, d = cfg.num_layers, cfg.num_kv_heads, cfg.num_q_heads, cfg.head_dim
+    # 20 prompt tokens in a 2-page budget: the first boundary comes at step
+    # 13, after the summaries have diverged
+    pool.add_request(0, rng.standard_normal((L, 20, hk, d)), rng.standard_normal((L, 20, hk, d)), 2)
+    for t in range(40):
+        res = pool.step([0], rng.standard_normal((1, L, hq, d)), rng.standard_normal((1, L, hk, d)),
+                        rng.standard_normal((1, L, hk, d)))
+        if res["records"]:
+            return res["records"][0]
+    raise AssertionError("no boundary")
+
+
+def test_inverse_and_fixed_policies_at_the_first_boundary():
+    # the three policies see the same inputs up to their first boundary,
+    # hence the same scores and the same Delta
+    g = _first_decision("growpage")
+    inv = _first_decision("inverse")
+    fx = _first_decision("fixed")
+    assert g.delta == inv.delta == fx.delta != 0
+    assert (g.decision == GROW) == (g.delta > 0)
+    assert (inv.decision == GROW) == (inv.delta < 0)
+    assert fx.decision == COMPACT
