@@ -54,6 +54,8 @@ def parse():
                     help="override the layer count (small profiling cases)")
     ap.add_argument("--pool-gb", type=float, default=0.0,
                     help="override the page-pool size in GB (small profiling cases)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch size (small profiling cases)")
     return ap.parse_args()
 
 
@@ -63,6 +65,8 @@ def workload_for(args):
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = w.replace(num_layers=args.layers)
+    if args.batch:
+        w = w.replace(batch=args.batch)
     if args.layers or args.pool_gb:
         gb = args.pool_gb or (w.num_pages * 2 * w.num_kv_heads * w.page_size * w.head_dim
                               * w.elem_bytes * synth.WORKLOADS[args.workload].num_layers / 1e9)
@@ -288,16 +292,19 @@ def run_ours(args, ws, rank, local):
         out["bytes_per_launch"] = nbytes
         return out
 
-    def measure_e2e(eng, k):
+    def measure_e2e(eng, k, chunk=8):
         """Same metric through the C-ABI with each step's q, k, v copied from
         pinned host memory and its outputs copied back to pinned host memory,
-        all copies inside the events.  The copies run on a second stream, per
-        layer: layer l waits only for its own inputs, and its output goes back
-        while layer l+1 computes (what a serving loop over the per-layer call
-        does)."""
+        all copies inside the events.  The copies run on a second stream in
+        chunks of `chunk` layers: a chunk's inputs are copied ahead, the
+        compute stream waits once per chunk, and a chunk's outputs go back
+        while the next chunk computes (what a serving loop over the per-layer
+        call does; waiting before every layer would break the programmatic
+        chaining of the layer kernels)."""
         stream = eng.pool.stream
         copy = torch.cuda.Stream(device=dev)
         L = w.num_layers
+        chunks = [(c, min(c + chunk, L)) for c in range(0, L, chunk)]
         hq_ = torch.empty_like(eng.q, device="cpu").pin_memory()
         hk_ = torch.empty_like(eng.k, device="cpu").pin_memory()
         hv_ = torch.empty_like(eng.v, device="cpu").pin_memory()
@@ -310,27 +317,30 @@ def run_ours(args, ws, rank, local):
             torch.cuda.synchronize()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
-            in_ready = [torch.cuda.Event() for _ in range(L)]
-            out_ready = [torch.cuda.Event() for _ in range(L)]
+            in_ready = {c0: torch.cuda.Event() for c0, _ in chunks}
+            out_ready = {c1 - 1: torch.cuda.Event() for _, c1 in chunks}
 
             def before():
                 e0.record(stream)
                 copy.wait_event(e0)
                 with torch.cuda.stream(copy):
-                    for l in range(L):
-                        eng.q[l].copy_(hq_[l], non_blocking=True)
-                        eng.k[l].copy_(hk_[l], non_blocking=True)
-                        eng.v[l].copy_(hv_[l], non_blocking=True)
-                        in_ready[l].record(copy)
+                    for c0, c1 in chunks:
+                        eng.q[c0:c1].copy_(hq_[c0:c1], non_blocking=True)
+                        eng.k[c0:c1].copy_(hk_[c0:c1], non_blocking=True)
+                        eng.v[c0:c1].copy_(hv_[c0:c1], non_blocking=True)
+                        in_ready[c0].record(copy)
 
             def before_layer(l):
-                stream.wait_event(in_ready[l])
+                if l in in_ready:
+                    stream.wait_event(in_ready[l])
 
             def after_layer(l):
-                out_ready[l].record(stream)
-                copy.wait_event(out_ready[l])
-                with torch.cuda.stream(copy):
-                    ho_[l].copy_(eng.out[l], non_blocking=True)
+                if l in out_ready:
+                    c0 = max(c for c, _ in chunks if c <= l)
+                    out_ready[l].record(stream)
+                    copy.wait_event(out_ready[l])
+                    with torch.cuda.stream(copy):
+                        ho_[c0:l + 1].copy_(eng.out[c0:l + 1], non_blocking=True)
 
             def after():
                 done = torch.cuda.Event()
