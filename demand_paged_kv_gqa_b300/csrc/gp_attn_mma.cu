@@ -134,14 +134,17 @@ __device__ __forceinline__ void issue_block_tma(const PoolDev& p, const CUtensor
 // Besides K/V blocks, a warp's ring carries one "meta" item in front of each
 // piece: what the piece needs besides the keys, copied by the bulk-copy
 // engine with the blocks.  Offsets inside a stage:
-constexpr int kMetaQ = 0;       // the G query rows, bf16 (<= 1024 B)
-constexpr int kMetaK = 1024;    // the step's new key, bf16
-constexpr int kMetaV = 1280;    // the step's new value, bf16
-constexpr int kMetaS = 1536;    // short and long summary before this step, fp32
-constexpr int kMetaC32 = 2560;  // rotary cos / sin rows of the position, fp32
-constexpr int kMetaS32 = 2816;
-constexpr int kMetaC64 = 3072;  // the same rows in fp64
-constexpr int kMetaS64 = 3584;
+constexpr int kQPitch = kMmaD + 8;  // query row pitch (elements): 272-byte rows put the
+                                    // G rows' pair loads in different banks
+constexpr int kMetaQ = 0;       // the G query rows, bf16 (<= 4 x 272 B)
+constexpr int kMetaK = 1088;    // the step's new key, bf16
+constexpr int kMetaV = 1344;    // the step's new value, bf16
+constexpr int kMetaS = 1600;    // short and long summary before this step, fp32
+constexpr int kMetaC32 = 2624;  // rotary cos / sin rows of the position, fp32
+constexpr int kMetaS32 = 2880;
+constexpr int kMetaC64 = 3136;  // the same rows in fp64
+constexpr int kMetaS64 = 3648;
+constexpr int kMetaSF = 4352;   // written in place: both summaries after this step's fold
 
 // Per-warp extra buffer (after ob): the staged-token score of each query
 // head and the staged value (fp32), for finishing a piece in place.
@@ -201,7 +204,9 @@ __device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, i
   constexpr int D = kMmaD;
   const uint32_t bytes = G * D * 2 + 2 * D * 2 + 2 * D * 4 + (p.rope ? D * 4 + D * 8 : 0);
   mbar_expect_tx(bar, bytes);
-  bulk_g2s(st + kMetaQ, q + ((size_t)i * p.Hq + h * G) * D, G * D * 2, bar);
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    bulk_g2s(st + kMetaQ + g * kQPitch * 2, q + ((size_t)i * p.Hq + h * G + g) * D, D * 2, bar);
   bulk_g2s(st + kMetaK, knew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
   bulk_g2s(st + kMetaV, vnew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
   bulk_g2s(st + kMetaS, p.summary + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * D, 2 * D * 4, bar);
@@ -215,7 +220,7 @@ __device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, i
 
 // Pointers to what a piece needs (a meta item in shared memory).
 struct PieceIn {
-  const __nv_bfloat16* q;  // [G][d]
+  const __nv_bfloat16* q;  // [G][kQPitch]
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   const float* s;          // [2][d] before this step
@@ -223,19 +228,56 @@ struct PieceIn {
   const float* s32;
   const double* c64;
   const double* s64;
+  const float* sf;         // [2][d] after this step's fold (set when needed)
 };
 
-// fp32 fold of the step's query mean into summary X at dim di (exact order):
-// q̄ = (sum of the G heads in head order) / G; s' = fl(fl(b*s) + fl((1-b)*q̄)),
-// or q̄ on the request's first step.
+// Both summaries after this step's fold, all d dims (4 per lane), in fp32 and
+// in exact order: q̄ = (sum of the G heads in head order) / G;
+// s' = fl(fl(b*s) + fl((1-b)*q̄)), or q̄ on the request's first step.
 template <int G>
-__device__ __forceinline__ float fold_at(const PieceIn& in, int X, int di, float beta, int first) {
-  float qb = __bfloat162float(in.q[di]);
+__device__ __forceinline__ void fold_rows(const PoolDev& p, const PieceIn& in, int flags, int lane,
+                                          float* sf) {
+  constexpr int D = kMmaD;
+  const int d0 = lane * 4;
+  float qb[4];
 #pragma unroll
-  for (int g = 1; g < G; ++g) qb = __fadd_rn(qb, __bfloat162float(in.q[g * kMmaD + di]));
-  const float qm = __fdiv_rn(qb, (float)G);
-  if (first) return qm;
-  return __fadd_rn(__fmul_rn(beta, in.s[X * kMmaD + di]), __fmul_rn(__fsub_rn(1.0f, beta), qm));
+  for (int g = 0; g < G; ++g) {
+    const uint2 w = *reinterpret_cast<const uint2*>(in.q + g * kQPitch + d0);
+    const float v[4] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y)};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qb[e] = g == 0 ? v[e] : __fadd_rn(qb[e], v[e]);
+  }
+  const float4 os = *reinterpret_cast<const float4*>(in.s + d0);
+  const float4 ol = *reinterpret_cast<const float4*>(in.s + D + d0);
+  const float osv[4] = {os.x, os.y, os.z, os.w}, olv[4] = {ol.x, ol.y, ol.z, ol.w};
+  const float aS = __fsub_rn(1.0f, p.beta_s), aL = __fsub_rn(1.0f, p.beta_l);
+  const int first = flags & kPlanFirst;
+  float ns[4], nl[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float qm = __fdiv_rn(qb[e], (float)G);
+    ns[e] = first ? qm : __fadd_rn(__fmul_rn(p.beta_s, osv[e]), __fmul_rn(aS, qm));
+    nl[e] = first ? qm : __fadd_rn(__fmul_rn(p.beta_l, olv[e]), __fmul_rn(aL, qm));
+  }
+  *reinterpret_cast<float4*>(sf + d0) = make_float4(ns[0], ns[1], ns[2], ns[3]);
+  *reinterpret_cast<float4*>(sf + D + d0) = make_float4(nl[0], nl[1], nl[2], nl[3]);
+}
+
+// Pair of fp32 values -> packed bf16 (hi) and the packed rounded residual.
+__device__ __forceinline__ void split2x(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+__device__ __forceinline__ void split3x(float a, float b, uint32_t& hi, uint32_t& mid, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float ra = a - __low2float(h), rb = b - __high2float(h);
+  const __nv_bfloat162 m = __floats2bfloat162_rn(ra, rb);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(ra - __low2float(m), rb - __high2float(m));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  mid = *reinterpret_cast<const uint32_t*>(&m);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // The tensor-core operand rows of lane (g = lane / 4, t = lane % 4): rows
@@ -253,65 +295,51 @@ __device__ __forceinline__ void build_rows(const PoolDev& p, const PieceIn& in, 
   const bool head_row = g < G;
   const bool sum_row = (flags & kPlanScore) && g >= 4;
   if (!(head_row || sum_row)) return;
-  const int X = g & 1, first = flags & kPlanFirst;
-  const float beta = X ? p.beta_l : p.beta_s;
+  const int X = g & 1;
   const float sc = head_row ? 1.4426950408889634f / sqrtf((float)D)   // log2(e)/sqrt(d)
                             : 1.0f / sqrtf((float)D);
 #pragma unroll
   for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {  // dims 16kk+2t+8*half, +1
-      float x[2], y[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int di = 16 * kk + 2 * t + 8 * half + u;  // < 64; partner di + 64
-        float a, b;
-        if (head_row) {
-          a = __bfloat162float(in.q[g * D + di]);
-          b = __bfloat162float(in.q[g * D + di + 64]);
-        } else {
-          a = fold_at<G>(in, X, di, beta, first);
-          b = fold_at<G>(in, X, di + 64, beta, first);
-        }
-        if (p.rope) {
-          const float c = in.c32[di], s = in.s32[di];
-          const float xa = a * c - b * s;
-          const float yb = b * c + a * s;
-          a = xa;
-          b = yb;
-        }
-        x[u] = a * sc;
-        y[u] = b * sc;
-      }
-      // registers: [0] row g, cols 2t..; [1] row g+8; [2] row g, cols 2t+8..; [3] row g+8
-      uint32_t xh[2], xl[2], yh[2], yl[2];
+    for (int half = 0; half < 2; ++half) {  // dims di, di+1 and their partners +64
+      const int di = 16 * kk + 2 * t + 8 * half;
+      float x0, x1, y0, y1;
       if (head_row) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          split2(x[u], xh[u], xl[u]);
-          split2(y[u], yh[u], yl[u]);
-        }
+        const uint32_t wa = *reinterpret_cast<const uint32_t*>(in.q + g * kQPitch + di);
+        const uint32_t wb = *reinterpret_cast<const uint32_t*>(in.q + g * kQPitch + di + 64);
+        x0 = bf16lo(wa); x1 = bf16hi(wa); y0 = bf16lo(wb); y1 = bf16hi(wb);
       } else {
-        uint32_t xm[2], ym[2], xlo[2], ylo[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          split3(x[u], xh[u], xm[u], xlo[u]);
-          split3(y[u], yh[u], ym[u], ylo[u]);
-        }
+        const float2 fa = *reinterpret_cast<const float2*>(in.sf + X * D + di);
+        const float2 fb = *reinterpret_cast<const float2*>(in.sf + X * D + di + 64);
+        x0 = fa.x; x1 = fa.y; y0 = fb.x; y1 = fb.y;
+      }
+      if (p.rope) {
+        const float2 c = *reinterpret_cast<const float2*>(in.c32 + di);
+        const float2 s = *reinterpret_cast<const float2*>(in.s32 + di);
+        const float a0 = x0 * c.x - y0 * s.x, b0 = y0 * c.x + x0 * s.x;
+        const float a1 = x1 * c.y - y1 * s.y, b1 = y1 * c.y + x1 * s.y;
+        x0 = a0; y0 = b0; x1 = a1; y1 = b1;
+      }
+      x0 *= sc; x1 *= sc; y0 *= sc; y1 *= sc;
+      // registers: [0] row g, cols 2t..; [1] row g+8; [2] row g, cols 2t+8..; [3] row g+8
+      uint32_t xh, xl, yh, yl;
+      if (head_row) {
+        split2x(x0, x1, xh, xl);
+        split2x(y0, y1, yh, yl);
+      } else {
+        uint32_t xm, ym, xlo, ylo;
+        split3x(x0, x1, xh, xm, xlo);
+        split3x(y0, y1, yh, ym, ylo);
         if (g >= 6) {  // rows 6/7 carry the lo parts; rows 14/15 stay zero
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            xh[u] = xlo[u]; yh[u] = ylo[u]; xl[u] = 0u; yl[u] = 0u;
-          }
-        } else {  // rows 4/5 hi, rows 12/13 mid
-#pragma unroll
-          for (int u = 0; u < 2; ++u) { xl[u] = xm[u]; yl[u] = ym[u]; }
+          xh = xlo; yh = ylo; xl = 0u; yl = 0u;
+        } else {       // rows 4/5 hi, rows 12/13 mid
+          xl = xm; yl = ym;
         }
       }
-      afr[kk][2 * half + 0] = pack2(xh[0], xh[1]);
-      afr[kk][2 * half + 1] = pack2(xl[0], xl[1]);
-      afr[kk + 4][2 * half + 0] = pack2(yh[0], yh[1]);
-      afr[kk + 4][2 * half + 1] = pack2(yl[0], yl[1]);
+      afr[kk][2 * half + 0] = xh;
+      afr[kk][2 * half + 1] = xl;
+      afr[kk + 4][2 * half + 0] = yh;
+      afr[kk + 4][2 * half + 1] = yl;
     }
   }
 }
@@ -356,7 +384,7 @@ __device__ void segment_duties(const PoolDev& p, int layer, int i, int h, int sl
     float sa = 0.f;
     if (grp < G) {  // one query head per 8-lane group
       float qr[NE];
-      load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(in.q + grp * D), sigma, qr);
+      load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(in.q + grp * kQPitch), sigma, qr);
       if (p.rope) {
 #pragma unroll
         for (int e = 0; e < H2; ++e) {
@@ -378,14 +406,9 @@ __device__ void segment_duties(const PoolDev& p, int layer, int i, int h, int sl
       obx[grp] = sa;
     }
   }
-  const int first = flags & kPlanFirst;
   float* nxt = p.summary_next + srow * D;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int di = lane * 4 + e;
-    nxt[di] = fold_at<G>(in, 0, di, p.beta_s, first);
-    nxt[D + di] = fold_at<G>(in, 1, di, p.beta_l, first);
-  }
+  reinterpret_cast<float4*>(nxt)[lane] = reinterpret_cast<const float4*>(in.sf)[lane];
+  reinterpret_cast<float4*>(nxt + D)[lane] = reinterpret_cast<const float4*>(in.sf + D)[lane];
 }
 
 // Output of one (request, kv head) from the attention state in the warp's
@@ -553,6 +576,12 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       in.s32 = reinterpret_cast<const float*>(st + kMetaS32);
       in.c64 = reinterpret_cast<const double*>(st + kMetaC64);
       in.s64 = reinterpret_cast<const double*>(st + kMetaS64);
+      float* sf = reinterpret_cast<float*>(ring + (citems % S) * kMmaStageB + kMetaSF);
+      in.sf = sf;
+      if (score || cc.blk == 0) {  // the folded summaries are needed
+        fold_rows<G>(p, in, pe.flags, lane, sf);
+        __syncwarp();
+      }
       build_rows<G>(p, in, pe.flags, lane, afr);
       if (cc.blk == 0) segment_duties<G>(p, layer, i, h, slot, pe.flags, in, obx, lane);
       release_item();
