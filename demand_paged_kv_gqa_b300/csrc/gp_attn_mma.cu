@@ -474,7 +474,8 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   // block tables, K/V pages).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (n <= 0 || w >= Weff) return;  // warp-uniform: warps never synchronise
-  const int64_t start = (w * Tb) / Weff, end = ((w + 1) * Tb) / Weff;
+  const int64_t start = p.wblk[w], end = p.wblk[w + 1];  // the plan's (weighted) share
+  if (start >= end) return;
 
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -726,16 +727,11 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
   const int gw = blockIdx.x * kSmallWarps + warp;
   if (gw >= n * p.Hk) return;
   const int i = gw / p.Hk, h = gw % p.Hk;
-  const int nb = p.plan_nb[i];
   const int slot = p.plan_slot[i];
-  const int64_t Tb = (int64_t)p.plan_misc[2] * p.Hk;
-  const int64_t W = (int64_t)p.num_workers;
-  const int64_t Weff = W < Tb ? W : Tb;
-  const int64_t seg_b0 = (int64_t)p.Hk * p.plan_cum[i] + (int64_t)h * nb;
-  const int64_t w_first = ((seg_b0 + 1) * Weff - 1) / Tb;
-  const int64_t w_last = ((seg_b0 + nb) * Weff - 1) / Tb;
+  const int4 si = p.seginfo[gw];   // first and last worker of this (request, head)
+  const int64_t w_first = si.x, w_last = si.y;
   if (w_first == w_last) return;  // finished by the attention kernel
-  const bool first_is_second = (w_first * Tb) / Weff != seg_b0;  // its 2nd state slot
+  const bool first_is_second = si.z != 0;  // the first worker's second state slot
   const int nparts = (int)(w_last - w_first + 1);
   auto part_of = [&](int k) -> const float* {
     const int64_t wk = w_first + k;

@@ -51,7 +51,8 @@ kv_read_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer, 
     sink[3] = (uint32_t)(bytes >> 32);
   }
   if (n <= 0 || w >= Weff) return;
-  const int64_t start = (w * Tb) / Weff, end = ((w + 1) * Tb) / Weff;
+  const int64_t start = p.wblk[w], end = p.wblk[w + 1];  // the attention kernel's shares
+  if (start >= end) return;
   uint32_t acc = 0u;
   // sequential modes wrap inside the K/V region (it holds num_pages * L * Hk blocks)
   const int64_t region_blocks = (int64_t)p.num_pages * p.L * p.Hk * (p.P / kBlockTok);

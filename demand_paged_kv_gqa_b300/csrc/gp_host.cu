@@ -65,6 +65,13 @@ struct gp_pool {
   std::vector<int> prefix_len;
 };
 
+// Work of starting a (request, head) segment in the bf16 attention kernel
+// (meta item, operand rows, staged token), in blocks' worth: the plan
+// weighs it when it splits the blocks between workers.
+#ifndef GP_SEG_COST
+#define GP_SEG_COST 4
+#endif
+
 namespace {
 
 constexpr uint64_t kAlign = 256;
@@ -142,6 +149,8 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 2) * 4);  // partials
   take(R * Hk * 4);                                            // seg_count
   take((uint64_t)gp::kMaxWorkersBound * 16);                   // wstart
+  take((uint64_t)(gp::kMaxWorkersBound + 1) * 4);              // wblk
+  take(R * Hk * 16);                                           // seginfo
   take(R * L * Hk * 2 * D * 4);                                // summary_next
   take(R * Hk * 4 * 4);                                        // sstage
   take(R * L * Hk * P * 2 * 4);                                // moves
@@ -204,6 +213,8 @@ void fill_dev(gp_pool* p) {
   d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 2) * 4);
   d.seg_count = (int32_t*)take(R * c.num_kv_heads * 4);
   d.wstart = (int4*)take((uint64_t)gp::kMaxWorkersBound * 16);
+  d.wblk = (int32_t*)take((uint64_t)(gp::kMaxWorkersBound + 1) * 4);
+  d.seginfo = (int4*)take(R * c.num_kv_heads * 16);
   d.summary_next = (float*)take(R * c.num_layers * c.num_kv_heads * 2 * c.head_dim * 4);
   d.sstage = (float*)take(R * c.num_kv_heads * 4 * 4);
   d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 2 * 4);
@@ -309,6 +320,7 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   p->launches += 1;
   p->use_mma = cfg->dtype == GP_DTYPE_BF16 && cfg->head_dim == 128;
   p->dev.summary_via_next = p->use_mma ? 1 : 0;
+  p->dev.seg_cost = p->use_mma ? GP_SEG_COST : 0;
   if (p->use_mma) {
     // The pool's K/V pages viewed as one 2-D bf16 tensor [rows][d], rows =
     // ((page * L + layer) * Hk + head) * 2 * P + kv * P + token; boxes of
@@ -529,15 +541,16 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
 // ---- read ceiling without caller scratch -------------------------------
 //
 // Scratch of gp_kv_read_ceiling_static: the step plan (eleven arrays of
-// kStaticMaxRequests + 1 ints, the Delta accumulators) and the per-worker
-// start cursors.  It is a file-scope device array, so every GPU that loads
+// kStaticMaxRequests + 1 ints, the Delta accumulators), the per-worker
+// start cursors and the per-worker first blocks.  It is a file-scope device array, so every GPU that loads
 // the library holds these bytes until the process exits.
 namespace {
 constexpr int kStaticMaxRequests = 1024;
 constexpr size_t kStaticPlanArrayBytes = ((size_t)(kStaticMaxRequests + 1) * 4 + 255) / 256 * 256;
 constexpr size_t kStaticDeltaBytes = (size_t)kStaticMaxRequests * 8;
-constexpr size_t kStaticBytes =
-    11 * kStaticPlanArrayBytes + kStaticDeltaBytes + (size_t)gp::kMaxWorkersBound * 16;
+constexpr size_t kStaticWblkBytes = ((size_t)(gp::kMaxWorkersBound + 1) * 4 + 255) / 256 * 256;
+constexpr size_t kStaticBytes = 11 * kStaticPlanArrayBytes + kStaticDeltaBytes +
+                                (size_t)gp::kMaxWorkersBound * 16 + kStaticWblkBytes;
 }  // namespace
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticBytes];
@@ -590,6 +603,9 @@ int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int3
   for (int k = 0; k < 11; ++k) *arrays[k] = (int32_t*)(base + k * kStaticPlanArrayBytes);
   d.plan_delta = (long long*)(base + 11 * kStaticPlanArrayBytes);
   d.wstart = (int4*)(base + 11 * kStaticPlanArrayBytes + kStaticDeltaBytes);
+  d.wblk = (int32_t*)(base + 11 * kStaticPlanArrayBytes + kStaticDeltaBytes +
+                      (size_t)gp::kMaxWorkersBound * 16);
+  d.seginfo = nullptr;  // not written by the plan in measurement calls
   GP_LAUNCH(pool, gp::launch_plan(d, n, slots_dev, 0, pool->stream));
   const int wpc = gp::ceiling_warps_per_cta();
   const int grid = (d.num_workers + wpc - 1) / wpc;

@@ -74,6 +74,11 @@ struct PoolDev {
   float* sstage;          // [max_req][Hk][4] each query head's score against the
                           // staged token (log2 domain)
   int32_t summary_via_next;  // 1: the attention kernel writes summary_next
+  int32_t* wblk;          // [kMaxWorkersBound + 1] first block of each worker's share
+                          // (bf16 path; the last entry is the total)
+  int4* seginfo;          // [max_req][Hk] first and last worker of each (request,
+                          // head) and whether it is the first worker's second state
+  int32_t seg_cost;       // extra blocks' worth of work a (request, head) start costs
   int4* wstart;           // [kMaxWorkersBound] first block of each attention worker:
                           // request index, (head << 20) | block, blocks of the
                           // segment, slot (written by the plan kernel)

@@ -110,24 +110,62 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
     bcarry += btot;
   }
   __syncthreads();
-  // Start cursor of every attention worker: worker w of Weff = min(workers,
-  // total blocks) takes blocks [w*Tb/Weff, (w+1)*Tb/Weff) of the sequence
-  // (request i, head h, block b) laid out request-major, then head, then block.
+  // Shares of the attention workers.  The blocks of all (request, head)
+  // segments are laid end to end (request-major, then head, then block);
+  // each segment start also costs seg_cost extra units (its piece set-up).
+  // Worker w of Weff = min(workers, total blocks) takes the blocks whose
+  // units fall in [w*U/Weff, (w+1)*U/Weff), U = blocks + seg_cost * segments.
+  // With seg_cost = 0 this is an equal split of the blocks.
+  __shared__ int s_wblk[kMaxWorkersBound + 1];
   if (!s_bad && n > 0) {
     const long long Tb = (long long)carry * p.Hk;
     const long long W = p.num_workers;
     const long long Weff = W < Tb ? W : Tb;
+    const long long c = p.seg_cost;
+    const int nseg = n * p.Hk;
+    const long long U = Tb + c * nseg;
     for (int w = threadIdx.x; w < Weff; w += blockDim.x) {
-      const long long b = ((long long)w * Tb) / Weff;
-      const long long x = b / p.Hk;  // largest i with cum[i] <= b / Hk
-      int lo = 0, hi = n - 1;
+      const long long u = ((long long)w * U) / Weff;
+      // largest segment k with (start block of k) + c*k <= u
+      int lo = 0, hi = nseg - 1;
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((long long)p.plan_cum[mid] <= x) lo = mid; else hi = mid - 1;
+        const int mi = mid / p.Hk, mh = mid % p.Hk;
+        const long long cb = (long long)p.Hk * p.plan_cum[mi] + (long long)mh * p.plan_nb[mi] + c * mid;
+        if (cb <= u) lo = mid; else hi = mid - 1;
       }
-      const int nb = p.plan_nb[lo];
-      const long long r = b - (long long)p.Hk * p.plan_cum[lo];
-      p.wstart[w] = make_int4(lo, (int)((r / nb) << 20) | (int)(r % nb), nb, p.plan_slot[lo]);
+      const int i = lo / p.Hk, h = lo % p.Hk;
+      const int nb = p.plan_nb[i];
+      const long long sb = (long long)p.Hk * p.plan_cum[i] + (long long)h * nb;
+      const long long off = u - sb - c * lo;
+      const int blk = off < c ? 0 : (int)(off - c);
+      p.wstart[w] = make_int4(i, (h << 20) | blk, nb, p.plan_slot[i]);
+      p.wblk[w] = (int)(sb + blk);
+      s_wblk[w] = (int)(sb + blk);
+    }
+    if (threadIdx.x == 0) {
+      p.wblk[Weff] = (int)Tb;
+      s_wblk[Weff] = (int)Tb;
+    }
+    __syncthreads();
+    // each segment's first and last worker: the last worker whose share
+    // starts at or before the segment's first (last) block (not needed by
+    // the read-ceiling measurement, count == 0)
+    for (int k = threadIdx.x; count && k < nseg; k += blockDim.x) {
+      const int i = k / p.Hk, h = k % p.Hk;
+      const int nb = p.plan_nb[i];
+      const long long sb = (long long)p.Hk * p.plan_cum[i] + (long long)h * nb;
+      int wf = 0, wl = 0;
+      for (int pass = 0; pass < 2; ++pass) {
+        const long long b = pass ? sb + nb - 1 : sb;
+        int lo = 0, hi = (int)Weff - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_wblk[mid] <= b) lo = mid; else hi = mid - 1;
+        }
+        if (pass) wl = lo; else wf = lo;
+      }
+      p.seginfo[k] = make_int4(wf, wl, s_wblk[wf] != sb ? 1 : 0, 0);
     }
   }
   if (threadIdx.x == 0) {

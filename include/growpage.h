@@ -285,8 +285,8 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
  * which gp_kv_read_ceiling overwrites (so that one may only run between
  * steps).  Same arguments, result and rules as gp_kv_read_ceiling, except:
  *   - the per-call scratch (the step plan of the n requests and the start
- *     cursor of every attention worker) lives in a file-scope device array
- *     of this library, about 135 KB, which every GPU that loads the library
+ *     cursor and first block of every attention worker) lives in a file-scope
+ *     device array of this library, about 155 KB, which every GPU that loads the library
  *     keeps until the process exits; nothing of it needs clearing, as each
  *     call writes all the scratch it reads;
  *   - n may not exceed 1024 (GP_ERR_INVALID with a message otherwise);
