@@ -187,39 +187,51 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
 
 constexpr int kSelThreads = 256;
 
-__device__ __forceinline__ float block_max_f(float v, float* red) {
-  v = warp_max(v);
+// Block-wide max of two values at once (one per summary).
+__device__ __forceinline__ float2 block_max2(float a, float b, float2* red) {
+  a = warp_max(a);
+  b = warp_max(b);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) red[wid] = v;
+  if (lane == 0) red[wid] = make_float2(a, b);
   __syncthreads();
   if (wid == 0) {
-    float x = (lane < (int)(blockDim.x >> 5)) ? red[lane] : -INFINITY;
+    const bool in = lane < (int)(blockDim.x >> 5);
+    float x = in ? red[lane].x : -INFINITY, y = in ? red[lane].y : -INFINITY;
     x = warp_max(x);
-    if (lane == 0) red[32] = x;
+    y = warp_max(y);
+    if (lane == 0) red[32] = make_float2(x, y);
   }
   __syncthreads();
-  const float r = red[32];
+  const float2 r = red[32];
   __syncthreads();
   return r;
 }
 
-__device__ __forceinline__ unsigned long long block_sum_ull(unsigned long long v,
-                                                            unsigned long long* red) {
+// Block-wide sums of two 64-bit values at once.
+__device__ __forceinline__ void block_sum2_ull(unsigned long long& a, unsigned long long& b,
+                                               ulonglong2* red) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) red[wid] = v;
+  if (lane == 0) red[wid] = make_ulonglong2(a, b);
   __syncthreads();
   if (wid == 0) {
-    unsigned long long x = (lane < (int)(blockDim.x >> 5)) ? red[lane] : 0ull;
+    const bool in = lane < (int)(blockDim.x >> 5);
+    unsigned long long x = in ? red[lane].x : 0ull, y = in ? red[lane].y : 0ull;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (lane == 0) red[32] = x;
+    for (int o = 16; o > 0; o >>= 1) {
+      x += __shfl_xor_sync(0xffffffffu, x, o);
+      y += __shfl_xor_sync(0xffffffffu, y, o);
+    }
+    if (lane == 0) red[32] = make_ulonglong2(x, y);
   }
   __syncthreads();
-  const unsigned long long r = red[32];
+  a = red[32].x;
+  b = red[32].y;
   __syncthreads();
-  return r;
 }
 
 // Probability mass of a token in fixed point: e * 2^40 rounded to nearest
@@ -250,16 +262,18 @@ __device__ __forceinline__ unsigned long long ceil_mul(float top_p, unsigned lon
   return qv + (rem ? 1ull : 0ull);
 }
 
+// Histograms for both summaries; the compaction plan's hole and source lists
+// reuse the second mass histogram (see holes()/srcs()), which is free by then.
 struct SelShared {
-  unsigned int cnt[256];
-  unsigned long long mass[256];
-  unsigned long long red[33];
-  float redf[33];
-  int holes[256];
-  int srcs[256];
-  unsigned int pick_d;
-  unsigned long long pick_a, pick_b;
+  unsigned int cnt[2][256];
+  unsigned long long mass[2][256];
+  ulonglong2 red[33];
+  float2 redf[33];
+  unsigned int pick_d[2];
+  unsigned long long pick_a[2], pick_b[2];
   int done;
+  __device__ __forceinline__ int* holes() { return reinterpret_cast<int*>(mass[1]); }
+  __device__ __forceinline__ int* srcs() { return reinterpret_cast<int*>(mass[1]) + 256; }
 };
 
 // Sources of e_j = exp(u_j - max) for one summary's scores: computed from the
@@ -292,49 +306,59 @@ struct PosSmem {
   __device__ __forceinline__ int operator()(int s) const { return pos[s]; }
 };
 
-// Top-p working-set size: smallest k with (mass of the k largest) >= thr,
-// by a 4-pass radix select (8 bits per pass, most significant first) on the
-// fp32 bit patterns of e_j, weighting each by its fixed-point mass.
-template <class EF>
-__device__ int topp_radix(EF e_at, int R, unsigned long long thr, SelShared& sh) {
-  uint32_t prefix = 0u, pmask = 0u;
-  unsigned long long mass_above = 0ull, cnt_above = 0ull;
+// Top-p working-set sizes of both summaries: for each, the smallest k with
+// (mass of the k largest) >= thr, by a 4-pass radix select (8 bits per pass,
+// most significant first) on the fp32 bit patterns of e_j, weighting each by
+// its fixed-point mass.  The two selects share their passes: warp X scans
+// summary X's histogram.
+__device__ __forceinline__ void hist_add(SelShared& sh, int X, int d, unsigned long long mq) {
+  const unsigned int peers = __match_any_sync(0xffffffffu, d);
+  const unsigned int hi = __reduce_add_sync(peers, (unsigned int)(mq >> 20));
+  const unsigned int lo = __reduce_add_sync(peers, (unsigned int)(mq & 0xfffffull));
+  if (d < 256 && (threadIdx.x & 31) == __ffs(peers) - 1) {
+    atomicAdd(&sh.cnt[X][d], (unsigned int)__popc(peers));
+    atomicAdd(&sh.mass[X][d], ((unsigned long long)hi << 20) + (unsigned long long)lo);
+  }
+}
+
+template <class ES, class EL>
+__device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsigned long long thr1,
+                            SelShared& sh) {
+  uint32_t prefix[2] = {0u, 0u}, pmask = 0u;
+  unsigned long long mass_above[2] = {0ull, 0ull}, cnt_above[2] = {0ull, 0ull};
+  for (int d = threadIdx.x; d < 512; d += blockDim.x) {
+    (&sh.cnt[0][0])[d] = 0u;
+    (&sh.mass[0][0])[d] = 0ull;
+  }
+  __syncthreads();
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int d = threadIdx.x; d < 256; d += blockDim.x) { sh.cnt[d] = 0u; sh.mass[d] = 0ull; }
-    if (threadIdx.x == 0) { sh.pick_d = 0u; sh.pick_a = 0ull; sh.pick_b = 0ull; }
-    __syncthreads();
     // Most weights share their top digits, so lanes with the same digit are
     // combined inside the warp first and one lane per digit does the atomics.
     for (int base = 0; base < R; base += blockDim.x) {
       const int j = base + threadIdx.x;
-      int d = 256;  // "no digit"
-      unsigned long long mq = 0ull;
+      int d0 = 256, d1 = 256;  // 256: "no digit"
+      unsigned long long m0 = 0ull, m1 = 0ull;
       if (j < R) {
-        const float e = e_at(j);
-        const uint32_t bits = __float_as_uint(e);
-        if ((bits & pmask) == prefix) {
-          d = (bits >> shift) & 255;
-          mq = mass_q(e);
-        }
+        const float e0 = eS(j), e1 = eL(j);
+        const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
+        if ((b0 & pmask) == prefix[0]) { d0 = (b0 >> shift) & 255; m0 = mass_q(e0); }
+        if ((b1 & pmask) == prefix[1]) { d1 = (b1 >> shift) & 255; m1 = mass_q(e1); }
       }
-      const unsigned int peers = __match_any_sync(0xffffffffu, d);
-      const unsigned int hi = __reduce_add_sync(peers, (unsigned int)(mq >> 20));
-      const unsigned int lo = __reduce_add_sync(peers, (unsigned int)(mq & 0xfffffull));
-      if (d < 256 && (threadIdx.x & 31) == __ffs(peers) - 1) {
-        atomicAdd(&sh.cnt[d], (unsigned int)__popc(peers));
-        atomicAdd(&sh.mass[d], ((unsigned long long)hi << 20) + (unsigned long long)lo);
-      }
+      hist_add(sh, 0, d0, m0);
+      hist_add(sh, 1, d1, m1);
     }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      // descending digits: lane L owns digits 255-8L .. 248-8L
-      const int lane = threadIdx.x;
+    const int wid = threadIdx.x >> 5;
+    if (wid < 2) {
+      // descending digits: lane L owns digits 255-8L .. 248-8L and is the
+      // only lane that reads them, so it clears them for the next pass
+      const int X = wid, lane = threadIdx.x & 31;
       unsigned long long mloc = 0ull, cloc = 0ull;
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        mloc += sh.mass[255 - 8 * lane - t];
-        cloc += sh.cnt[255 - 8 * lane - t];
+        mloc += sh.mass[X][255 - 8 * lane - t];
+        cloc += sh.cnt[X][255 - 8 * lane - t];
       }
       unsigned long long mex = mloc, cex = cloc;
 #pragma unroll
@@ -344,35 +368,51 @@ __device__ int topp_radix(EF e_at, int R, unsigned long long thr, SelShared& sh)
         if (lane >= o) { mex += y; cex += z; }
       }
       mex -= mloc; cex -= cloc;  // mass / count of the digits above this lane's
-      const unsigned long long need = thr - mass_above;
+      // (register selects, not indexing: the arrays stay in registers)
+      const unsigned long long need = X ? thr1 - mass_above[1] : thr0 - mass_above[0];
       const bool here = (mex < need) && (mex + mloc >= need);
       const unsigned int bal = __ballot_sync(0xffffffffu, here);
+      if (bal == 0u && lane == 0) { sh.pick_d[X] = 0u; sh.pick_a[X] = 0ull; sh.pick_b[X] = 0ull; }
       if (here && lane == __ffs(bal) - 1) {
         unsigned long long macc = mex, cacc = cex;
         for (int t = 0; t < 8; ++t) {
           const int d = 255 - 8 * lane - t;
-          if (macc + sh.mass[d] >= need || t == 7) {
-            sh.pick_d = (unsigned)d;
-            sh.pick_a = macc;
-            sh.pick_b = cacc;
+          if (macc + sh.mass[X][d] >= need || t == 7) {
+            sh.pick_d[X] = (unsigned)d;
+            sh.pick_a[X] = macc;
+            sh.pick_b[X] = cacc;
             break;
           }
-          macc += sh.mass[d];
-          cacc += sh.cnt[d];
+          macc += sh.mass[X][d];
+          cacc += sh.cnt[X][d];
         }
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        sh.mass[X][255 - 8 * lane - t] = 0ull;
+        sh.cnt[X][255 - 8 * lane - t] = 0u;
       }
     }
     __syncthreads();
-    prefix |= sh.pick_d << shift;
+    // the picks are rewritten only after the next pass's histogram barrier
+#pragma unroll
+    for (int X = 0; X < 2; ++X) {
+      prefix[X] |= sh.pick_d[X] << shift;
+      mass_above[X] += sh.pick_a[X];
+      cnt_above[X] += sh.pick_b[X];
+    }
     pmask |= 255u << shift;
-    mass_above += sh.pick_a;
-    cnt_above += sh.pick_b;
-    __syncthreads();
   }
-  const unsigned long long qstar = mass_q(__uint_as_float(prefix));
-  const unsigned long long rest = thr > mass_above ? thr - mass_above : 0ull;
-  const unsigned long long k = qstar ? (rest + qstar - 1ull) / qstar : 1ull;
-  return (int)(cnt_above + (k ? k : 1ull));
+  int W[2];
+#pragma unroll
+  for (int X = 0; X < 2; ++X) {
+    const unsigned long long thr = X ? thr1 : thr0;
+    const unsigned long long qstar = mass_q(__uint_as_float(prefix[X]));
+    const unsigned long long rest = thr > mass_above[X] ? thr - mass_above[X] : 0ull;
+    const unsigned long long k = qstar ? (rest + qstar - 1ull) / qstar : 1ull;
+    W[X] = (int)(cnt_above[X] + (k ? k : 1ull));
+  }
+  return make_int2(W[0], W[1]);
 }
 
 // Compaction key of private slot s: (importance bits << 32 | position), with
@@ -395,14 +435,15 @@ struct KeyOf {
 // Threshold key such that exactly `k` candidates have key <= threshold (keys
 // are distinct: they end with the token position).  Radix select, 8 bits per
 // pass from the top, stopping as soon as the chosen bucket is taken whole.
+// The bucket is found by warp 0: lane L owns digits 8L .. 8L+7.
 template <class KF>
 __device__ unsigned long long kth_smallest(const KF& key_of, int C, int k, SelShared& sh) {
   unsigned long long prefix = 0ull, pmask = 0ull;
   unsigned int below = 0u;
+  for (int d = threadIdx.x; d < 256; d += blockDim.x) sh.cnt[0][d] = 0u;
+  __syncthreads();
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
-    for (int d = threadIdx.x; d < 256; d += blockDim.x) sh.cnt[d] = 0u;
-    __syncthreads();
     for (int base = 0; base < C; base += blockDim.x) {
       const int s = base + threadIdx.x;
       int d = 256;
@@ -413,28 +454,46 @@ __device__ unsigned long long kth_smallest(const KF& key_of, int C, int k, SelSh
       }
       const unsigned int peers = __match_any_sync(0xffffffffu, d);
       if (d < 256 && (threadIdx.x & 31) == __ffs(peers) - 1)
-        atomicAdd(&sh.cnt[d], (unsigned int)__popc(peers));
+        atomicAdd(&sh.cnt[0][d], (unsigned int)__popc(peers));
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned int acc = below;
-      int d = 0;
-      for (; d < 255; ++d) {
-        if (acc + sh.cnt[d] >= (unsigned)k) break;
-        acc += sh.cnt[d];
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      unsigned int c[8], cloc = 0u;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) { c[t] = sh.cnt[0][8 * lane + t]; cloc += c[t]; }
+      unsigned int cex = cloc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned int y = __shfl_up_sync(0xffffffffu, cex, o);
+        if (lane >= o) cex += y;
       }
-      sh.pick_d = (unsigned)d;
-      sh.pick_a = acc;
-      sh.done = (acc + sh.cnt[d] == (unsigned)k) ? 1 : 0;
+      cex = below + cex - cloc;  // candidates below this lane's digits
+      const bool here = (cex < (unsigned)k) && (cex + cloc >= (unsigned)k);
+      const unsigned int bal = __ballot_sync(0xffffffffu, here);
+      // no crossing (fewer than k candidates): the last digit, as a scan would end
+      const int owner = bal ? __ffs(bal) - 1 : 31;
+      if (lane == owner) {
+        unsigned int acc = cex;
+        int t = 0;
+        for (; t < 7; ++t) {
+          if (acc + c[t] >= (unsigned)k) break;
+          acc += c[t];
+        }
+        sh.pick_d[0] = (unsigned)(8 * lane + t);
+        sh.pick_a[0] = acc;
+        sh.done = (acc + c[t] == (unsigned)k) ? 1 : 0;
+      }
+#pragma unroll
+      for (int t = 0; t < 8; ++t) sh.cnt[0][8 * lane + t] = 0u;
     }
     __syncthreads();
-    const unsigned int d = sh.pick_d;
-    below = (unsigned int)sh.pick_a;
+    // the picks are rewritten only after the next pass's histogram barrier
+    const unsigned int d = sh.pick_d[0];
+    below = (unsigned int)sh.pick_a[0];
     prefix |= (unsigned long long)d << shift;
     pmask |= 255ull << shift;
-    const int done = sh.done;
-    __syncthreads();
-    if (done) return prefix | ((shift == 0) ? 0ull : ((1ull << shift) - 1ull));
+    if (sh.done) return prefix | ((shift == 0) ? 0ull : ((1ull << shift) - 1ull));
   }
   return prefix;
 }
@@ -442,18 +501,13 @@ __device__ unsigned long long kth_smallest(const KF& key_of, int C, int k, SelSh
 // Working sets, Delta and the compaction plan of one (request, layer, head).
 template <class ES, class EL, class PF>
 __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const gp_req_meta& m,
-                            int R, ES eS, EL eL, float mS, float mL, PF posf, SelShared& sh) {
-  // fixed-point masses, Top-p counts
-  float inv[2];
-  int W[2];
-  for (int X = 0; X < 2; ++X) {
-    unsigned long long s = 0ull;
-    for (int j = threadIdx.x; j < R; j += blockDim.x) s += mass_q(X ? eL(j) : eS(j));
-    const unsigned long long T = block_sum_ull(s, sh.red);
-    const unsigned long long thr = ceil_mul(p.top_p, T);
-    W[X] = X ? topp_radix(eL, R, thr, sh) : topp_radix(eS, R, thr, sh);
-    inv[X] = (float)(0x1p40 / (double)(T ? T : 1ull));
-  }
+                            int R, ES eS, EL eL, unsigned long long TS, unsigned long long TL,
+                            PF posf, SelShared& sh) {
+  // Top-p counts from the fixed-point total masses TS, TL
+  const int2 Wv = topp_radix2(eS, eL, R, ceil_mul(p.top_p, TS), ceil_mul(p.top_p, TL), sh);
+  const int W[2] = {Wv.x, Wv.y};
+  const float inv[2] = {(float)(0x1p40 / (double)(TS ? TS : 1ull)),
+                        (float)(0x1p40 / (double)(TL ? TL : 1ull))};
   if (threadIdx.x == 0) {
     p.wset[row * 2 + 0] = W[0];
     p.wset[row * 2 + 1] = W[1];
@@ -479,7 +533,7 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
       const unsigned int bal = __ballot_sync(0xffffffffu, dropped);
       if (dropped) {
         const int r = nh + __popc(bal & ((1u << lane) - 1u));
-        if (r < 256) sh.holes[r] = s;
+        if (r < 256) sh.holes()[r] = s;
       }
       nh += __popc(bal);
     }
@@ -495,7 +549,7 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
       const unsigned int bal = __ballot_sync(0xffffffffu, kept);
       if (kept) {
         const int r = ns + __popc(bal & ((1u << lane) - 1u));
-        if (r < 256) sh.srcs[r] = s;
+        if (r < 256) sh.srcs()[r] = s;
       }
       ns += __popc(bal);
     }
@@ -505,8 +559,8 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
     }
     int32_t* mv = p.moves + row * p.P * 2;
     for (int t = lane; t < nh; t += 32) {
-      mv[2 * t] = sh.holes[t];
-      mv[2 * t + 1] = sh.srcs[t];
+      mv[2 * t] = sh.holes()[t];
+      mv[2 * t + 1] = sh.srcs()[t];
     }
     if (lane == 0) p.moves_n[row] = nh;
   }
@@ -538,26 +592,31 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(PoolDev p) {
     const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
     const float* uS = p.logits + row * 2 * p.logit_width;
     const float* uL = uS + p.logit_width;
-    float mx[2];
-    for (int X = 0; X < 2; ++X) {
-      const float* u = X ? uL : uS;
-      float v = -INFINITY;
-      for (int j = threadIdx.x; j < R; j += blockDim.x) v = fmaxf(v, u[j]);
-      mx[X] = block_max_f(v, sh.redf);
+    float a = -INFINITY, b = -INFINITY;
+    for (int j = threadIdx.x; j < R; j += blockDim.x) {
+      a = fmaxf(a, uS[j]);
+      b = fmaxf(b, uL[j]);
     }
+    const float2 mx = block_max2(a, b, sh.redf);
     PosGlobal pg{p.block + (size_t)slot * p.block_width + m.n_pre_pages, p.tok_pos, p.P, p.L, p.Hk,
                  layer, h, p.num_pages};
-    if (R <= kSelSmemTok && C <= kSelSmemTok) {
-      for (int j = threadIdx.x; j < R; j += blockDim.x) {
-        eSs[j] = expf(uS[j] - mx[0]);
-        eLs[j] = expf(uL[j] - mx[1]);
-      }
-      for (int s = threadIdx.x; s < C; s += blockDim.x) poss[s] = pg(s);
-      __syncthreads();
-      select_item(p, i, slot, row, m, R, ESmem{eSs}, ESmem{eLs}, mx[0], mx[1], PosSmem{poss}, sh);
-    } else {
-      select_item(p, i, slot, row, m, R, EGlobal{uS, mx[0]}, EGlobal{uL, mx[1]}, mx[0], mx[1], pg, sh);
+    // fixed-point total masses; the staged path stages e_j in the same loop
+    // (the sums' barriers also publish the staged rows)
+    unsigned long long TS = 0ull, TL = 0ull;
+    const bool staged = R <= kSelSmemTok && C <= kSelSmemTok;
+    for (int j = threadIdx.x; j < R; j += blockDim.x) {
+      const float eS = expf(uS[j] - mx.x), eL = expf(uL[j] - mx.y);
+      TS += mass_q(eS);
+      TL += mass_q(eL);
+      if (staged) { eSs[j] = eS; eLs[j] = eL; }
     }
+    if (staged)
+      for (int s = threadIdx.x; s < C; s += blockDim.x) poss[s] = pg(s);
+    block_sum2_ull(TS, TL, sh.red);
+    if (staged)
+      select_item(p, i, slot, row, m, R, ESmem{eSs}, ESmem{eLs}, TS, TL, PosSmem{poss}, sh);
+    else
+      select_item(p, i, slot, row, m, R, EGlobal{uS, mx.x}, EGlobal{uL, mx.y}, TS, TL, pg, sh);
   }
 }
 
@@ -701,23 +760,38 @@ __global__ void __launch_bounds__(256) commit_kernel(PoolDev p) {
       for (int c = lane; c < 2 * p.D / 4; c += 32) dst[c] = src[c];
     }
     if (dec == kCompact || dec == kCompactDenied) {
+      // Four moves at a time, eight lanes each, every load of a group issued
+      // before its stores.  Moves never overlap: holes lie below C - P and
+      // survivors at or above it.
       const int nm = p.moves_n[row];
       const int32_t* mv = p.moves + row * p.P * 2;
-      for (int t = 0; t < nm; ++t) {
-        const int dst = mv[2 * t], src = mv[2 * t + 1];
-        int pd, ps;
-        uint8_t* rd = slot_row(p, bt, dst, layer, h, rowb, &pd);
-        const uint8_t* rs = slot_row(p, bt, src, layer, h, rowb, &ps);
-        for (int c = lane; c < chunks; c += 32) {
-          const uint4 kx = *reinterpret_cast<const uint4*>(rs + 16 * c);
-          const uint4 vx = *reinterpret_cast<const uint4*>(rs + p.half_bytes + 16 * c);
-          *reinterpret_cast<uint4*>(rd + 16 * c) = kx;
-          *reinterpret_cast<uint4*>(rd + p.half_bytes + 16 * c) = vx;
-        }
-        if (lane == 0) {
-          int32_t* tp_s = p.tok_pos + (((size_t)ps * p.L + layer) * p.Hk + h) * p.P + (src % p.P);
-          int32_t* tp_d = p.tok_pos + (((size_t)pd * p.L + layer) * p.Hk + h) * p.P + (dst % p.P);
-          *tp_d = *tp_s;
+      const int sub = lane & 7;
+      for (int base = 0; base < nm; base += 4) {
+        const int t = base + (lane >> 3);
+        if (t < nm) {
+          const int dst = mv[2 * t], src = mv[2 * t + 1];
+          int pd, ps;
+          uint8_t* rd = slot_row(p, bt, dst, layer, h, rowb, &pd);
+          const uint8_t* rs = slot_row(p, bt, src, layer, h, rowb, &ps);
+          uint4 kx[4], vx[4];
+          const int per = chunks / 8;  // 2 or 4 chunks per lane
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j < per) {
+              kx[j] = *reinterpret_cast<const uint4*>(rs + 16 * (sub + 8 * j));
+              vx[j] = *reinterpret_cast<const uint4*>(rs + p.half_bytes + 16 * (sub + 8 * j));
+            }
+          }
+          int tpos = 0;
+          if (sub == 0) tpos = p.tok_pos[(((size_t)ps * p.L + layer) * p.Hk + h) * p.P + (src % p.P)];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (j < per) {
+              *reinterpret_cast<uint4*>(rd + 16 * (sub + 8 * j)) = kx[j];
+              *reinterpret_cast<uint4*>(rd + p.half_bytes + 16 * (sub + 8 * j)) = vx[j];
+            }
+          }
+          if (sub == 0) p.tok_pos[(((size_t)pd * p.L + layer) * p.Hk + h) * p.P + (dst % p.P)] = tpos;
         }
       }
       moved += (unsigned long long)nm;
