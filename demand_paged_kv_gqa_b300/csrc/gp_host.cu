@@ -31,6 +31,7 @@ cudaError_t launch_kv_read(const PoolDev& p, const CUtensorMap* map, int layer, 
                            uint32_t* sink, int grid, cudaStream_t st);
 cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st);
 cudaError_t select_setup();
+cudaError_t select_occupancy(int* blocks);
 cudaError_t launch_decide(const PoolDev& p, cudaStream_t st);
 cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st);
 cudaError_t launch_init(const PoolDev& p, cudaStream_t st);
@@ -353,7 +354,9 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   if (grid * wpc > gp::kMaxWorkersBound) grid = gp::kMaxWorkersBound / wpc;
   p->attn_grid = grid;
   p->dev.num_workers = grid * wpc;
-  p->select_grid = sms * 4;
+  int sel_blocks = 0;
+  if (gp::select_occupancy(&sel_blocks) != cudaSuccess || sel_blocks < 1) return bail(GP_ERR_CUDA);
+  p->select_grid = sms * sel_blocks;
   p->commit_grid = sms * 4;
   e = cudaStreamSynchronize(p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);

@@ -185,7 +185,16 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
 
 // -------------------------------------------------------------- select ---
 
-constexpr int kSelThreads = 256;
+#ifndef GP_SEL_THREADS
+#define GP_SEL_THREADS 256
+#endif
+#ifndef GP_SEL_TOK
+#define GP_SEL_TOK 4096
+#endif
+#ifndef GP_SEL_MINB
+#define GP_SEL_MINB 4
+#endif
+constexpr int kSelThreads = GP_SEL_THREADS;
 
 // Block-wide max of two values at once (one per summary).
 __device__ __forceinline__ float2 block_max2(float a, float b, float2* red) {
@@ -569,10 +578,10 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
 
 // Rows of up to this many tokens are staged in shared memory: both
 // summaries' e_j and the private slots' positions (48 KiB).
-constexpr int kSelSmemTok = 4096;
+constexpr int kSelSmemTok = GP_SEL_TOK;
 constexpr size_t kSelSmemBytes = (size_t)kSelSmemTok * (4 + 4 + 4);
 
-__global__ void __launch_bounds__(kSelThreads) select_kernel(PoolDev p) {
+__global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDev p) {
   __shared__ SelShared sh;
   extern __shared__ float sel_dyn[];
   float* eSs = sel_dyn;
@@ -943,6 +952,10 @@ cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count
 cudaError_t select_setup() {
   return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)kSelSmemBytes);
+}
+cudaError_t select_occupancy(int* blocks) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, select_kernel, kSelThreads,
+                                                       kSelSmemBytes);
 }
 cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st) {
   select_kernel<<<grid, kSelThreads, kSelSmemBytes, st>>>(p);
