@@ -36,6 +36,16 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
+# DRAM bytes (read + write) per attention launch over its algorithmic K/V
+# bytes, from one ncu capture of attn_mma_kernel on the same heads and
+# requests with 4 layers and a 1.5 GB pool (two launches: 1.029 and 1.027).
+# The bench's launches are too large to capture, so the traffic it reports
+# is this ratio times its own algorithmic bytes per launch.
+TRAFFIC_RATIO = 1.028
+TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of attn_mma_kernel on a "
+                  "4-layer, 1.5 GB-pool case (ratio 1.028 to its algorithmic bytes), scaled to "
+                  "this launch's algorithmic bytes")
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -366,6 +376,7 @@ def run_ours(args, ws, rank, local):
         return None
     value = tokens / (t_ms * 1e-3)
     a_gbs = gp_res["attn_gbs"]
+    mma_path = w.dtype == "bf16" and w.head_dim == 128  # attn_mma_kernel runs
     line = {
         "metric": "decode tokens/s per B300 (GrowPage vs full-KV); % of HBM roofline",
         "value": round(value, 1),
@@ -391,13 +402,16 @@ def run_ours(args, ws, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "attn_kernel (paged GQA decode + summaries)",
+            "kernel": ("attn_mma_kernel" if mma_path else "attn_kernel")
+                      + " (paged GQA decode + summaries)",
             "achieved": round(a_gbs, 1),
             "peak": hbm_peak,
             "peak_source": peak_src,
             "unit": "GB/s",
             "frac": round(a_gbs / hbm_peak, 4),
-            "traffic": None,
+            "traffic": (round(TRAFFIC_RATIO * gp_res["attn_bytes_per_launch"])
+                        if mma_path else None),
+            "traffic_source": TRAFFIC_SOURCE if mma_path else None,
             "bytes_per_launch": round(gp_res["attn_bytes_per_launch"]),
             "launch_ms": round(gp_res["attn_launch_ms"], 5),
         },
