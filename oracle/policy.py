@@ -75,24 +75,27 @@ def drop_set(imp: np.ndarray, pos: np.ndarray, n_drop: int) -> np.ndarray:
 
 
 def compaction_plan(imp_priv: np.ndarray, pos_priv: np.ndarray, pos_now: int,
-                    capacity: int, page_size: int, recent_window: int):
+                    capacity: int, page_size: int, recent_window: int, n_free: int = None):
     """Which private tokens a compaction drops, and the near-tie gap at the cut.
 
     The request holds ``capacity`` private tokens (all its pages full).  It
-    keeps capacity - page_size of them, so that one page-worth of slots is
-    free within the same allocation: the most recent W = min(recent_window,
-    capacity - page_size) tokens always, plus the best of the older ones by
-    importance.  Returns (indices dropped, relative gap at the cut or inf).
+    keeps capacity - n_free of them (n_free = page_size by default: one
+    page-worth of slots free within the same allocation): the most recent
+    W = min(recent_window, capacity - n_free) tokens always, plus the best of
+    the older ones by importance.  Returns (indices dropped, relative gap at
+    the cut or inf).
     """
     n = len(pos_priv)
     assert n == capacity
-    w_eff = min(recent_window, capacity - page_size)
-    keep_total = capacity - page_size
+    if n_free is None:
+        n_free = page_size
+    w_eff = min(recent_window, capacity - n_free)
+    keep_total = capacity - n_free
     recent = pos_priv >= pos_now - w_eff
     assert int(recent.sum()) == w_eff, (int(recent.sum()), w_eff)
     cand = np.nonzero(~recent)[0]
     n_drop = len(cand) - (keep_total - w_eff)
-    assert n_drop == page_size
+    assert n_drop == n_free
     order = np.lexsort((pos_priv[cand], imp_priv[cand]))
     dropped = cand[order[:n_drop]]
     gap = np.inf
@@ -101,6 +104,21 @@ def compaction_plan(imp_priv: np.ndarray, pos_priv: np.ndarray, pos_now: int,
         b = imp_priv[cand[order[n_drop]]]       # smallest kept
         gap = abs(b - a) / max(b, 1e-300)
     return dropped, gap
+
+
+def may_shrink(pages: int, page_size: int, recent_window: int) -> bool:
+    """Whether the SHRINK ablation may release a page at this boundary.
+
+    Reading: the review names a SHRINK ablation (Tables 8-9) that isolates
+    "the cost of irreversible shrinking" and gives no rule.  Here, a
+    boundary that does not want to grow releases the request's last private
+    page instead of compacting in place: it drops two pages' worth of tokens
+    by the compaction rule, so that the remaining pages - 1 pages again have
+    one page of free slots.  A page is released only while the kept set
+    still holds the whole recent window, (pages - 2) * page_size >=
+    recent_window; otherwise the boundary compacts as GrowPage does.
+    """
+    return pages >= 2 and (pages - 2) * page_size >= recent_window
 
 
 MASK64 = (1 << 64) - 1

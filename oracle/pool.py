@@ -36,6 +36,8 @@ Readings this module takes (the pages leave them open):
 * Allocator: a stack whose pops return 0, 1, 2, ... initially; growth is
   served in ascending slot order; freeing pushes a request's private pages in
   block-table order, and a prefix's pages once its reference count is 0.
+  Pages released by the SHRINK ablation are pushed after every growth of the
+  step has popped, in ascending slot order.
 * Full-KV mode: the same steps, every boundary grows, nothing is compacted;
   a boundary with no free page drops the step's token ("starved").
 """
@@ -50,7 +52,7 @@ import numpy as np
 from . import numerics as nm
 from . import policy as pol
 
-GROW, COMPACT, COMPACT_DENIED, STARVED = 1, 2, 3, 4
+GROW, COMPACT, COMPACT_DENIED, STARVED, SHRINK = 1, 2, 3, 4, 5
 
 
 @dataclasses.dataclass
@@ -71,7 +73,8 @@ class OracleConfig:
     tau: float = 0.0
     full_kv: bool = False
     # grow decision at a boundary: "growpage" (Delta > tau), "fixed" (never),
-    # "inverse" (-Delta > tau) or "random" (see policy.random_grow)
+    # "inverse" (-Delta > tau), "random" (see policy.random_grow) or "shrink"
+    # (Delta > tau grows; otherwise a page is released, see policy.may_shrink)
     policy: str = "growpage"
     random_grow_rate: float = 0.0
 
@@ -338,7 +341,7 @@ class OraclePool:
             delta = pol.demand_delta(ws, wl)
             dmin = int(np.sum(band[:, :, 0, 0] - band[:, :, 1, 1]))
             dmax = int(np.sum(band[:, :, 0, 1] - band[:, :, 1, 0]))
-            if c.policy == "growpage":
+            if c.policy in ("growpage", "shrink"):
                 want = pol.wants_grow(delta, c.tau)
                 exempt = pol.wants_grow(dmin, c.tau) != pol.wants_grow(dmax, c.tau)
             elif c.policy == "inverse":
@@ -364,22 +367,30 @@ class OraclePool:
                 dec = GROW
             elif want:
                 dec = COMPACT_DENIED
+            elif c.policy == "shrink" and pol.may_shrink(len(r.pages), P, c.recent_window):
+                dec = SHRINK
             else:
                 dec = COMPACT
             decisions[slot] = dec
             near = band[:, :, :, 0] != band[:, :, :, 1]
             records[slot] = BoundaryRecord(slot, delta, dec, exempt, ws, wl, near, None,
                                            lg if self.keep_logits else None)
+        # SHRINK releases the last private page of each shrinking request, in
+        # ascending slot order, after every growth of the step has popped.
+        for slot in sorted(decisions):
+            if decisions[slot] == SHRINK:
+                self.free.append(self.req[slot].pages[-1])
         # A8/A9: compaction of the requests that did not grow.
         for slot, dec in decisions.items():
-            if dec not in (COMPACT, COMPACT_DENIED):
+            if dec not in (COMPACT, COMPACT_DENIED, SHRINK):
                 continue
             r = self.req[slot]
             cap = len(r.pages) * P
             lg = boundary_logits[slot]
             plen = r.prefix_len
             gaps = np.full((L, hk), np.inf)
-            keep_n = cap - P
+            n_free = 2 * P if dec == SHRINK else P
+            keep_n = cap - n_free
             newK = np.zeros((L, hk, r.toks.cap, d))
             newV = np.zeros_like(newK)
             newpos = np.zeros((L, hk, r.toks.cap), np.int64)
@@ -390,12 +401,12 @@ class OraclePool:
                     imp = pol.importance(ps, pl)
                     posp = r.toks.pos[l, g, :cap]
                     dropped, gap = pol.compaction_plan(imp, posp, r.pos, cap, P,
-                                                       c.recent_window)
+                                                       c.recent_window, n_free)
                     if arbiter is not None and gap <= 1e-5:
                         alt = arbiter.dropped(slot, l, g, posp.copy(), dropped.copy(), gap)
                         if alt is not None:
                             alt = np.asarray(alt, dtype=np.int64)
-                            w_eff = min(c.recent_window, cap - P)
+                            w_eff = min(c.recent_window, cap - n_free)
                             ok = (len(set(alt.tolist())) == len(dropped)
                                   and np.all(posp[alt] < r.pos - w_eff))
                             if not ok:
@@ -409,6 +420,8 @@ class OraclePool:
                     newpos[l, g, :keep_n] = posp[keep]
             r.toks.K, r.toks.V, r.toks.pos = newK, newV, newpos
             r.toks.n = keep_n
+            if dec == SHRINK:
+                r.pages.pop()
             records[slot].cut_gap = gaps
         # A10: commit the staged token.
         for i, slot in enumerate(slots):

@@ -16,7 +16,7 @@ import torch
 
 from oracle import numerics as nm
 from oracle import policy as pol
-from oracle.pool import OracleConfig, OraclePool, GROW, COMPACT, COMPACT_DENIED
+from oracle.pool import OracleConfig, OraclePool, GROW, COMPACT, COMPACT_DENIED, SHRINK
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -178,29 +178,31 @@ def test_demand_rule_strict():
 
 # ------------------------------------------------------ kept-set choice ----
 
-def test_compaction_plan_brute_force():
-    rng = np.random.default_rng(9)
+@pytest.mark.parametrize("pages_freed", [1, 2])
+def test_compaction_plan_brute_force(pages_freed):
+    rng = np.random.default_rng(9 + pages_freed)
     P = 4
+    n_free = pages_freed * P
     for trial in range(200):
-        cap = P * int(rng.integers(2, 6))
+        cap = P * int(rng.integers(pages_freed + 1, 6 + pages_freed))
         window = int(rng.integers(0, cap + 2))
         pos = np.sort(rng.choice(np.arange(0, 3 * cap), size=cap, replace=False))
         pos_now = int(pos[-1]) + 1
         # force the most recent tokens to be contiguous up to pos_now
-        w_eff = min(window, cap - P)
+        w_eff = min(window, cap - n_free)
         pos[cap - w_eff:] = np.arange(pos_now - w_eff, pos_now)
         pos = np.sort(pos)
         if len(set(pos.tolist())) != cap:
             continue
         imp = rng.choice([0.1, 0.2, 0.3, 0.5], size=cap) * rng.choice([1, 1, 2], size=cap)
-        dropped, _ = pol.compaction_plan(imp, pos, pos_now, cap, P, window)
+        dropped, _ = pol.compaction_plan(imp, pos, pos_now, cap, P, window, n_free)
         kept = set(range(cap)) - set(dropped.tolist())
         recent = {j for j in range(cap) if pos[j] >= pos_now - w_eff}
         older = sorted((j for j in range(cap) if j not in recent),
                        key=lambda j: (imp[j], pos[j]), reverse=True)
-        want = recent | set(older[:cap - P - w_eff])
+        want = recent | set(older[:cap - n_free - w_eff])
         assert kept == want
-        assert len(kept) == cap - P
+        assert len(kept) == cap - n_free
 
 
 # ------------------------------------------- attention vs dense SDPA ----
@@ -451,3 +453,52 @@ def test_inverse_and_fixed_policies_at_the_first_boundary():
     assert (g.decision == GROW) == (g.delta > 0)
     assert (inv.decision == GROW) == (inv.delta < 0)
     assert fx.decision == COMPACT
+
+
+def test_shrink_policy_releases_pages_down_to_the_window():
+    # equal smoothing makes Delta == 0 at every boundary: never a grow.  With
+    # 8 pages of 16 tokens and a 16-token window, SHRINK releases one page per
+    # boundary while (pages - 2) * 16 >= 16, i.e. down to 2 pages, then
+    # compacts in place.
+    cfg = _small_cfg(beta_s=0.95, beta_l=0.95, num_pages=40, policy="shrink")
+    rng = np.random.default_rng(5)
+    pool = OraclePool(cfg)
+    L, hk, hq, d, P = cfg.num_layers, cfg.num_kv_heads, cfg.num_q_heads, cfg.head_dim, 16
+    pool.add_request(0, rng.standard_normal((L, 128, hk, d)), rng.standard_normal((L, 128, hk, d)),
+                     budget_pages=8)
+    decs, pages = [], []
+    for t in range(130):
+        before = list(pool.req[0].pages)
+        res = pool.step([0], rng.standard_normal((1, L, hq, d)), rng.standard_normal((1, L, hk, d)),
+                        rng.standard_normal((1, L, hk, d)))
+        pool.check_invariants()
+        rec = res["records"].get(0)
+        r = pool.req[0]
+        if rec is None:
+            continue
+        assert t % P == 0               # the cadence of boundaries is unchanged
+        decs.append(rec.decision)
+        pages.append(len(r.pages))
+        if rec.decision == SHRINK:
+            # the last private page went back on top of the free stack
+            assert r.pages == before[:-1] and pool.free[-1] == before[-1]
+            assert r.toks.n == (len(before) - 2) * P + 1   # kept + the staged token
+        # the most recent tokens are always resident
+        pos = np.sort(r.toks.pos[:, :, :r.toks.n], axis=-1)
+        assert np.all(pos[..., -16:] == np.arange(r.pos - 16, r.pos))
+    assert decs == [SHRINK] * 6 + [COMPACT] * (len(decs) - 6)
+    assert pages[:7] == [7, 6, 5, 4, 3, 2, 2]
+
+
+def test_shrink_policy_grows_like_growpage():
+    # tau < 0: every boundary wants to grow, so SHRINK never releases a page
+    cfg = _small_cfg(beta_s=0.95, beta_l=0.95, tau=-1.0, num_pages=40, policy="shrink")
+    pool, recs = _run_tiny(cfg, 64)
+    decs = [r.decision for rr in recs for r in rr.values()]
+    assert decs and all(x == GROW for x in decs)
+    assert pool.req[0].toks.n == 32 + 64
+
+
+def test_may_shrink_floor():
+    assert pol.may_shrink(6, 16, 64) and not pol.may_shrink(5, 16, 64)
+    assert pol.may_shrink(2, 16, 0) and not pol.may_shrink(1, 16, 0)
