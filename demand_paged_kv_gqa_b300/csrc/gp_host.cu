@@ -29,7 +29,7 @@ cudaError_t ceiling_setup();
 int ceiling_warps_per_cta();
 cudaError_t launch_kv_read(const PoolDev& p, const CUtensorMap* map, int layer, int mode,
                            uint32_t* sink, int grid, cudaStream_t st);
-cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st);
+cudaError_t launch_select(const PoolDev& p, int grid, int replan, cudaStream_t st);
 cudaError_t select_setup();
 cudaError_t select_occupancy(int* blocks);
 cudaError_t launch_decide(const PoolDev& p, cudaStream_t st);
@@ -103,7 +103,7 @@ const char* check_config(const gp_config* c) {
   if (c->max_prefixes < 0 || c->max_prefix_len < 0 || c->max_prefix_len % c->page_size)
     return "max_prefix_len must be a non-negative multiple of page_size";
   if (c->max_seq_len < 1) return "bad max_seq_len";
-  if (c->mode < GP_MODE_GROWPAGE || c->mode > GP_MODE_RANDOM) return "unknown mode";
+  if (c->mode < GP_MODE_GROWPAGE || c->mode > GP_MODE_SHRINK) return "unknown mode";
   if (c->mode == GP_MODE_RANDOM && !(c->random_grow_rate >= 0.f && c->random_grow_rate <= 1.f))
     return "random_grow_rate must be in [0, 1]";
   if (c->recent_window < 0) return "recent_window < 0";
@@ -154,7 +154,7 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   take(R * Hk * 16);                                           // seginfo
   take(R * L * Hk * 2 * D * 4);                                // summary_next
   take(R * Hk * 4 * 4);                                        // sstage
-  take(R * L * Hk * P * 2 * 4);                                // moves
+  take(R * L * Hk * P * 4 * 4);                                // moves (up to 2P pairs)
   take(R * L * Hk * 4);                                        // moves_n
   l->total = off;
 }
@@ -218,7 +218,7 @@ void fill_dev(gp_pool* p) {
   d.seginfo = (int4*)take(R * c.num_kv_heads * 16);
   d.summary_next = (float*)take(R * c.num_layers * c.num_kv_heads * 2 * c.head_dim * 4);
   d.sstage = (float*)take(R * c.num_kv_heads * 4 * 4);
-  d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 2 * 4);
+  d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 4 * 4);
   d.moves_n = (int32_t*)take(R * c.num_layers * c.num_kv_heads * 4);
 }
 
@@ -504,8 +504,12 @@ int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev) {
   pool->next_layer = 0;
   if (n == 0) return GP_OK;
   if (pool->cfg.mode != GP_MODE_FULL_KV)
-    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, pool->stream));
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 0, pool->stream));
   GP_LAUNCH(pool, gp::launch_decide(pool->dev, pool->stream));
+  // SHRINK: the requests that release a page drop 2P tokens, not P; their
+  // plans are redone once the decisions are known
+  if (pool->cfg.mode == GP_MODE_SHRINK)
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 1, pool->stream));
   GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, pool->stream));
   return GP_OK;
 }

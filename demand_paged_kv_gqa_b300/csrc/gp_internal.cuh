@@ -17,7 +17,9 @@ constexpr int kBlockTok = 16;     // tokens per attention block (one bulk-copy u
 constexpr int kAttnWarps = 4;     // warps per attention CTA (independent workers)
 constexpr int kMaxWorkersBound = 160 * 8 * kAttnWarps;  // sizing bound
 
-enum Decision : int32_t { kNone = 0, kGrow = 1, kCompact = 2, kCompactDenied = 3, kStarved = 4 };
+enum Decision : int32_t {
+  kNone = 0, kGrow = 1, kCompact = 2, kCompactDenied = 3, kStarved = 4, kShrink = 5
+};
 
 // Flags of a request in the current step's plan.
 constexpr int32_t kPlanBoundary = 1;  // all private pages full at step start

@@ -271,8 +271,7 @@ __device__ __forceinline__ unsigned long long ceil_mul(float top_p, unsigned lon
   return qv + (rem ? 1ull : 0ull);
 }
 
-// Histograms for both summaries; the compaction plan's hole and source lists
-// reuse the second mass histogram (see holes()/srcs()), which is free by then.
+// Histograms for both summaries.
 struct SelShared {
   unsigned int cnt[2][256];
   unsigned long long mass[2][256];
@@ -281,8 +280,6 @@ struct SelShared {
   unsigned int pick_d[2];
   unsigned long long pick_a[2], pick_b[2];
   int done;
-  __device__ __forceinline__ int* holes() { return reinterpret_cast<int*>(mass[1]); }
-  __device__ __forceinline__ int* srcs() { return reinterpret_cast<int*>(mass[1]) + 256; }
 };
 
 // Sources of e_j = exp(u_j - max) for one summary's scores: computed from the
@@ -508,33 +505,40 @@ __device__ unsigned long long kth_smallest(const KF& key_of, int C, int k, SelSh
 }
 
 // Working sets, Delta and the compaction plan of one (request, layer, head).
+// The plan frees nfree private slots of a request holding C: it drops the
+// nfree lowest (importance, position) candidates older than the window and
+// moves the survivors at or above C - nfree into the holes below it.  With
+// replan set (the SHRINK ablation's second pass, after the decisions), only
+// the plan is computed.
 template <class ES, class EL, class PF>
 __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const gp_req_meta& m,
                             int R, ES eS, EL eL, unsigned long long TS, unsigned long long TL,
-                            PF posf, SelShared& sh) {
-  // Top-p counts from the fixed-point total masses TS, TL
-  const int2 Wv = topp_radix2(eS, eL, R, ceil_mul(p.top_p, TS), ceil_mul(p.top_p, TL), sh);
-  const int W[2] = {Wv.x, Wv.y};
+                            PF posf, int C, int pos, int nfree, bool replan, SelShared& sh) {
+  if (!replan) {
+    // Top-p counts from the fixed-point total masses TS, TL
+    const int2 Wv = topp_radix2(eS, eL, R, ceil_mul(p.top_p, TS), ceil_mul(p.top_p, TL), sh);
+    if (threadIdx.x == 0) {
+      p.wset[row * 2 + 0] = Wv.x;
+      p.wset[row * 2 + 1] = Wv.y;
+      atomicAdd((unsigned long long*)&p.plan_delta[i], (unsigned long long)(long long)(Wv.x - Wv.y));
+    }
+  }
   const float inv[2] = {(float)(0x1p40 / (double)(TS ? TS : 1ull)),
                         (float)(0x1p40 / (double)(TL ? TL : 1ull))};
-  if (threadIdx.x == 0) {
-    p.wset[row * 2 + 0] = W[0];
-    p.wset[row * 2 + 1] = W[1];
-    atomicAdd((unsigned long long*)&p.plan_delta[i], (unsigned long long)(long long)(W[0] - W[1]));
-  }
-  // compaction plan: drop the P lowest (importance, position) candidates
-  const int C = m.n_pages * p.P;
-  const int weff = min(p.recent_window, C - p.P);
-  KeyOf<ES, EL, PF> key_of{eS, eL, posf, inv[0], inv[1], m.n_pre_pages * p.P, m.pos - weff};
-  const unsigned long long thr_key = kth_smallest(key_of, C, p.P, sh);
-  // holes below C-P and survivors of the last page, both ascending
+  const int keep = C - nfree;
+  const int weff = min(p.recent_window, keep);
+  KeyOf<ES, EL, PF> key_of{eS, eL, posf, inv[0], inv[1], m.n_pre_pages * p.P, pos - weff};
+  const unsigned long long thr_key = kth_smallest(key_of, C, nfree, sh);
+  // holes below C - nfree and the survivors above it, both ascending, paired
+  // in order straight into the move list
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
+    int32_t* mv = p.moves + row * (size_t)p.P * 4;  // room for 2P moves
     int nh = 0;
-    for (int base = 0; base < C - p.P; base += 32) {
+    for (int base = 0; base < keep; base += 32) {
       const int s = base + lane;
       bool dropped = false;
-      if (s < C - p.P) {
+      if (s < keep) {
         bool cand;
         const unsigned long long key = key_of(s, &cand);
         dropped = cand && key <= thr_key;
@@ -542,12 +546,12 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
       const unsigned int bal = __ballot_sync(0xffffffffu, dropped);
       if (dropped) {
         const int r = nh + __popc(bal & ((1u << lane) - 1u));
-        if (r < 256) sh.holes()[r] = s;
+        if (r < nfree) mv[2 * r] = s;
       }
       nh += __popc(bal);
     }
     int ns = 0;
-    for (int base = C - p.P; base < C; base += 32) {
+    for (int base = keep; base < C; base += 32) {
       const int s = base + lane;
       bool kept = false;
       if (s < C) {
@@ -558,18 +562,13 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
       const unsigned int bal = __ballot_sync(0xffffffffu, kept);
       if (kept) {
         const int r = ns + __popc(bal & ((1u << lane) - 1u));
-        if (r < 256) sh.srcs()[r] = s;
+        if (r < nfree) mv[2 * r + 1] = s;
       }
       ns += __popc(bal);
     }
-    if (nh != ns || nh > p.P) {
+    if (nh != ns || nh > nfree) {
       if (lane == 0) set_status(p, GP_ST_BAD_PLAN, slot);
       nh = 0;
-    }
-    int32_t* mv = p.moves + row * p.P * 2;
-    for (int t = lane; t < nh; t += 32) {
-      mv[2 * t] = sh.holes()[t];
-      mv[2 * t + 1] = sh.srcs()[t];
     }
     if (lane == 0) p.moves_n[row] = nh;
   }
@@ -581,7 +580,7 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
 constexpr int kSelSmemTok = GP_SEL_TOK;
 constexpr size_t kSelSmemBytes = (size_t)kSelSmemTok * (4 + 4 + 4);
 
-__global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDev p) {
+__global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDev p, int replan) {
   __shared__ SelShared sh;
   extern __shared__ float sel_dyn[];
   float* eSs = sel_dyn;
@@ -594,10 +593,14 @@ __global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDe
     const int rem = item % (p.L * p.Hk);
     const int layer = rem / p.Hk, h = rem % p.Hk;
     const int i = p.plan_bnd[bi];
+    if (replan && p.plan_dec[i] != kShrink) continue;  // uniform over the CTA
     const int slot = p.plan_slot[i];
     const int R = p.plan_R[i];
     const gp_req_meta m = p.req[slot];
-    const int C = m.n_pages * p.P;
+    // the replan runs after the decisions, which have moved n_pages and pos
+    const int C = replan ? p.plan_commit[i] + 2 * p.P : m.n_pages * p.P;
+    const int pos = replan ? p.plan_cpos[i] : m.pos;
+    const int nfree = replan ? 2 * p.P : p.P;
     const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
     const float* uS = p.logits + row * 2 * p.logit_width;
     const float* uL = uS + p.logit_width;
@@ -623,9 +626,11 @@ __global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDe
       for (int s = threadIdx.x; s < C; s += blockDim.x) poss[s] = pg(s);
     block_sum2_ull(TS, TL, sh.red);
     if (staged)
-      select_item(p, i, slot, row, m, R, ESmem{eSs}, ESmem{eLs}, TS, TL, PosSmem{poss}, sh);
+      select_item(p, i, slot, row, m, R, ESmem{eSs}, ESmem{eLs}, TS, TL, PosSmem{poss}, C, pos,
+                  nfree, replan != 0, sh);
     else
-      select_item(p, i, slot, row, m, R, EGlobal{uS, mx.x}, EGlobal{uL, mx.y}, TS, TL, pg, sh);
+      select_item(p, i, slot, row, m, R, EGlobal{uS, mx.x}, EGlobal{uL, mx.y}, TS, TL, pg, C, pos,
+                  nfree, replan != 0, sh);
   }
 }
 
@@ -643,9 +648,9 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
 __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
   __shared__ int s_warp[33];
   __shared__ int s_avail;
-  __shared__ unsigned long long s_cnt[5];
+  __shared__ unsigned long long s_cnt[6];
   const int n = p.plan_misc[0];
-  if (threadIdx.x < 5) s_cnt[threadIdx.x] = 0ull;
+  if (threadIdx.x < 6) s_cnt[threadIdx.x] = 0ull;
   __syncthreads();
   for (int base = 0; base < n; base += blockDim.x) {
     if (threadIdx.x == 0) s_avail = p.ctrl->free_top;
@@ -661,7 +666,8 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
       if (at_b) {
         const double delta = (double)p.plan_delta[i];
         switch (p.mode) {
-          case GP_MODE_GROWPAGE: want = delta > (double)p.tau; break;
+          case GP_MODE_GROWPAGE:
+          case GP_MODE_SHRINK: want = delta > (double)p.tau; break;
           case GP_MODE_FULL_KV: want = 1; break;
           case GP_MODE_FIXED: want = 0; break;
           case GP_MODE_INVERSE: want = -delta > (double)p.tau; break;
@@ -686,7 +692,15 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
         m.n_grows += 1;
         atomicAdd(&s_cnt[1], 1ull);
       } else if (at_b) {
-        if (p.mode != GP_MODE_FULL_KV) {
+        if (p.mode == GP_MODE_SHRINK && !want && m.n_pages >= 2 &&
+            (m.n_pages - 2) * p.P >= p.recent_window) {
+          // release the last private page (pushed after this step's grows)
+          dec = kShrink;
+          commit = C - 2 * p.P;
+          m.n_pages -= 1;
+          m.n_shrinks += 1;
+          atomicAdd(&s_cnt[5], 1ull);
+        } else if (p.mode != GP_MODE_FULL_KV) {
           dec = want ? kCompactDenied : kCompact;
           commit = C - p.P;
           m.n_compacts += 1;
@@ -722,12 +736,37 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
     }
     __syncthreads();
   }
+  // Pages released by SHRINK go on the free stack after every pop of the
+  // step, in ascending slot order: a page released now is not handed out
+  // before the next step (its tokens are still read by the commit's moves).
+  if (p.mode == GP_MODE_SHRINK) {
+    for (int base = 0; base < n; base += blockDim.x) {
+      if (threadIdx.x == 0) s_avail = p.ctrl->free_top;
+      __syncthreads();
+      const int top = s_avail;
+      const int i = base + threadIdx.x;
+      const int sh = (i < n && p.plan_dec[i] == kShrink) ? 1 : 0;
+      int total;
+      const int rank = block_excl_scan(sh, s_warp, &total);
+      if (sh) {
+        const int slot = p.plan_slot[i];
+        const gp_req_meta& m = p.req[slot];
+        // the released page still sits in the block table, just past the
+        // request's (already reduced) page count
+        p.free_stack[top + rank] = p.block[(size_t)slot * p.block_width + m.n_pre_pages + m.n_pages];
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) p.ctrl->free_top = top + total;
+      __syncthreads();
+    }
+  }
   if (threadIdx.x == 0) {
     p.ctrl->boundaries += (long long)s_cnt[0];
     p.ctrl->grows += (long long)s_cnt[1];
     p.ctrl->compacts += (long long)s_cnt[2];
     p.ctrl->denied += (long long)s_cnt[3];
     p.ctrl->starved += (long long)s_cnt[4];
+    p.ctrl->shrinks += (long long)s_cnt[5];
   }
 }
 
@@ -768,12 +807,12 @@ __global__ void __launch_bounds__(256) commit_kernel(PoolDev p) {
       float4* dst = reinterpret_cast<float4*>(p.summary + row * 2 * p.D);
       for (int c = lane; c < 2 * p.D / 4; c += 32) dst[c] = src[c];
     }
-    if (dec == kCompact || dec == kCompactDenied) {
+    if (dec == kCompact || dec == kCompactDenied || dec == kShrink) {
       // Four moves at a time, eight lanes each, every load of a group issued
       // before its stores.  Moves never overlap: holes lie below C - P and
       // survivors at or above it.
       const int nm = p.moves_n[row];
-      const int32_t* mv = p.moves + row * p.P * 2;
+      const int32_t* mv = p.moves + row * (size_t)p.P * 4;
       const int sub = lane & 7;
       for (int base = 0; base < nm; base += 4) {
         const int t = base + (lane >> 3);
@@ -957,8 +996,8 @@ cudaError_t select_occupancy(int* blocks) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, select_kernel, kSelThreads,
                                                        kSelSmemBytes);
 }
-cudaError_t launch_select(const PoolDev& p, int grid, cudaStream_t st) {
-  select_kernel<<<grid, kSelThreads, kSelSmemBytes, st>>>(p);
+cudaError_t launch_select(const PoolDev& p, int grid, int replan, cudaStream_t st) {
+  select_kernel<<<grid, kSelThreads, kSelSmemBytes, st>>>(p, replan);
   return cudaGetLastError();
 }
 cudaError_t launch_decide(const PoolDev& p, cudaStream_t st) {

@@ -21,7 +21,8 @@ LIB_PATH = os.environ.get("GROWPAGE_LIB") or os.path.join(_HERE, "libgrowpage.so
 GP_OK, GP_ERR_INVALID, GP_ERR_NO_PAGES, GP_ERR_CUDA, GP_ERR_DEVICE = 0, 1, 2, 3, 4
 GP_DTYPE_F32, GP_DTYPE_BF16 = 0, 1
 GP_MODE_GROWPAGE, GP_MODE_FULL_KV, GP_MODE_FIXED, GP_MODE_INVERSE, GP_MODE_RANDOM = 0, 1, 2, 3, 4
-DEC_NONE, DEC_GROW, DEC_COMPACT, DEC_COMPACT_DENIED, DEC_STARVED = 0, 1, 2, 3, 4
+GP_MODE_SHRINK = 5
+DEC_NONE, DEC_GROW, DEC_COMPACT, DEC_COMPACT_DENIED, DEC_STARVED, DEC_SHRINK = 0, 1, 2, 3, 4, 5
 
 
 class gp_config(ctypes.Structure):
@@ -48,8 +49,7 @@ class gp_req_meta(ctypes.Structure):
         "active", "prefix_id", "n_pre_pages", "n_pages", "seq_priv", "pos",
         "steps", "last_decision")] + [("delta", ctypes.c_int64)] + [
         (n, ctypes.c_int32) for n in ("n_boundaries", "n_grows", "n_compacts",
-                                      "n_denied", "n_starved")] + [
-        ("reserved", ctypes.c_int32)]
+                                      "n_denied", "n_starved", "n_shrinks")]
 
 
 class gp_ctrl(ctypes.Structure):
@@ -57,8 +57,8 @@ class gp_ctrl(ctypes.Structure):
                 ("status_info", ctypes.c_int32), ("plan_n", ctypes.c_int32)] + [
         (n, ctypes.c_int64) for n in (
             "steps", "tokens_attended", "boundary_tokens", "boundaries", "grows",
-            "compacts", "denied", "starved", "moved_tokens")] + [
-        ("reserved", ctypes.c_int64 * 4)]
+            "compacts", "denied", "starved", "moved_tokens", "shrinks")] + [
+        ("reserved", ctypes.c_int64 * 3)]
 
 
 assert ctypes.sizeof(gp_req_meta) == 64

@@ -79,6 +79,16 @@ extern "C" {
 #define GP_MODE_RANDOM   4 /* grow iff u < random_grow_rate, u uniform in [0,1)
                               from SplitMix64 of (slot << 32 | boundaries
                               seen so far by the request), top 53 bits */
+/* The review's SHRINK ablation ("the cost of irreversible shrinking"; the
+ * pages give no rule, this is a reading): grow iff Delta > tau as in
+ * GP_MODE_GROWPAGE; otherwise release the request's last private page.  The
+ * boundary then drops 2P private tokens by the compaction rule (keeping the
+ * most recent min(W_r, C - 2P) and the most important older ones), so that
+ * the remaining b - 1 pages again hold P free slots.  A page is released
+ * only while (b - 2) * P >= W_r; below that the boundary compacts in place.
+ * Released pages are pushed on the free stack after every growth of the
+ * step has popped, in ascending slot order. */
+#define GP_MODE_SHRINK   5
 
 typedef struct gp_config {
   int32_t num_layers;        /* L */
@@ -149,12 +159,13 @@ typedef struct gp_req_meta {
   int32_t pos;           /* absolute position of the next token */
   int32_t steps;         /* decode steps done */
   int32_t last_decision; /* 0 none, 1 grow, 2 compact, 3 compact (grow
-                            denied), 4 starved (full-KV, no page) */
+                            denied), 4 starved (full-KV, no page),
+                            5 shrink (GP_MODE_SHRINK: a page released) */
   int64_t delta;         /* sum over layers and kv heads of W_S - W_L at the
                             last boundary */
   int32_t n_boundaries, n_grows, n_compacts, n_denied;
   int32_t n_starved;
-  int32_t reserved;
+  int32_t n_shrinks;     /* pages released (GP_MODE_SHRINK) */
 } gp_req_meta; /* 64 bytes */
 
 typedef struct gp_prefix_meta {
@@ -175,7 +186,8 @@ typedef struct gp_ctrl {
                                resident tokens R (prefix + private) */
   int64_t boundary_tokens;  /* same, restricted to requests at a boundary */
   int64_t boundaries, grows, compacts, denied, starved, moved_tokens;
-  int64_t reserved[4];
+  int64_t shrinks;       /* pages released (GP_MODE_SHRINK) */
+  int64_t reserved[3];
 } gp_ctrl;
 
 typedef struct gp_pool gp_pool; /* opaque host handle */

@@ -26,7 +26,7 @@ import torch
 
 from demand_paged_kv_gqa_b300 import growpage as gpb
 from demand_paged_kv_gqa_b300 import synth
-from oracle.pool import OracleConfig, OraclePool, GROW, COMPACT, COMPACT_DENIED, STARVED
+from oracle.pool import OracleConfig, OraclePool, GROW, COMPACT, COMPACT_DENIED, STARVED, SHRINK
 
 
 @dataclasses.dataclass
@@ -35,6 +35,7 @@ class Report:
     boundaries: int = 0
     grows: int = 0
     compacts: int = 0
+    shrinks: int = 0
     decision_resyncs: int = 0
     cut_resyncs: int = 0
     w_in_band: int = 0
@@ -78,7 +79,7 @@ def oracle_config(w, mode, num_pages, random_grow_rate=0.0):
     """The oracle's configuration for a GPU pool mode."""
     policy = {gpb.GP_MODE_GROWPAGE: "growpage", gpb.GP_MODE_FULL_KV: "growpage",
               gpb.GP_MODE_FIXED: "fixed", gpb.GP_MODE_INVERSE: "inverse",
-              gpb.GP_MODE_RANDOM: "random"}[mode]
+              gpb.GP_MODE_RANDOM: "random", gpb.GP_MODE_SHRINK: "shrink"}[mode]
     return OracleConfig.from_workload(w, full_kv=mode == gpb.GP_MODE_FULL_KV, num_pages=num_pages,
                                       policy=policy, random_grow_rate=random_grow_rate)
 
@@ -161,7 +162,7 @@ class Harness:
             m = metas[s]
             if m.steps > 0 and m.n_boundaries > 0 and self._had_boundary(s, m):
                 self.arb.gpu_dec[s] = m.last_decision
-                if m.last_decision in (COMPACT, COMPACT_DENIED):
+                if m.last_decision in (COMPACT, COMPACT_DENIED, SHRINK):
                     if tok_pos is None:
                         tok_pos = self.pool.region("tok_pos").cpu().numpy()
                     npre = m.n_pre_pages
@@ -220,6 +221,8 @@ class Harness:
                 rep.grows += 1
             elif rec.decision in (COMPACT, COMPACT_DENIED):
                 rep.compacts += 1
+            elif rec.decision == SHRINK:
+                rep.shrinks += 1
             if self.full_kv:
                 continue
             if wset is None:
@@ -234,7 +237,7 @@ class Harness:
             rep.w_in_band += int(np.sum(near & (wg != wo)))
             if not near.any() and m.delta != rec.delta:
                 rep.fail(f"step {t} slot {s}: delta {m.delta} vs {rec.delta}")
-            if rec.decision in (COMPACT, COMPACT_DENIED):
+            if rec.decision in (COMPACT, COMPACT_DENIED, SHRINK):
                 if tok_pos is None:
                     tok_pos = self.pool.region("tok_pos").cpu().numpy()
                 npre = m.n_pre_pages
@@ -353,7 +356,7 @@ class Scenario:
             m = metas[s]
             if m.n_boundaries > self.prev_nb[s]:
                 self.arb.gpu_dec[s] = m.last_decision
-                if m.last_decision in (COMPACT, COMPACT_DENIED):
+                if m.last_decision in (COMPACT, COMPACT_DENIED, SHRINK):
                     tok_pos = self.pool.region("tok_pos")
                     pos = _private_positions(tok_pos, bts[s][m.n_pre_pages:], m.seq_priv - 1, L, hk, P)
                     self.arb.gpu_kept[s] = [[set(pos[l, h].tolist()) for h in range(hk)] for l in range(L)]
@@ -404,6 +407,8 @@ class Scenario:
                 rep.grows += 1
             elif rec.decision in (COMPACT, COMPACT_DENIED):
                 rep.compacts += 1
+            elif rec.decision == SHRINK:
+                rep.shrinks += 1
             if self.full_kv:
                 continue
             if wset is None:
@@ -416,7 +421,7 @@ class Scenario:
             rep.w_in_band += int(np.sum(near & (wg != wo)))
             if not near.any() and m.delta != rec.delta:
                 rep.fail(f"step {t} slot {s}: delta {m.delta} vs {rec.delta}")
-            if rec.decision in (COMPACT, COMPACT_DENIED):
+            if rec.decision in (COMPACT, COMPACT_DENIED, SHRINK):
                 pos = _private_positions(self.pool.region("tok_pos"), bts[s][m.n_pre_pages:],
                                          m.seq_priv, L, hk, P)
                 if not np.array_equal(np.sort(pos, axis=-1), self.ora.kept_positions(s)):

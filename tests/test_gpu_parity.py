@@ -136,3 +136,23 @@ def test_review_hyperparameters_page_256(env):
     rep = h.run(300)
     _check(rep)
     assert rep.boundaries >= 12
+
+
+def test_shrink_policy(env):
+    # the SHRINK ablation: boundaries that do not grow release a page while
+    # the kept set still holds the recent window, else compact in place;
+    # grows and releases of several requests in the same step exercise the
+    # allocator order (block tables are compared exactly)
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=180, prompt_max=192, budget_pages=12,
+                                                  max_pages_per_req=20)
+    h = H.Harness(w, 6, mode=gp.GP_MODE_SHRINK, budget_pages=12)
+    rep = h.run(260)
+    _check(rep)
+    assert rep.shrinks > 6 and rep.boundaries > 30
+    st = h.pool.stats()
+    assert st.shrinks == rep.shrinks
+    t = H.Harness(synth.WORKLOADS["tiny"], 1, mode=gp.GP_MODE_SHRINK)
+    rt = t.run(200)
+    _check(rt)
+    assert rt.shrinks >= 1
