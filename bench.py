@@ -402,8 +402,8 @@ def run_ours(args, ws, rank, local):
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": ("attn_mma_kernel" if mma_path else "attn_kernel")
-                      + " (paged GQA decode + summaries)",
+            "kernel": ("attn_mma_kernel + combine_kernel" if mma_path else "attn_kernel")
+                      + " (one gp_decode_step layer call: paged GQA decode + summaries)",
             "achieved": round(a_gbs, 1),
             "peak": hbm_peak,
             "peak_source": peak_src,
