@@ -257,6 +257,8 @@ class Pool:
                               (R, L, hk, 2, l.logit_width))
         if name == "wset":
             return self._view(l.wset, R * L * hk * 2, torch.int32, (R, L, hk, 2))
+        if name == "req":  # gp_req_meta as 16 int32 words per slot (delta: words 8-9)
+            return self._view(l.req, R * 16, torch.int32, (R, 16))
         if name == "free_stack":
             return self._view(l.free_stack, c.num_pages, torch.int32, (c.num_pages,))
         raise KeyError(name)

@@ -156,3 +156,29 @@ def test_shrink_policy(env):
     rt = t.run(200)
     _check(rt)
     assert rt.shrinks >= 1
+
+
+def test_signal_quality_traces_match_oracle(env):
+    # the Delta / demand traces the signal-quality analysis reads from the
+    # device equal the oracle's, and so do the statistics drawn from them
+    H, gp, synth = env
+    from demand_paged_kv_gqa_b300 import signal_quality as sq
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=100, prompt_max=128, budget_pages=8,
+                                                  max_pages_per_req=24)
+    h = H.Harness(w, 6, budget_pages=8)
+    req, wset = h.pool.region("req"), h.pool.region("wset")
+    gpu_tr, ora_tr = {}, {}
+    for _ in range(300):
+        res = h.step()
+        _check(h.rep)
+        meta = req[: h.n].cpu()
+        ws = wset[: h.n].sum(dim=(1, 2)).cpu()
+        for s, rec in res["records"].items():
+            delta = (int(meta[s, 9]) << 32) | (int(meta[s, 8]) & 0xFFFFFFFF)
+            gpu_tr.setdefault(s, []).append((delta, int(ws[s, 0])))
+            ora_tr.setdefault(s, []).append((int(rec.delta), int(rec.w_short.sum())))
+    g, o = sq.statistics(gpu_tr), sq.statistics(ora_tr)
+    assert g["pairs"] == o["pairs"] > 30
+    if h.rep.w_in_band == 0:
+        assert gpu_tr == ora_tr
+    assert abs(g["spearman_rho"] - o["spearman_rho"]) < 0.05
