@@ -58,6 +58,11 @@ def parse():
                     help="untimed decode steps before warm-up (boundaries need history)")
     ap.add_argument("--no-full-kv", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=16)
+    ap.add_argument("--e2e-chunk", type=int, default=8,
+                    help="largest group of layers per host<->device copy in the e2e measurement")
+    ap.add_argument("--e2e-ramp", type=int, default=0,
+                    help="1: copy groups grow 1, 2, 4, .. up to --e2e-chunk for the inputs and "
+                         "shrink back to 1 for the outputs; 0: equal groups")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
@@ -270,7 +275,8 @@ def run_ours(args, ws, rank, local):
         res["step_bytes"] = per_layer_bytes * L / args.steps
         res["step_gbs"] = per_layer_bytes * L / (step_ms * 1e-3) / 1e9 if step_ms else 0.0
         res["ceilings"] = measure_ceilings(eng) if label == "growpage" else None
-        res["e2e"] = measure_e2e(eng, args.e2e_steps) if (args.e2e_steps and label == "growpage") else None
+        res["e2e"] = (measure_e2e(eng, args.e2e_steps, args.e2e_chunk, bool(args.e2e_ramp))
+                      if (args.e2e_steps and label == "growpage") else None)
         eng.pool.sync()
         del eng
         torch.cuda.empty_cache()
@@ -302,19 +308,32 @@ def run_ours(args, ws, rank, local):
         out["bytes_per_launch"] = nbytes
         return out
 
-    def measure_e2e(eng, k, chunk=8):
+    def groups(L, chunk, ramp):
+        """Layer groups [(first, end)]: equal groups of `chunk`, or with
+        `ramp` sizes 1, 2, 4, .. up to `chunk` and then `chunk`."""
+        out, c, size = [], 0, (1 if ramp else chunk)
+        while c < L:
+            out.append((c, min(c + size, L)))
+            c += size
+            size = min(2 * size, chunk)
+        return out
+
+    def measure_e2e(eng, k, chunk=8, ramp=True):
         """Same metric through the C-ABI with each step's q, k, v copied from
         pinned host memory and its outputs copied back to pinned host memory,
         all copies inside the events.  The copies run on a second stream in
-        chunks of `chunk` layers: a chunk's inputs are copied ahead, the
-        compute stream waits once per chunk, and a chunk's outputs go back
-        while the next chunk computes (what a serving loop over the per-layer
-        call does; waiting before every layer would break the programmatic
-        chaining of the layer kernels)."""
+        groups of layers: a group's inputs are copied ahead, the compute
+        stream waits once per group, and a group's outputs go back while the
+        next group computes (what a serving loop over the per-layer call
+        does; waiting before every layer would break the programmatic
+        chaining of the layer kernels).  With `ramp`, the input groups start
+        small (the first layer waits only for its own inputs) and the output
+        groups end small (little is left to copy after the last layer)."""
         stream = eng.pool.stream
         copy = torch.cuda.Stream(device=dev)
         L = w.num_layers
-        chunks = [(c, min(c + chunk, L)) for c in range(0, L, chunk)]
+        chunks = groups(L, chunk, ramp)
+        out_chunks = [(L - b, L - a) for a, b in reversed(groups(L, chunk, ramp))]
         hq_ = torch.empty_like(eng.q, device="cpu").pin_memory()
         hk_ = torch.empty_like(eng.k, device="cpu").pin_memory()
         hv_ = torch.empty_like(eng.v, device="cpu").pin_memory()
@@ -328,7 +347,7 @@ def run_ours(args, ws, rank, local):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             in_ready = {c0: torch.cuda.Event() for c0, _ in chunks}
-            out_ready = {c1 - 1: torch.cuda.Event() for _, c1 in chunks}
+            out_ready = {c1 - 1: torch.cuda.Event() for _, c1 in out_chunks}
 
             def before():
                 e0.record(stream)
@@ -346,7 +365,7 @@ def run_ours(args, ws, rank, local):
 
             def after_layer(l):
                 if l in out_ready:
-                    c0 = max(c for c, _ in chunks if c <= l)
+                    c0 = max(c for c, _ in out_chunks if c <= l)
                     out_ready[l].record(stream)
                     copy.wait_event(out_ready[l])
                     with torch.cuda.stream(copy):
