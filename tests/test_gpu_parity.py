@@ -182,3 +182,48 @@ def test_signal_quality_traces_match_oracle(env):
     if h.rep.w_in_band == 0:
         assert gpu_tr == ora_tr
     assert abs(g["spearman_rho"] - o["spearman_rho"]) < 0.05
+
+
+@pytest.mark.parametrize("over", [dict(top_p=1.0), dict(top_p=0.05), dict(recent_window=0),
+                                  dict(recent_window=10000)],
+                         ids=["top_p_1", "top_p_0.05", "window_0", "window_covers_all"])
+def test_degenerate_settings(env, over):
+    # Top-p at the whole mass and at a sliver of it; no recent window; a
+    # window wider than the kept set (the C - P most recent tokens are kept)
+    H, gp, synth = env
+    h = H.Harness(synth.WORKLOADS["tiny"].replace(**over), 1)
+    rep = h.run(200)
+    _check(rep)
+    assert rep.boundaries >= 12
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=100, prompt_max=128, budget_pages=8,
+                                                  max_pages_per_req=16, **over)
+    hb = H.Harness(w, 4, budget_pages=8)
+    rb = hb.run(120)
+    _check(rb)
+    assert rb.boundaries >= 8
+
+
+def test_empty_steps_and_call_order(env):
+    # a step with no requests changes nothing; calls out of order are
+    # refused with GP_ERR_INVALID and leave the pool usable
+    H, gp, synth = env
+    h = H.Harness(synth.WORKLOADS["tiny"], 1)
+    rep = h.run(20)
+    _check(rep)
+    w = h.w
+    none = torch.zeros(0, dtype=torch.int32, device="cuda")
+    qe = torch.zeros(0, w.num_q_heads, w.head_dim, dtype=w.torch_dtype, device="cuda")
+    ke = torch.zeros(0, w.num_kv_heads, w.head_dim, dtype=w.torch_dtype, device="cuda")
+    for _ in range(3):
+        for l in range(w.num_layers):
+            h.pool.decode_step(l, none, qe, ke, ke, qe)
+        h.pool.boundary(none)
+    with pytest.raises(gp.GrowPageError) as e:
+        h.pool.boundary(h.slots_dev)        # gp_boundary before the step's layers
+    assert e.value.code == gp.GP_ERR_INVALID
+    with pytest.raises(gp.GrowPageError):
+        h.pool.free(5)                      # not an active slot
+    h.pool.sync()
+    rep = h.run(60)                         # the trajectory continues in step with the oracle
+    _check(rep)
+    assert rep.boundaries >= 4
