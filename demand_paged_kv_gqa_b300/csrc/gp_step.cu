@@ -57,6 +57,10 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
 // count == 0: lay out the plan without touching the pool's step counters
 // (used by the read-ceiling measurement between steps).
 __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int32_t* slots, int count) {
+  // Launched as a programmatic dependent of the kernel before it: wait for it.
+  // No early trigger: the attention kernel after this one reads the plan
+  // before its own wait, so it may start only once this kernel has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ int s_warp[33];
   __shared__ int s_bad;
   __shared__ unsigned long long s_tok, s_btok;
@@ -581,6 +585,9 @@ constexpr int kSelSmemTok = GP_SEL_TOK;
 constexpr size_t kSelSmemBytes = (size_t)kSelSmemTok * (4 + 4 + 4);
 
 __global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDev p, int replan) {
+  // programmatic dependent of the kernel before it; lets the next one launch
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ SelShared sh;
   extern __shared__ float sel_dyn[];
   float* eSs = sel_dyn;
@@ -646,6 +653,8 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
 }
 
 __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int s_warp[33];
   __shared__ int s_avail;
   __shared__ unsigned long long s_cnt[6];
@@ -785,6 +794,8 @@ __device__ __forceinline__ uint8_t* slot_row(const PoolDev& p, const int32_t* bt
 }
 
 __global__ void __launch_bounds__(256) commit_kernel(PoolDev p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int n = p.plan_misc[0];
   const int rowb = p.D * p.elem_bytes;
   const int chunks = rowb / 16;
@@ -984,9 +995,27 @@ __global__ void release_prefix_kernel(PoolDev p, int pid) {
 
 // ------------------------------------------------------------ launchers ---
 
+// The per-step kernels are launched as programmatic dependents of the kernel
+// before them in the stream (each waits for it with griddepcontrol.wait
+// before touching memory), so a launch overlaps its predecessor's tail.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_t smem,
+                              cudaStream_t st, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count, cudaStream_t st) {
-  plan_kernel<<<1, 1024, 0, st>>>(p, n, slots, count);
-  return cudaGetLastError();
+  return launch_pdl(plan_kernel, 1, 1024, 0, st, p, n, slots, count);
 }
 cudaError_t select_setup() {
   return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -997,16 +1026,13 @@ cudaError_t select_occupancy(int* blocks) {
                                                        kSelSmemBytes);
 }
 cudaError_t launch_select(const PoolDev& p, int grid, int replan, cudaStream_t st) {
-  select_kernel<<<grid, kSelThreads, kSelSmemBytes, st>>>(p, replan);
-  return cudaGetLastError();
+  return launch_pdl(select_kernel, grid, kSelThreads, kSelSmemBytes, st, p, replan);
 }
 cudaError_t launch_decide(const PoolDev& p, cudaStream_t st) {
-  decide_kernel<<<1, 1024, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decide_kernel, 1, 1024, 0, st, p);
 }
 cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st) {
-  commit_kernel<<<grid, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(commit_kernel, grid, 256, 0, st, p);
 }
 cudaError_t launch_init(const PoolDev& p, cudaStream_t st) {
   init_kernel<<<256, 256, 0, st>>>(p);
