@@ -56,6 +56,8 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
 
 // count == 0: lay out the plan without touching the pool's step counters
 // (used by the read-ceiling measurement between steps).
+constexpr int kPlanSmemReq = 2048;
+
 __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int32_t* slots, int count) {
   // Launched as a programmatic dependent of the kernel before it: wait for it.
   // No early trigger: the attention kernel after this one reads the plan
@@ -64,6 +66,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
   __shared__ int s_warp[33];
   __shared__ int s_bad;
   __shared__ unsigned long long s_tok, s_btok;
+  // per-request block counts and prefix sums for the searches below (up to
+  // kPlanSmemReq requests; beyond that the searches read the global copies)
+  __shared__ int s_cum[kPlanSmemReq], s_nb[kPlanSmemReq];
+  const bool in_smem = n <= kPlanSmemReq;
+  const int* cum = in_smem ? s_cum : p.plan_cum;
+  const int* nbs = in_smem ? s_nb : p.plan_nb;
   if (threadIdx.x == 0) { s_bad = 0; s_tok = 0ull; s_btok = 0ull; }
   __syncthreads();
   int carry = 0, bcarry = 0;
@@ -108,6 +116,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
     const int bex = block_excl_scan(isb, s_warp, &btot);
     if (i < n) {
       p.plan_cum[i] = carry + ex;
+      if (in_smem) { s_cum[i] = carry + ex; s_nb[i] = nb; }
       if (isb) p.plan_bnd[bcarry + bex] = i;
     }
     carry += tot;
@@ -135,12 +144,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         const int mi = mid / p.Hk, mh = mid % p.Hk;
-        const long long cb = (long long)p.Hk * p.plan_cum[mi] + (long long)mh * p.plan_nb[mi] + c * mid;
+        const long long cb = (long long)p.Hk * cum[mi] + (long long)mh * nbs[mi] + c * mid;
         if (cb <= u) lo = mid; else hi = mid - 1;
       }
       const int i = lo / p.Hk, h = lo % p.Hk;
-      const int nb = p.plan_nb[i];
-      const long long sb = (long long)p.Hk * p.plan_cum[i] + (long long)h * nb;
+      const int nb = nbs[i];
+      const long long sb = (long long)p.Hk * cum[i] + (long long)h * nb;
       const long long off = u - sb - c * lo;
       const int blk = off < c ? 0 : (int)(off - c);
       p.wstart[w] = make_int4(i, (h << 20) | blk, nb, p.plan_slot[i]);
@@ -157,8 +166,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
     // the read-ceiling measurement, count == 0)
     for (int k = threadIdx.x; count && k < nseg; k += blockDim.x) {
       const int i = k / p.Hk, h = k % p.Hk;
-      const int nb = p.plan_nb[i];
-      const long long sb = (long long)p.Hk * p.plan_cum[i] + (long long)h * nb;
+      const int nb = nbs[i];
+      const long long sb = (long long)p.Hk * cum[i] + (long long)h * nb;
       int wf = 0, wl = 0;
       for (int pass = 0; pass < 2; ++pass) {
         const long long b = pass ? sb + nb - 1 : sb;
