@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--preroll", type=int, default=1024,
                     help="untimed decode steps before warm-up (boundaries need history)")
     ap.add_argument("--no-full-kv", action="store_true")
+    ap.add_argument("--no-policies", action="store_true",
+                    help="skip the ablation policies (fixed, inverse, random, shrink)")
     ap.add_argument("--e2e-steps", type=int, default=48)
     ap.add_argument("--e2e-chunk", type=int, default=8,
                     help="largest group of layers per host<->device copy in the e2e measurement")
@@ -209,8 +211,8 @@ def run_ours(args, ws, rank, local):
     hbm_peak = float(peaks.get("hbm_gbs", 6400.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
-    def measure(mode, label):
-        eng = Engine(w, mode=mode, device=dev, seed_offset=rank)
+    def measure(mode, label, rate=0.0):
+        eng = Engine(w, mode=mode, device=dev, seed_offset=rank, random_grow_rate=rate)
         eng.fill()
         stream = eng.pool.stream
         for _ in range(args.preroll):
@@ -264,6 +266,7 @@ def run_ours(args, ws, rank, local):
                    clocks=clocks, launches=launches, dtok=dtok, dbtok=dbtok, req_steps=req_steps,
                    boundaries=st1.boundaries - st0.boundaries, grows=st1.grows - st0.grows,
                    compacts=st1.compacts - st0.compacts, denied=st1.denied - st0.denied,
+                   shrinks=st1.shrinks - st0.shrinks,
                    moved=st1.moved_tokens - st0.moved_tokens, preempted=eng.preempted,
                    free_pages=st1.free_top, num_pages=eng.num_pages)
         # attention kernel: layers 1..L-1 of each timed step
@@ -390,6 +393,17 @@ def run_ours(args, ws, rank, local):
 
     gp_res = measure(gpb.GP_MODE_GROWPAGE, "growpage")
     fk_res = None if args.no_full_kv else measure(gpb.GP_MODE_FULL_KV, "full_kv")
+    # the review's ablation policies on the same kernels and workload; RANDOM
+    # grows at GrowPage's measured grow frequency
+    pol_res = {}
+    if not args.no_policies:
+        rate = gp_res["grows"] / max(1, gp_res["boundaries"])
+        for name, mode, r in (("fixed", gpb.GP_MODE_FIXED, 0.0),
+                              ("inverse", gpb.GP_MODE_INVERSE, 0.0),
+                              ("random", gpb.GP_MODE_RANDOM, rate),
+                              ("shrink", gpb.GP_MODE_SHRINK, 0.0)):
+            pol_res[name] = measure(mode, name, rate=r)
+            pol_res[name]["rate"] = r
 
     # max over ranks of the time, sum of tokens
     t_ms, tokens = reduce_over_ranks(gp_res["step_ms"], gp_res["tokens"], dev)
@@ -461,6 +475,16 @@ def run_ours(args, ws, rank, local):
             "mean_resident_tokens": round(fk_res["dtok"] / max(1, fk_res["req_steps"]), 1),
             "preempted": fk_res["preempted"], "tokens": fk_res["tokens"],
         }
+    if pol_res:
+        line["policies"] = {}
+        for name, r in pol_res.items():
+            o = {"value": round(r["tokens"] / (r["step_ms"] * 1e-3) * ws, 1), "unit": "tokens/s",
+                 "ms_per_step": round(r["step_ms"] / args.steps, 4),
+                 "mean_resident_tokens": round(r["dtok"] / max(1, r["req_steps"]), 1)}
+            o.update({k: int(r[k]) for k in ("boundaries", "grows", "compacts", "shrinks")})
+            if name == "random":
+                o["random_grow_rate"] = round(r["rate"], 4)
+            line["policies"][name] = o
     return line
 
 

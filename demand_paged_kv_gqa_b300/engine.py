@@ -48,14 +48,16 @@ class Req:
 class Engine:
     def __init__(self, w: synth.Workload, mode=gpb.GP_MODE_GROWPAGE, device="cuda",
                  num_pages: Optional[int] = None, batch: Optional[int] = None,
-                 seed_offset: int = 0, max_seq_len: Optional[int] = None):
+                 seed_offset: int = 0, max_seq_len: Optional[int] = None,
+                 random_grow_rate: float = 0.0):
         self.w = w
         self.mode = mode
         self.full_kv = mode == gpb.GP_MODE_FULL_KV
         self.device = torch.device(device)
         self.batch = batch or w.batch
         self.cfg = gpb.config_for(w, mode=mode, max_requests=self.batch,
-                                  num_pages=num_pages or w.num_pages, max_seq_len=max_seq_len)
+                                  num_pages=num_pages or w.num_pages, max_seq_len=max_seq_len,
+                                  random_grow_rate=random_grow_rate)
         self.pool = gpb.Pool(self.cfg, device=self.device)
         self.num_pages = self.cfg.num_pages
         self.P = w.page_size
