@@ -308,9 +308,13 @@ class BatchStream:
         q = sd * u.repeat_interleave(w.group, dim=2) + sig.view(n, 1, 1, 1) * self._randn(n, L, hq, d)
         k = self._randn(n, L, hk, d)
         v = self._randn(n, L, hk, d)
-        per = torch.clamp(self.T // max(1, w.n_planted), min=1)
-        hot = ((self.t % per) == 0) & (self.t < per * w.n_planted)
-        k = torch.where(hot.view(n, 1, 1, 1), sd * u, k)
+        # planted steps floor(j T / n_planted), j < n_planted, as in RequestStream:
+        # t is one iff j = ceil(t n / T) is below n and floor(j T / n) == t
+        npl = w.n_planted
+        if npl > 0:
+            j = (self.t * npl + self.T - 1) // self.T
+            hot = (j < npl) & (j * self.T < (self.t + 1) * npl)
+            k = torch.where(hot.view(n, 1, 1, 1), sd * u, k)
         self.t += 1
         dt = w.torch_dtype
         return q.to(dt), k.to(dt), v.to(dt)
