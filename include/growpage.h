@@ -266,7 +266,12 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n,
  * private tokens plus the best older ones by max(p_S, p_L) (ties: the more
  * recent), C - P in all, and move the survivors of the last page into the
  * freed slots.  Then every request appends its staged token.  Full-KV mode:
- * every boundary grows.  Asynchronous. */
+ * every boundary grows.  The ablation modes change only the grow decision
+ * (GP_MODE_FIXED, GP_MODE_INVERSE, GP_MODE_RANDOM) or, for GP_MODE_SHRINK,
+ * replace in-place compaction by a page release (see its definition above).
+ * n and slots_dev must be the step's own (those given to gp_decode_step);
+ * called before the step's last layer it returns GP_ERR_INVALID.
+ * Asynchronous. */
 int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev);
 
 /* Release a request: its private pages are pushed in block-table order; a
