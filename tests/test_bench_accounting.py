@@ -1,0 +1,23 @@
+"""The bench's algorithmic byte count (no GPU), written out by hand for the
+32-layer workload's heads: 8 kv heads, 32 query heads, d = 128, bf16."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from demand_paged_kv_gqa_b300 import synth  # noqa: E402
+
+
+def test_attention_bytes_by_hand():
+    w = synth.WORKLOADS["llama8b_32layer"]
+    # one request-layer with 1000 resident tokens, not at a boundary
+    kv = 1000 * (8 * 128 * 2) * 2                    # K and V rows, bf16
+    fixed = (32 * 128 * 2) * 2 + (8 * 128 * 2) * 2 * 2 + (8 * 128 * 4) * 2 * 2
+    assert fixed == 40960
+    bt = 1000 / 16 * 4
+    assert bench.attention_bytes(w, 1000, 1, 0) == kv + fixed + bt
+    # at a boundary both summaries' fp32 scores are written for every resident key
+    assert bench.attention_bytes(w, 1000, 1, 1000) - bench.attention_bytes(w, 1000, 1, 0) == 1000 * 2 * 8 * 4
