@@ -691,10 +691,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       // a cut (request, head): leave this piece's state for combine_kernel
       const int seg = i * p.Hk + h;
       const int pslot = (seg == first_seg) ? 0 : 1;
-      constexpr int PW = G * (D + 2);
+      constexpr int PW = G * (D + 4);  // per head: D outputs, m, l, 2 pad (16-byte rows)
       float* part = p.partials + (size_t)(w * 2 + pslot) * PW;
-      for (int x = lane; x < G * D; x += 32) part[(x / D) * (D + 2) + (x % D)] = ob[x];
-      if (lane < 2 * G) part[(lane % G) * (D + 2) + D + lane / G] = ob[G * D + lane];
+      for (int x = lane; x < G * D; x += 32) part[(x / D) * (D + 4) + (x % D)] = ob[x];
+      if (lane < 2 * G) part[(lane % G) * (D + 4) + D + lane / G] = ob[G * D + lane];
     }
     __syncwarp();  // the buffers are reused by the next piece
     if (j < end) {  // next piece: block 0 of the following (request, head)
@@ -719,7 +719,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
 template <int G>
 __global__ void __launch_bounds__(kSmallWarps * 32)
 combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
-  constexpr int D = kMmaD, PW = G * (D + 2);
+  constexpr int D = kMmaD, PW = G * (D + 4);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // which workers cut this (request, head): from the plan, final before the step
@@ -740,11 +740,13 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
   };
   // the workers' states and the staged token come from earlier kernels
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every lane holds dims 4*lane .. 4*lane+3 of each head: 16-byte loads of
+  // the states, 8-byte loads and stores of the bf16 rows
   const size_t srow = (((size_t)slot * p.L + layer) * p.Hk + h) * 2;
-  const __nv_bfloat16* vst = reinterpret_cast<const __nv_bfloat16*>(p.staging) + (srow + 1) * D;
-  float vs[4], sst[G];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) vs[e] = __bfloat162float(vst[lane + 32 * e]);
+  const uint2 vraw = reinterpret_cast<const uint2*>(p.staging + (srow + 1) * D * 2)[lane];
+  const float vs[4] = {__uint_as_float(vraw.x << 16), __uint_as_float(vraw.x & 0xffff0000u),
+                       __uint_as_float(vraw.y << 16), __uint_as_float(vraw.y & 0xffff0000u)};
+  float sst[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) sst[g] = p.sstage[(i * p.Hk + h) * 4 + g];
   float mmax[G], lsum[G], acc[G][4];
@@ -754,35 +756,37 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
     lsum[g] = 0.f;
     acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
   }
-  // online merge over the parts, four at a time with all their loads issued
-  // first: every lane holds dims lane + 32e of each head
+  // online merge over the parts, four at a time with all their loads issued first
   constexpr int CH = 4;
   for (int base = 0; base < nparts; base += CH) {
-    float mv[CH][G], lv[CH][G], ov[CH][G][4];
+    float2 ml[CH][G];
+    float4 ov[CH][G];
 #pragma unroll
     for (int u = 0; u < CH; ++u) {
       const bool ok = base + u < nparts;
       const float* pk = part_of(ok ? base + u : base);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        mv[u][g] = ok ? __ldcg(pk + g * (D + 2) + D) : -INFINITY;
-        lv[u][g] = ok ? __ldcg(pk + g * (D + 2) + D + 1) : 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) ov[u][g][e] = ok ? __ldcg(pk + g * (D + 2) + lane + 32 * e) : 0.f;
+        ml[u][g] = ok ? __ldcg(reinterpret_cast<const float2*>(pk + g * (D + 4) + D))
+                      : make_float2(-INFINITY, 0.f);
+        ov[u][g] = ok ? __ldcg(reinterpret_cast<const float4*>(pk + g * (D + 4)) + lane)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
 #pragma unroll
     for (int u = 0; u < CH; ++u) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float mk = mv[u][g];
+        const float mk = ml[u][g].x;
         if (mk == -INFINITY) continue;
         const float mn = fmaxf(mmax[g], mk);
         const float al = (mmax[g] == -INFINITY) ? 0.f : exp2f(mmax[g] - mn);
         const float be = exp2f(mk - mn);
-        lsum[g] = lsum[g] * al + lv[u][g] * be;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[g][e] = acc[g][e] * al + ov[u][g][e] * be;
+        lsum[g] = lsum[g] * al + ml[u][g].y * be;
+        acc[g][0] = acc[g][0] * al + ov[u][g].x * be;
+        acc[g][1] = acc[g][1] * al + ov[u][g].y * be;
+        acc[g][2] = acc[g][2] * al + ov[u][g].z * be;
+        acc[g][3] = acc[g][3] * al + ov[u][g].w * be;
         mmax[g] = mn;
       }
     }
@@ -794,10 +798,14 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
     const float al = (mmax[g] == -INFINITY) ? 0.f : exp2f(mmax[g] - mn);
     const float be = exp2f(sst[g] - mn);
     const float inv = 1.0f / (lsum[g] * al + be);
-    __nv_bfloat16* orow = out + ((size_t)i * p.Hq + h * G + g) * D;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      orow[lane + 32 * e] = __float2bfloat16_rn((acc[g][e] * al + be * vs[e]) * inv);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn((acc[g][0] * al + be * vs[0]) * inv,
+                                                    (acc[g][1] * al + be * vs[1]) * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn((acc[g][2] * al + be * vs[2]) * inv,
+                                                    (acc[g][3] * al + be * vs[3]) * inv);
+    uint2 wv;
+    wv.x = *reinterpret_cast<const uint32_t*>(&lo);
+    wv.y = *reinterpret_cast<const uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(out + ((size_t)i * p.Hq + h * G + g) * D)[lane] = wv;
   }
 }
 

@@ -147,7 +147,7 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   l->scratch = off;
   for (int k = 0; k < 11; ++k) take((R + 1) * 4);             // plan arrays
   take(R * 8);                                                 // plan_delta
-  take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 2) * 4);  // partials
+  take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 4) * 4);  // partials
   take(R * Hk * 4);                                            // seg_count
   take((uint64_t)gp::kMaxWorkersBound * 16);                   // wstart
   take((uint64_t)(gp::kMaxWorkersBound + 1) * 4);              // wblk
@@ -211,7 +211,7 @@ void fill_dev(gp_pool* p) {
   d.plan_misc = (int32_t*)take((R + 1) * 4);
   d.plan_pos = (int32_t*)take((R + 1) * 4);
   d.plan_delta = (long long*)take(R * 8);
-  d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 2) * 4);
+  d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 4) * 4);
   d.seg_count = (int32_t*)take(R * c.num_kv_heads * 4);
   d.wstart = (int4*)take((uint64_t)gp::kMaxWorkersBound * 16);
   d.wblk = (int32_t*)take((uint64_t)(gp::kMaxWorkersBound + 1) * 4);
