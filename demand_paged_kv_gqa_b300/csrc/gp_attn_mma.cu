@@ -33,10 +33,11 @@
 // item (bulk copies of the query rows, the new key and value, the summaries
 // and the rotary rows), so building a piece's operands never waits on a
 // dependent global load.
-// Work is split over a persistent grid as in the fp32 kernel (equal ranges
-// of blocks per warp; a cut (request, head) is merged by the warp that
-// finishes its last piece).  Every wait is bounded and on the warp's own
-// copies.
+// Work is split over a persistent grid: contiguous ranges of blocks per warp,
+// weighted so that each (request, head) start counts as a few blocks (the
+// plan kernel computes them).  A (request, head) cut between warps leaves one
+// state per warp, and combine_kernel merges them after the attention grid has
+// finished.  Every wait is bounded and on the warp's own copies.
 #include <cuda.h>
 
 #include "gp_attn_common.cuh"

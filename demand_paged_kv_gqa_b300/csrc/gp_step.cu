@@ -1,14 +1,21 @@
 // gp_step.cu -- the per-step kernels around the attention kernel.
 //
 //   plan_kernel     once per step (before layer 0): per request, resident
-//                   tokens, attention blocks, boundary flags; prefix sums.
+//                   tokens, attention blocks, boundary flags; prefix sums;
+//                   the attention workers' weighted ranges and each cut
+//                   (request, head)'s first and last worker.
 //   select_kernel   per (boundary request, layer, kv head): softmax of both
 //                   summaries' scores, Top-p working-set size by radix select
 //                   with exact integer mass, Delta contribution, and the
-//                   compaction plan (which private tokens to drop).
-//   decide_kernel   one CTA: grow or compact per request, pages popped from
-//                   the lock-free stack in ascending slot order, metadata.
-//   commit_kernel   per (request, layer, kv head): compaction moves, then the
+//                   compaction plan (which private tokens to drop); for the
+//                   SHRINK ablation a second launch re-plans the requests
+//                   that release a page.
+//   decide_kernel   one CTA: grow, compact or (SHRINK) release a page per
+//                   request; pages popped from the lock-free stack in
+//                   ascending slot order, released pages pushed after every
+//                   pop; metadata.
+//   commit_kernel   per (request, layer, kv head): the step's folded
+//                   summaries made current, compaction moves, then the
 //                   staged token written into its slot.
 //
 // Method: "GrowPage: On-Demand KV Budgeting for Efficient LLM Reasoning
