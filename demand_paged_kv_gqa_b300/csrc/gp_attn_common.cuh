@@ -2,8 +2,10 @@
 //
 // Work decomposition (both kernels): the resident tokens of every
 // (request, kv head) are cut into 16-token blocks; all blocks of a layer
-// launch are laid end to end and split into equal contiguous ranges, one per
-// warp of a persistent grid.  A Cursor walks that sequence.
+// launch are laid end to end and split into contiguous ranges, one per warp
+// of a persistent grid: equal ranges for the fp32 kernel, ranges weighted by
+// (request, head) starts for the bf16 kernel (the plan kernel computes both).
+// A Cursor walks that sequence.
 #pragma once
 
 #include "gp_internal.cuh"
