@@ -502,3 +502,17 @@ def test_shrink_policy_grows_like_growpage():
 def test_may_shrink_floor():
     assert pol.may_shrink(6, 16, 64) and not pol.may_shrink(5, 16, 64)
     assert pol.may_shrink(2, 16, 0) and not pol.may_shrink(1, 16, 0)
+
+
+def test_topp_near_tie_band():
+    # uniform mass over 10 tokens: Top-p 0.3 reaches its mass exactly at 3
+    # tokens, so a relative move of 1e-5 either way changes W (a near tie);
+    # at Top-p 0.35 the threshold sits mid-token and the band is one value
+    p = np.full(10, 0.1)
+    assert pol.topp_count(p, 0.3) in (3, 4)
+    lo, hi = pol.topp_range(p, 0.3)
+    assert (lo, hi) == (3, 4)
+    assert pol.topp_range(p, 0.35) == (4, 4)
+    # a dominant token: W = 1 for any Top-p up to its mass
+    q = np.array([0.97, 0.01, 0.01, 0.01])
+    assert pol.topp_range(q, 0.9) == (1, 1)
