@@ -649,6 +649,25 @@ int gp_get_request(gp_pool* pool, int32_t slot, gp_req_meta* meta, int32_t* bloc
   return GP_OK;
 }
 
+int gp_get_state(gp_pool* pool, gp_state_view* out) {
+  if (!pool || !out) return GP_ERR_INVALID;
+  const gp_config& c = pool->cfg;
+  const gp::PoolDev& d = pool->dev;
+  const size_t R = (size_t)c.max_requests;
+  cudaError_t e = cudaStreamSynchronize(pool->stream);
+  auto copy = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess && dst) e = cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost);
+  };
+  copy(out->req, d.req, R * sizeof(gp_req_meta));
+  copy(out->block, d.block, R * (size_t)pool->lay.block_width * 4);
+  copy(out->ctrl, d.ctrl, sizeof(gp_ctrl));
+  copy(out->wset, d.wset, R * c.num_layers * c.num_kv_heads * 2 * 4);
+  copy(out->tok_pos, d.tok_pos, (size_t)c.num_pages * c.num_layers * c.num_kv_heads * c.page_size * 4);
+  copy(out->free_stack, d.free_stack, (size_t)c.num_pages * 4);
+  if (e != cudaSuccess) return cuda_fail(pool, e, "gp_get_state");
+  return GP_OK;
+}
+
 const char* gp_last_error(const gp_pool* pool) { return pool ? pool->err.c_str() : "null pool"; }
 
 int64_t gp_launch_count(const gp_pool* pool) { return pool ? pool->launches : 0; }

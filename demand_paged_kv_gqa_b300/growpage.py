@@ -61,6 +61,11 @@ class gp_ctrl(ctypes.Structure):
         ("reserved", ctypes.c_int64 * 3)]
 
 
+class gp_state_view(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("req", "block", "ctrl", "wset", "tok_pos",
+                                               "free_stack")]
+
+
 assert ctypes.sizeof(gp_req_meta) == 64
 
 
@@ -86,6 +91,7 @@ def _load():
         "gp_get_stats": (ctypes.c_int, [P, ctypes.POINTER(gp_ctrl)]),
         "gp_get_request": (ctypes.c_int, [P, I32, ctypes.POINTER(gp_req_meta),
                                           ctypes.POINTER(I32), I32]),
+        "gp_get_state": (ctypes.c_int, [P, ctypes.POINTER(gp_state_view)]),
         "gp_kv_read_ceiling": (ctypes.c_int, [P, I32, I32, I32, I32, P, P]),
         "gp_kv_read_ceiling_static": (ctypes.c_int, [P, I32, I32, I32, I32, P, P]),
         "gp_last_error": (ctypes.c_char_p, [P]),
@@ -216,6 +222,30 @@ class Pool:
         bt = (ctypes.c_int32 * w)()
         self._check(lib.gp_get_request(self.h, slot, ctypes.byref(m), bt, w))
         return m, list(bt)[: m.n_pre_pages + m.n_pages]
+
+    def state(self, tok_pos: bool = False) -> dict:
+        """The pool's state on the host (gp_get_state): request metadata, block
+        tables, counters, working-set sizes, the free stack and, if asked,
+        every slot's token position."""
+        import numpy as np
+        c, lay = self.cfg, self.layout
+        R = c.max_requests
+        req = (gp_req_meta * R)()
+        ctrl = gp_ctrl()
+        block = np.zeros((R, lay.block_width), np.int32)
+        wset = np.zeros((R, c.num_layers, c.num_kv_heads, 2), np.int32)
+        free = np.zeros(c.num_pages, np.int32)
+        pos = (np.zeros((c.num_pages, c.num_layers, c.num_kv_heads, c.page_size), np.int32)
+               if tok_pos else None)
+        v = gp_state_view(ctypes.cast(req, ctypes.c_void_p), block.ctypes.data,
+                          ctypes.addressof(ctrl), wset.ctypes.data,
+                          pos.ctypes.data if pos is not None else None, free.ctypes.data)
+        self._check(lib.gp_get_state(self.h, ctypes.byref(v)))
+        out = {"req": list(req), "block": block, "ctrl": ctrl, "wset": wset,
+               "free_stack": free[: ctrl.free_top]}
+        if pos is not None:
+            out["tok_pos"] = pos
+        return out
 
     def kv_read_ceiling(self, layer0: int, count: int, mode: int, slots: torch.Tensor,
                         sink: torch.Tensor):

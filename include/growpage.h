@@ -329,6 +329,31 @@ int gp_get_stats(gp_pool* pool, gp_ctrl* out);
 int gp_get_request(gp_pool* pool, int32_t slot, gp_req_meta* meta,
                    int32_t* block_table, int32_t cap);
 
+/* Host destinations for gp_get_state; any pointer may be NULL (that region
+ * is not copied).  Sizes, with the pool's configuration and layout:
+ *   req        [max_requests] gp_req_meta
+ *   block      [max_requests][block_width] int32 (gp_layout.block_width)
+ *   ctrl       one gp_ctrl
+ *   wset       [max_requests][num_layers][num_kv_heads][2] int32: W_S, W_L
+ *              of each request's last boundary
+ *   tok_pos    [num_pages][num_layers][num_kv_heads][page_size] int32: the
+ *              absolute position of the token in each page slot
+ *   free_stack [num_pages] int32, valid up to ctrl->free_top
+ * The caller owns these buffers. */
+typedef struct gp_state_view {
+  gp_req_meta* req;
+  int32_t* block;
+  gp_ctrl* ctrl;
+  int32_t* wset;
+  int32_t* tok_pos;
+  int32_t* free_stack;
+} gp_state_view;
+
+/* Copy the pool's state (block tables, request metadata with sequence
+ * lengths, budgets and the last Delta, working-set sizes, kept positions,
+ * counters, the free stack) to the host in one call.  SYNC. */
+int gp_get_state(gp_pool* pool, gp_state_view* out);
+
 /* Text of the last error on this handle ("" if none).  Owned by the pool. */
 const char* gp_last_error(const gp_pool* pool);
 

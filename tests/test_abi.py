@@ -51,12 +51,14 @@ def test_struct_layouts_match_header(gp):
 #include "growpage.h"
 #define F(S, f) printf(#S "." #f " %zu\n", offsetof(S, f))
 int main(void) {
-  printf("gp_config %zu\ngp_layout %zu\ngp_req_meta %zu\ngp_ctrl %zu\n",
-         sizeof(gp_config), sizeof(gp_layout), sizeof(gp_req_meta), sizeof(gp_ctrl));
+  printf("gp_config %zu\ngp_layout %zu\ngp_req_meta %zu\ngp_ctrl %zu\ngp_state_view %zu\n",
+         sizeof(gp_config), sizeof(gp_layout), sizeof(gp_req_meta), sizeof(gp_ctrl),
+         sizeof(gp_state_view));
   F(gp_config, beta_s); F(gp_config, rope_theta); F(gp_config, flags);
   F(gp_layout, page_bytes); F(gp_layout, block_width); F(gp_layout, num_workers);
   F(gp_req_meta, delta); F(gp_req_meta, n_starved);
-  F(gp_ctrl, steps); F(gp_ctrl, moved_tokens);
+  F(gp_ctrl, steps); F(gp_ctrl, moved_tokens); F(gp_ctrl, shrinks);
+  F(gp_req_meta, n_shrinks); F(gp_state_view, tok_pos); F(gp_state_view, free_stack);
   return 0;
 }
 """
@@ -71,6 +73,7 @@ int main(void) {
     assert int(got["gp_layout"]) == ctypes.sizeof(gp.gp_layout)
     assert int(got["gp_req_meta"]) == ctypes.sizeof(gp.gp_req_meta) == 64
     assert int(got["gp_ctrl"]) == ctypes.sizeof(gp.gp_ctrl)
+    assert int(got["gp_state_view"]) == ctypes.sizeof(gp.gp_state_view)
     for key, val in got.items():
         if "." in key:
             s, f = key.split(".")
@@ -98,7 +101,7 @@ def test_pool_bytes_host_only(gp):
 @pytest.mark.parametrize("bad", [
     dict(num_q_heads=6), dict(num_q_heads=16, num_kv_heads=2), dict(page_size=8),
     dict(head_dim=96), dict(head_dim=64), dict(top_p=0.0), dict(top_p=1.5),
-    dict(beta_s=1.0), dict(max_prefix_len=24), dict(mode=7), dict(recent_window=-1),
+    dict(beta_s=1.0), dict(max_prefix_len=24), dict(mode=7), dict(mode=6), dict(recent_window=-1),
     dict(page_size=512),
 ])
 def test_pool_bytes_rejects_unsupported(gp, bad):
@@ -110,4 +113,5 @@ def test_null_arguments_are_rejected_without_gpu(gp):
     assert gp.lib.gp_pool_bytes(None, None) == gp.GP_ERR_INVALID
     assert gp.lib.gp_destroy_pool(None) == gp.GP_ERR_INVALID
     assert gp.lib.gp_decode_step(None, 0, 0, None, None, None, None, None) == gp.GP_ERR_INVALID
+    assert gp.lib.gp_get_state(None, None) == gp.GP_ERR_INVALID
     assert gp.lib.gp_launch_count(None) == 0

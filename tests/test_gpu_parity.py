@@ -4,6 +4,7 @@ Marked ``gpu``: these call the C-ABI library on a B300.  Sizes are the
 workloads' own where the oracle finishes in seconds to a minute; longer
 trajectories are cut to a window that still spans many boundaries.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -227,3 +228,27 @@ def test_empty_steps_and_call_order(env):
     rep = h.run(60)                         # the trajectory continues in step with the oracle
     _check(rep)
     assert rep.boundaries >= 4
+
+
+def test_get_state_matches_per_request_reads(env):
+    # one call copies the whole state; it agrees with the per-request and
+    # counter reads, and with the oracle's block tables and kept positions
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=100, prompt_max=128, budget_pages=8,
+                                                  max_pages_per_req=16)
+    h = H.Harness(w, 4, budget_pages=8)
+    _check(h.run(60))
+    st = h.pool.state(tok_pos=True)
+    c = h.pool.stats()
+    assert st["ctrl"].boundaries == c.boundaries and st["ctrl"].free_top == c.free_top
+    assert len(st["free_stack"]) == c.free_top
+    for s in h.slots:
+        m, bt = h.pool.request(s)
+        assert bytes(st["req"][s]) == bytes(m)
+        assert st["block"][s, : len(bt)].tolist() == bt == h.ora.block_table(s)
+        pos = H._private_positions(st["tok_pos"], bt[m.n_pre_pages:], m.seq_priv, w.num_layers,
+                                   w.num_kv_heads, w.page_size)
+        assert np.array_equal(np.sort(pos, axis=-1), h.ora.kept_positions(s))
+    owned = {p for s in h.slots for p in h.pool.request(s)[1]}
+    assert not owned & set(st["free_stack"].tolist())
+    assert len(owned) + c.free_top == h.cfg.num_pages
