@@ -21,3 +21,20 @@ def test_attention_bytes_by_hand():
     assert bench.attention_bytes(w, 1000, 1, 0) == kv + fixed + bt
     # at a boundary both summaries' fp32 scores are written for every resident key
     assert bench.attention_bytes(w, 1000, 1, 1000) - bench.attention_bytes(w, 1000, 1, 0) == 1000 * 2 * 8 * 4
+
+
+def test_reference_arm_line_on_cpu():
+    # the oracle arm runs on the host cores and prints the contract's line
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--steps", "1", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    for k in ("metric", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "dtype", "config"):
+        assert k in line
