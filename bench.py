@@ -565,7 +565,7 @@ def main():
         line = run_reference(args, ws, rank)
     else:
         line = run_ours(args, ws, rank, local)
-        if line is not None and not args.no_cpu_baseline:
+        if line is not None and not args.no_cpu_baseline and ws == 1:  # N = 1 only
             w = workload_for(args)
             v, s, e, cores = oracle_sample(w, args.cpu_seconds)
             line["cpu_baseline"] = {
