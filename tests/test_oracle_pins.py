@@ -516,3 +516,41 @@ def test_topp_near_tie_band():
     # a dominant token: W = 1 for any Top-p up to its mass
     q = np.array([0.97, 0.01, 0.01, 0.01])
     assert pol.topp_range(q, 0.9) == (1, 1)
+
+
+def test_shrink_with_prefix_and_several_requests_keeps_invariants():
+    # SHRINK with a shared prefix and three requests at boundaries in the same
+    # steps: request 1 sees one constant query, so its two summaries stay
+    # equal (Delta = 0) and it releases pages, while the other two see random
+    # queries and grow.  Every page is owned once, prefix tokens are never
+    # dropped, and pages released in a step go on the stack after the step's
+    # pops, in ascending slot order.
+    cfg = _small_cfg(num_pages=80, num_layers=1, policy="shrink", recent_window=16)
+    rng = np.random.default_rng(21)
+    pool = OraclePool(cfg)
+    L, hk, hq, d = 1, cfg.num_kv_heads, cfg.num_q_heads, cfg.head_dim
+    pid = pool.add_prefix(rng.standard_normal((L, 32, hk, d)), rng.standard_normal((L, 32, hk, d)))
+    for s, pre in enumerate([pid, -1, pid]):
+        pool.add_request(s, rng.standard_normal((L, 96, hk, d)), rng.standard_normal((L, 96, hk, d)),
+                         6, pre)
+    q_const = rng.standard_normal((L, hq, d))
+    mixed = 0
+    for t in range(160):
+        before = {s: list(pool.req[s].pages) for s in range(3)}
+        q = rng.standard_normal((3, L, hq, d))
+        q[1] = q_const
+        res = pool.step([0, 1, 2], q, rng.standard_normal((3, L, hk, d)),
+                        rng.standard_normal((3, L, hk, d)))
+        pool.check_invariants()
+        recs = res["records"]
+        released = [before[s][-1] for s in sorted(recs) if recs[s].decision == SHRINK]
+        grown = [pool.req[s].pages[-1] for s in sorted(recs) if recs[s].decision == GROW]
+        if released:
+            assert pool.free[-len(released):] == released
+            assert not set(released) & set(grown)
+            mixed += bool(grown)
+        if 1 in recs and len(before[1]) >= 3:
+            assert recs[1].delta == 0 and recs[1].decision == SHRINK
+        for s in range(3):
+            assert np.all(pool.kept_positions(s) >= pool.req[s].prefix_len)
+    assert mixed >= 2
