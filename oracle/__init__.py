@@ -28,6 +28,13 @@ Parity status of each function (what pins it, see tests/test_oracle_pins.py):
 * ``pool.OraclePool``       pinned: dense softmax attention (torch SDPA) with
                             compaction off; GQA G=1 equals MHA; pool
                             invariants; hand-built grow / compact cases.
+* boundary wiring: ``OraclePool._summary_scores``, ``policy.private_importance``
+  and ``policy.delta_range``, pinned in tests/test_oracle_boundary_pins.py:
+  the summary scores against a recomputation with complex-rotation RoPE and
+  closed-form EMAs; the importance normalisation by a case where
+  normalising over private tokens only keeps another set; the near-tie
+  exemption by enumerating every working-set size inside its band.  Each
+  pin is shown to fail on its plausible mistake.
 * decision statistics vs the paper's measured grow ratios: parity unpinned
   (the pages print no worked example or intermediate values).
 """

@@ -64,6 +64,35 @@ def importance(p_short: np.ndarray, p_long: np.ndarray) -> np.ndarray:
     return np.maximum(np.asarray(p_short, np.float64), np.asarray(p_long, np.float64))
 
 
+def private_importance(u_short: np.ndarray, u_long: np.ndarray, prefix_len: int) -> np.ndarray:
+    """Importance of the private tokens from both summaries' scores.
+
+    u_short, u_long: scores of every resident token, prefix first.  Each
+    summary's probabilities are one softmax over the whole resident set
+    (prefix included: the prefix is part of the attention distribution the
+    summary induces); the private tokens' entries are then taken, and the
+    importance is the larger of the two probabilities.  Reading: the review's
+    Summary says compaction ranks history by "the maximum of both temporal
+    importance scores"; normalising each over the same resident set keeps the
+    two scores comparable.
+    """
+    ps = softmax(u_short)[prefix_len:]
+    pl = softmax(u_long)[prefix_len:]
+    return importance(ps, pl)
+
+
+def delta_range(band_short: np.ndarray, band_long: np.ndarray):
+    """Smallest and largest Delta when every W may take any value of its band.
+
+    band_*: [..., 2] integer (W at Top-p*(1-1e-5), W at Top-p*(1+1e-5)) per
+    (layer, kv head).  Delta is smallest with every short W at its low end
+    and every long W at its high end, and largest the other way round.
+    """
+    bs = np.asarray(band_short, dtype=np.int64)
+    bl = np.asarray(band_long, dtype=np.int64)
+    return int(np.sum(bs[..., 0] - bl[..., 1])), int(np.sum(bs[..., 1] - bl[..., 0]))
+
+
 def drop_set(imp: np.ndarray, pos: np.ndarray, n_drop: int) -> np.ndarray:
     """Indices of the n_drop candidates ranked lowest by (importance, position).
 

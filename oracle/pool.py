@@ -39,7 +39,8 @@ Readings this module takes (the pages leave them open):
   Pages released by the SHRINK ablation are pushed after every growth of the
   step has popped, in ascending slot order.
 * Full-KV mode: the same steps, every boundary grows, nothing is compacted;
-  a boundary with no free page drops the step's token ("starved").
+  a boundary that cannot get a page (none free, or the request already holds
+  max_pages_per_req) drops the step's token ("starved").
 """
 from __future__ import annotations
 
@@ -154,6 +155,7 @@ class BoundaryRecord:
     w_near_tie: np.ndarray       # [L][Hk][2] bool: W moves inside the band
     cut_gap: Optional[np.ndarray]  # [L][Hk] relative gap at the kept-set cut
     logits: Optional[np.ndarray] = None  # [L][Hk][2][R] when kept
+    w_band: Optional[np.ndarray] = None  # [L][Hk][2][2]: W at Top-p*(1-1e-5), *(1+1e-5)
 
 
 class OraclePool:
@@ -235,6 +237,19 @@ class OraclePool:
             self._unref(r.prefix_id)
 
     # ------------------------------------------------------------- step ----
+    def _summary_scores(self, Kres, s, pos_t, scale):
+        """Summary scores of one layer: u_j = RoPE(s, pos_t) . k_j / sqrt(d).
+
+        Kres: [Hk][R][d] resident keys (prefix first, then private; the step's
+        staged token is not among them), stored rotated to their own
+        positions.  s: [Hk][d] fp32 summary, kept pre-RoPE.  Reading: the
+        review keeps the summaries pre-RoPE, so a summary is rotated to the
+        current position before it meets the rotated cache, as a query of
+        that position would be.
+        """
+        sr = nm.rope_apply(np.asarray(s, dtype=np.float64), self.rope, pos_t)
+        return np.matmul(Kres, sr[:, :, None])[:, :, 0] * scale
+
     def step(self, slots, q, k, v, arbiter=None):
         """One decode step for the requests ``slots`` (ascending).
 
@@ -305,8 +320,7 @@ class OraclePool:
                 # A4: summary logits against every resident key.
                 if at_b and not c.full_kv:
                     for X, s in ((0, r.s_short[l]), (1, r.s_long[l])):
-                        sr = nm.rope_apply(s.astype(np.float64), self.rope, pos_t)
-                        lg[l, :, X] = np.matmul(Kres, sr[:, :, None])[:, :, 0] * scale
+                        lg[l, :, X] = self._summary_scores(Kres, s, pos_t, scale)
             if at_b:
                 boundary_logits[slot] = lg
         # A5/A6: working sets and decisions; A7: growth in ascending slot order.
@@ -317,7 +331,7 @@ class OraclePool:
             if r.toks.n != cap:
                 continue
             if c.full_kv:
-                if self.free:
+                if self.free and len(r.pages) < c.max_pages_per_req:
                     r.pages.append(self.free.pop())
                     decisions[slot] = GROW
                 else:
@@ -339,8 +353,7 @@ class OraclePool:
                         W[l, g] = pol.topp_count(pr, c.top_p)
                         band[l, g, X] = pol.topp_range(pr, c.top_p)
             delta = pol.demand_delta(ws, wl)
-            dmin = int(np.sum(band[:, :, 0, 0] - band[:, :, 1, 1]))
-            dmax = int(np.sum(band[:, :, 0, 1] - band[:, :, 1, 0]))
+            dmin, dmax = pol.delta_range(band[:, :, 0], band[:, :, 1])
             if c.policy in ("growpage", "shrink"):
                 want = pol.wants_grow(delta, c.tau)
                 exempt = pol.wants_grow(dmin, c.tau) != pol.wants_grow(dmax, c.tau)
@@ -374,7 +387,7 @@ class OraclePool:
             decisions[slot] = dec
             near = band[:, :, :, 0] != band[:, :, :, 1]
             records[slot] = BoundaryRecord(slot, delta, dec, exempt, ws, wl, near, None,
-                                           lg if self.keep_logits else None)
+                                           lg if self.keep_logits else None, band)
         # SHRINK releases the last private page of each shrinking request, in
         # ascending slot order, after every growth of the step has popped.
         for slot in sorted(decisions):
@@ -396,9 +409,7 @@ class OraclePool:
             newpos = np.zeros((L, hk, r.toks.cap), np.int64)
             for l in range(L):
                 for g in range(hk):
-                    ps = pol.softmax(lg[l, g, 0])[plen:]
-                    pl = pol.softmax(lg[l, g, 1])[plen:]
-                    imp = pol.importance(ps, pl)
+                    imp = pol.private_importance(lg[l, g, 0], lg[l, g, 1], plen)
                     posp = r.toks.pos[l, g, :cap]
                     dropped, gap = pol.compaction_plan(imp, posp, r.pos, cap, P,
                                                        c.recent_window, n_free)
