@@ -568,7 +568,9 @@ std::mutex g_static_mu;
 uint8_t* g_static_addr[kMaxDevices] = {};
 
 // Device address of g_static_scratch on the current device (set up once per
-// device; the host-side name of the array is not a device address).
+// device; the host-side name of the array is not a device address).  The
+// address stays valid while the device's primary context lives, which the
+// header asks callers to keep for the life of the process.
 cudaError_t static_scratch(uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -624,6 +626,20 @@ int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int3
 int gp_sync(gp_pool* pool) {
   if (!pool) return GP_ERR_INVALID;
   return sync_status(pool);
+}
+
+int gp_clear_status(gp_pool* pool, uint32_t* status_out, int32_t* info_out) {
+  if (!pool) return GP_ERR_INVALID;
+  cudaError_t e = cudaStreamSynchronize(pool->stream);
+  uint32_t st[2] = {0u, 0u};  // status, status_info (adjacent in gp_ctrl)
+  if (e == cudaSuccess) e = cudaMemcpy(st, &pool->dev.ctrl->status, 8, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemsetAsync(&pool->dev.ctrl->status, 0, 8, pool->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(pool->stream);
+  if (e != cudaSuccess) return cuda_fail(pool, e, "gp_clear_status");
+  if (status_out) *status_out = st[0];
+  if (info_out) *info_out = (int32_t)st[1];
+  pool->err.clear();
+  return GP_OK;
 }
 
 int gp_get_stats(gp_pool* pool, gp_ctrl* out) {

@@ -194,11 +194,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
     p.plan_misc[0] = good;
     p.plan_misc[1] = s_bad ? 0 : bcarry;
     p.plan_misc[2] = carry;
-    if (count) {
+    if (count) {  // a rejected step (bad slot list) is not counted
       p.ctrl->plan_n = good;
-      p.ctrl->steps += 1;
-      p.ctrl->tokens_attended += (long long)s_tok;
-      p.ctrl->boundary_tokens += (long long)s_btok;
+      if (!s_bad) {
+        p.ctrl->steps += 1;
+        p.ctrl->tokens_attended += (long long)s_tok;
+        p.ctrl->boundary_tokens += (long long)s_btok;
+      }
     }
   }
 }
@@ -732,10 +734,11 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
           atomicAdd(&s_cnt[2], 1ull);
           if (want) { m.n_denied += 1; atomicAdd(&s_cnt[3], 1ull); }
         } else {
+          // full KV and no page (none free, or the request at its cap): the
+          // step's token is dropped; counted, not a fault
           dec = kStarved; commit = -1;
           m.n_starved += 1;
           atomicAdd(&s_cnt[4], 1ull);
-          set_status(p, GP_ST_STARVED, slot);
         }
       } else {
         dec = kNone; commit = m.seq_priv;

@@ -88,6 +88,8 @@ def _load():
         "gp_boundary": (ctypes.c_int, [P, I32, P]),
         "gp_free": (ctypes.c_int, [P, I32]),
         "gp_sync": (ctypes.c_int, [P]),
+        "gp_clear_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32),
+                                           ctypes.POINTER(I32)]),
         "gp_get_stats": (ctypes.c_int, [P, ctypes.POINTER(gp_ctrl)]),
         "gp_get_request": (ctypes.c_int, [P, I32, ctypes.POINTER(gp_req_meta),
                                           ctypes.POINTER(I32), I32]),
@@ -210,6 +212,12 @@ class Pool:
 
     def sync(self):
         self._check(lib.gp_sync(self.h))
+
+    def clear_status(self):
+        """Read and clear the device status word: (GP_ST_* bits, info)."""
+        st, info = ctypes.c_uint32(0), ctypes.c_int32(0)
+        self._check(lib.gp_clear_status(self.h, ctypes.byref(st), ctypes.byref(info)))
+        return st.value, info.value
 
     def stats(self) -> gp_ctrl:
         s = gp_ctrl()

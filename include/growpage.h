@@ -58,7 +58,8 @@ extern "C" {
 #define GP_ST_BAD_SLOTS    0x1u  /* slot list not ascending / not active     */
 #define GP_ST_BAD_PAGE     0x2u  /* a block-table entry outside the pool     */
 #define GP_ST_TIMEOUT      0x4u  /* a bounded wait gave up                   */
-#define GP_ST_STARVED      0x8u  /* full-KV boundary with no free page       */
+#define GP_ST_STARVED      0x8u  /* not raised: a starved full-KV boundary is
+                                    counted in gp_ctrl.starved instead       */
 #define GP_ST_BAD_PLAN     0x10u /* inconsistent compaction plan            */
 #define GP_ST_POS_RANGE    0x20u /* a request reached max_seq_len            */
 
@@ -225,7 +226,11 @@ int gp_add_prefix(gp_pool* pool, const void* k_prefix, const void* v_prefix,
                   int32_t len, int32_t* prefix_id);
 int gp_release_prefix(gp_pool* pool, int32_t prefix_id);
 
-/* Admit a request into an empty slot (continuous batching).  Its block
+/* Admit a request into an empty slot.  Follows the abstract of "GrowPage:
+ * On-Demand KV Budgeting for Efficient LLM Reasoning Serving": requests live
+ * on PagedAttention's page-level memory with continuous batching and prefix
+ * caching kept, so a request joins between steps with an initial KV budget
+ * of physical pages and may share a cached prefix.  Its block
  * table becomes the prefix's pages (prefix_id >= 0) followed by
  * budget_pages freshly popped private pages (the initial KV budget).
  * k_prompt, v_prompt: device [L][prompt_len][Hk][d] (keys not yet
@@ -239,7 +244,13 @@ int gp_add_request(gp_pool* pool, int32_t slot, const void* k_prompt,
 
 /* One layer of one decode step for the n requests in slots_dev (device
  * int32[n], strictly ascending active slots; the same list for every layer
- * of the step).  q, out: [n][Hq][d]; k_new, v_new: [n][Hk][d]; q and k_new
+ * of the step).  Follows the evolve.pub review of "GrowPage: On-Demand KV
+ * Budgeting for Efficient LLM Reasoning Serving", section "Summary": paged
+ * (PagedAttention) decode attention, with the short (beta 0.9) and long
+ * (beta 0.999) exponentially smoothed query summaries maintained pre-RoPE,
+ * and, at a capacity boundary, the attention scores those summaries induce
+ * over the resident keys (their Top-p working sets are taken by
+ * gp_boundary).  q, out: [n][Hq][d]; k_new, v_new: [n][Hk][d]; q and k_new
  * are pre-RoPE.  For each request i, kv head g and query head h in
  * [g*G, (g+1)*G):
  *   - stages k_new rotated to the request's position (fp64 rotation, one
@@ -257,7 +268,14 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n,
                    const int32_t* slots_dev, const void* q, const void* k_new,
                    const void* v_new, void* out);
 
-/* Finish the step for the same n requests: for each request at a boundary,
+/* Finish the step for the same n requests.  Follows the abstract of
+ * "GrowPage: On-Demand KV Budgeting for Efficient LLM Reasoning Serving" (at
+ * each capacity boundary, compress KV within the current allocation or
+ * acquire one more physical page) and its evolve.pub review, section
+ * "Summary" (compare the Top-p working sets of the two summaries; a larger
+ * recent one allocates an extra page, otherwise compact by the maximum of
+ * both importance scores) and "Frequently asked questions" (Top-p, demand
+ * threshold tau = 0, local retention quota).  For each request at a boundary,
  * softmax of each summary's scores, Top-p working-set sizes W_S, W_L per
  * (layer, kv head), Delta = sum (W_S - W_L); grow by one page iff
  * Delta > tau, a page is free and n_pages < max_pages_per_req (requests
@@ -300,7 +318,10 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
  * once at start-up, or a runtime whose allocator must not be entered at that
  * point -- and for callers that must not disturb the pool's own scratch,
  * which gp_kv_read_ceiling overwrites (so that one may only run between
- * steps).  Same arguments, result and rules as gp_kv_read_ceiling, except:
+ * steps).  Same arguments and result as gp_kv_read_ceiling, except:
+ *   - it leaves the pool's scratch untouched, so it may also be called
+ *     between two layers of a step (after gp_decode_step(layer), before the
+ *     next layer): the step's outputs and decisions do not change;
  *   - the per-call scratch (the step plan of the n requests and the start
  *     cursor and first block of every attention worker) lives in a file-scope
  *     device array of this library, about 155 KB, which every GPU that loads the library
@@ -309,7 +330,9 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
  *   - n may not exceed 1024 (GP_ERR_INVALID with a message otherwise);
  *   - the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture;
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: it assumes the device's primary context lives as long, so do
+ *     not reset the device (cudaDeviceReset) while the library is used there;
  *   - all calls share the array: two calls whose work overlaps on the GPU
  *     (different streams, or different pools on one device) race.
  * It calls no cudaMalloc, cudaFree or allocating library routine.
@@ -318,8 +341,23 @@ int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int3
                               int32_t n, const int32_t* slots_dev, uint32_t* sink_dev);
 
 /* Wait for the stream; GP_ERR_DEVICE if the device status word is set.
- * SYNC. */
+ * The word stays set (every later gp_sync reports it) until
+ * gp_clear_status.  SYNC. */
 int gp_sync(gp_pool* pool);
+
+/* Read and clear the device status word: *status_out receives the GP_ST_*
+ * bits that were set and *info_out the first offending slot or page (either
+ * pointer may be NULL).  What a flagged step left behind:
+ *   GP_ST_BAD_SLOTS / GP_ST_POS_RANGE: the plan kernel dropped the whole
+ *     step before any state changed (no token staged, no summary folded, no
+ *     boundary work, `out` not written); the pool continues as if the step
+ *     had not been called;
+ *   GP_ST_TIMEOUT: a bounded wait gave up; that step's outputs are
+ *     incomplete;
+ *   GP_ST_BAD_PAGE: an out-of-range page id was read as page 0; the
+ *     affected request's contents are undefined.
+ * SYNC. */
+int gp_clear_status(gp_pool* pool, uint32_t* status_out, int32_t* info_out);
 
 /* Copy the pool-wide counters to the host.  SYNC. */
 int gp_get_stats(gp_pool* pool, gp_ctrl* out);

@@ -134,7 +134,9 @@ class Harness:
         self.outs = [torch.empty(n_req, hq, d, dtype=w.torch_dtype, device=dev) for _ in range(L)]
 
     # -------------------------------------------------------------------
-    def step(self, check=True):
+    def step(self, check=True, after_layer=None):
+        """One step on both sides; ``after_layer(l)`` (optional) runs after
+        the GPU call of layer l, before the next one."""
         w, rep = self.w, self.rep
         L, hk, hq, d, P = w.num_layers, w.num_kv_heads, w.num_q_heads, w.head_dim, w.page_size
         qs, ks, vs = [], [], []
@@ -148,6 +150,8 @@ class Harness:
         for l in range(L):
             self.pool.decode_step(l, self.slots_dev, qd[:, l].contiguous(), kd[:, l].contiguous(),
                                   vd[:, l].contiguous(), self.outs[l])
+            if after_layer is not None:
+                after_layer(l)
         self.pool.boundary(self.slots_dev)
         self.pool.sync()
         # GPU state after the step
@@ -247,9 +251,9 @@ class Harness:
                 if not np.array_equal(got, want):
                     rep.fail(f"step {t} slot {s}: kept positions differ")
 
-    def run(self, steps, check_every=1):
+    def run(self, steps, check_every=1, after_layer=None):
         for t in range(steps):
-            self.step(check=(t % check_every == 0))
+            self.step(check=(t % check_every == 0), after_layer=after_layer)
             if self.rep.failures:
                 break
         return self.rep

@@ -252,3 +252,69 @@ def test_get_state_matches_per_request_reads(env):
     owned = {p for s in h.slots for p in h.pool.request(s)[1]}
     assert not owned & set(st["free_stack"].tolist())
     assert len(owned) + c.free_top == h.cfg.num_pages
+
+
+def test_select_rows_beyond_shared_memory(env):
+    # Rows longer than the select kernel stages in shared memory (4096
+    # tokens): the working-set counts and the compaction keys read the scores
+    # and token positions from global memory.  One Llama-3-8B-shaped layer,
+    # 4 requests whose 4480-token prompts fill their 280-page budgets, so the
+    # first boundary is on step 1 and then every 16 steps.
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=4480, prompt_max=4480,
+                                                  budget_pages=280, max_pages_per_req=320,
+                                                  num_pages=1400)
+    h = H.Harness(w, 4, budget_pages=280, max_seq_len=4480 + 200)
+    rep = h.run(130)
+    _check(rep)
+    assert rep.boundaries == 4 * 9
+    assert rep.grows > 0 and rep.compacts > 0
+    assert rep.max_out_err < 2e-2
+
+
+def test_select_rows_beyond_shared_memory_with_prefix(env):
+    # The 36-layer Qwen3-shaped workload's request shape on one layer: a
+    # 2048-token shared prefix plus 2304 private tokens (R = 4352 > 4096,
+    # C = 2304), three requests sharing the prefix.
+    H, gp, synth = env
+    w = synth.WORKLOADS["qwen3_8b_36layer_cb"].replace(
+        num_layers=1, prompt_min=2304, prompt_max=2304, budget_pages=144, max_pages_per_req=200)
+    sc = H.Scenario(w, max_requests=3, num_pages=1200, max_prefixes=2,
+                    max_seq_len=2048 + 2304 + 200)
+    sc.add_prefix(0)
+    for s in range(3):
+        sc.admit(s, s, prefix=0, budget_pages=144)
+    sc.release_prefix(0)
+    for _ in range(110):
+        sc.step()
+        if sc.rep.failures:
+            break
+        sc.ora.check_invariants()
+    _check(sc.rep)
+    assert sc.rep.boundaries == 3 * 7
+    assert sc.rep.compacts > 0
+
+
+@pytest.mark.parametrize("shape", ["tiny", "llama8b_1layer"])
+def test_full_kv_stops_at_the_page_cap(env, shape):
+    # Full KV with a cap on a request's private pages: once a request holds
+    # max_pages_per_req pages its boundaries cannot grow, and drop the step's
+    # token (starved), as a boundary with no free page does.  Starvation is
+    # counted, not raised: the pool's status word stays clear.
+    H, gp, synth = env
+    if shape == "tiny":
+        w = synth.WORKLOADS["tiny"].replace(max_pages_per_req=6)
+        n, budget, steps = 1, None, 120
+    else:
+        w = synth.WORKLOADS["llama8b_1layer"].replace(prompt_min=100, prompt_max=128,
+                                                      budget_pages=8, max_pages_per_req=10)
+        n, budget, steps = 4, 8, 120
+    h = H.Harness(w, n, mode=gp.GP_MODE_FULL_KV, budget_pages=budget)
+    rep = h.run(steps)
+    _check(rep)
+    st = h.pool.stats()
+    assert st.starved > 0 and st.status == 0
+    assert st.starved + st.grows == st.boundaries == rep.boundaries
+    for s in h.slots:
+        m, _ = h.pool.request(s)
+        assert m.n_pages == w.max_pages_per_req and m.n_starved > 0
