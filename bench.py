@@ -73,6 +73,19 @@ def parse():
                     help="override the page-pool size in GB (small profiling cases)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch size (small profiling cases)")
+    ap.add_argument("--late-preroll", type=int, default=4096,
+                    help="second timed window of the default workload after this many decode "
+                         "steps, where full KV has grown (0: none)")
+    ap.add_argument("--late-steps", type=int, default=128)
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads (1-layer, continuous batching, burst)")
+    ap.add_argument("--workloads", default="llama8b_1layer,qwen3_8b_36layer_cb,stress_burst")
+    ap.add_argument("--cb-preroll", type=int, default=2560,
+                    help="continuous-batching workload: decode steps before its window "
+                         "(arrivals fill the 128 slots by about step 1600)")
+    ap.add_argument("--cb-steps", type=int, default=128)
+    ap.add_argument("--burst-steps", type=int, default=1024,
+                    help="burst workload: timed steps from its first step (a burst every 16)")
     return ap.parse_args()
 
 
@@ -196,6 +209,117 @@ def attention_bytes(w, tok, req_steps, btok):
 
 # ------------------------------------------------------------ our arm
 
+def _load_peaks():
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = json.load(open(pk)) if os.path.exists(pk) else {}
+    if "hbm_gbs" in peaks:
+        return float(peaks["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+def time_window(eng, steps, w, sample_clocks=False, local=0):
+    """Time `steps` decode steps of an engine with CUDA events on its stream.
+
+    Events per step: before the step, after layer 0, after the last layer,
+    after the boundary call.  The layer-call time is taken over layers
+    1..L-1 (for a 1-layer stack: the whole step before the boundary call,
+    plan kernel included).  Returns the window's counters and times.
+    """
+    stream = eng.pool.stream
+    L = w.num_layers
+    torch.cuda.synchronize()
+    st0 = eng.pool.stats()
+    launches0 = eng.pool.launch_count()
+    tok0 = eng.tokens_timed
+    pre0 = eng.preempted
+    evs, nbs = [], []
+    req_steps = 0
+    clk = ClockSampler(local) if sample_clocks else None
+    if clk:
+        clk.start()
+    for _ in range(steps):
+        eng.prepare_inputs()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+
+        def before():
+            e[0].record(stream)
+
+        def after_layer(l):
+            if l == 0:
+                e[1].record(stream)
+            if l == L - 1:
+                e[2].record(stream)
+
+        def after():
+            e[3].record(stream)
+
+        n = eng.step(timed=True, before_step=before, after_layer=after_layer, after_step=after)
+        if n:
+            req_steps += n
+            evs.append(e)
+            nbs.append(eng.last_boundaries)
+    torch.cuda.synchronize()
+    clocks = clk.stop() if clk else None
+    st1 = eng.pool.stats()
+    step_t = [e[0].elapsed_time(e[3]) for e in evs]
+    bnd_t = [e[2].elapsed_time(e[3]) for e in evs]
+    if L > 1:
+        attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
+        n_attn = (L - 1) * len(evs)
+    else:
+        attn_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
+        n_attn = len(evs)
+    step_ms = sum(step_t)
+    dtok = st1.tokens_attended - st0.tokens_attended
+    dbtok = st1.boundary_tokens - st0.boundary_tokens
+    nsteps = max(1, len(evs))
+    per_layer_bytes = attention_bytes(w, dtok, req_steps, dbtok)   # one layer, all steps
+    res = dict(steps=len(evs), step_ms=step_ms, attn_ms=attn_ms, tokens=eng.tokens_timed - tok0,
+               clocks=clocks, launches=eng.pool.launch_count() - launches0, dtok=dtok,
+               dbtok=dbtok, req_steps=req_steps,
+               boundaries=st1.boundaries - st0.boundaries, grows=st1.grows - st0.grows,
+               compacts=st1.compacts - st0.compacts, denied=st1.denied - st0.denied,
+               shrinks=st1.shrinks - st0.shrinks, starved=st1.starved - st0.starved,
+               moved=st1.moved_tokens - st0.moved_tokens, preempted=eng.preempted - pre0,
+               free_pages=st1.free_top, num_pages=eng.num_pages,
+               attn_launch_ms=attn_ms / n_attn if n_attn else float("nan"),
+               attn_bytes_per_launch=per_layer_bytes / nsteps,
+               attn_gbs=(per_layer_bytes * n_attn / nsteps / (attn_ms * 1e-3) / 1e9) if attn_ms else 0.0,
+               step_bytes=per_layer_bytes * L / nsteps,
+               step_gbs=per_layer_bytes * L / (step_ms * 1e-3) / 1e9 if step_ms else 0.0)
+    # steps with boundaries against steps without (the boundary burst)
+    bt = [(t, b) for t, b, nb in zip(step_t, bnd_t, nbs) if nb > 0]
+    qt = [t for t, nb in zip(step_t, nbs) if nb == 0]
+    res["boundary_steps"] = len(bt)
+    res["boundary_step_ms"] = sum(t for t, _ in bt) / len(bt) if bt else None
+    res["boundary_call_ms"] = sum(b for _, b in bt) / len(bt) if bt else None
+    res["plain_step_ms"] = sum(qt) / len(qt) if qt else None
+    res["mean_boundaries_per_boundary_step"] = (sum(nb for nb in nbs if nb) / len(bt)) if bt else 0
+    return res
+
+
+def summarize(r, ws, hbm_peak):
+    """The per-mode object of the JSON line from a timed window."""
+    o = {"value": round(r["tokens"] / (r["step_ms"] * 1e-3) * ws, 1) if r["step_ms"] else 0.0,
+         "unit": "tokens/s",
+         "ms_per_step": round(r["step_ms"] / max(1, r["steps"]), 4),
+         "layer_call_gbs": round(r["attn_gbs"], 1),
+         "layer_call_frac": round(r["attn_gbs"] / hbm_peak, 4),
+         "step_gbs": round(r["step_gbs"], 1),
+         "mean_batch": round(r["req_steps"] / max(1, r["steps"]), 1),
+         "mean_resident_tokens": round(r["dtok"] / max(1, r["req_steps"]), 1)}
+    o.update({k: int(r[k]) for k in ("steps", "tokens", "boundaries", "grows", "compacts",
+                                     "denied", "starved", "shrinks", "preempted")})
+    if r["boundary_steps"]:
+        o["boundary_steps"] = {
+            "count": r["boundary_steps"],
+            "mean_requests_at_boundary": round(r["mean_boundaries_per_boundary_step"], 1),
+            "step_ms": round(r["boundary_step_ms"], 4),
+            "boundary_call_ms": round(r["boundary_call_ms"], 4),
+            "plain_step_ms": round(r["plain_step_ms"], 4) if r["plain_step_ms"] else None}
+    return o
+
+
 def run_ours(args, ws, rank, local):
     from demand_paged_kv_gqa_b300 import growpage as gpb
     from demand_paged_kv_gqa_b300 import synth
@@ -204,88 +328,34 @@ def run_ours(args, ws, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workload_for(args)
-    peaks = {}
-    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(pk):
-        peaks = json.load(open(pk))
-    hbm_peak = float(peaks.get("hbm_gbs", 6400.0))
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    hbm_peak, peak_src = _load_peaks()
 
-    def measure(mode, label, rate=0.0):
-        eng = Engine(w, mode=mode, device=dev, seed_offset=rank, random_grow_rate=rate)
+    def run_engine(wl, mode, label, windows, rate=0.0, extras=False):
+        """One engine; windows = [(decode steps before the window, timed steps)].
+        The warm-up steps come right before the first window."""
+        eng = Engine(wl, mode=mode, device=dev, seed_offset=rank, random_grow_rate=rate)
         eng.fill()
-        stream = eng.pool.stream
-        for _ in range(args.preroll):
-            eng.prepare_inputs()
-            eng.step()
-        for _ in range(args.warmup):
-            eng.prepare_inputs()
-            eng.step()
-        torch.cuda.synchronize()
-        if ws > 1:
-            torch.distributed.barrier()
-        st0 = eng.pool.stats()
-        launches0 = eng.pool.launch_count()
-        tok0 = eng.tokens_timed
-        L = w.num_layers
-        evs = []
-        req_steps = 0
-        clk = ClockSampler(local)
-        clk.start()
-        t_wall = time.time()
-        for _ in range(args.steps):
-            eng.prepare_inputs()
-            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-
-            def before():
-                e[0].record(stream)
-
-            def after_layer(l):
-                if l == 0:
-                    e[1].record(stream)
-                elif l == L - 1:
-                    e[2].record(stream)
-
-            def after():
-                e[3].record(stream)
-
-            n = eng.step(timed=True, before_step=before, after_layer=after_layer, after_step=after)
-            req_steps += n
-            evs.append(e)
-        torch.cuda.synchronize()
-        wall = time.time() - t_wall
-        clocks = clk.stop()
-        st1 = eng.pool.stats()
-        launches = eng.pool.launch_count() - launches0
-        step_ms = sum(e[0].elapsed_time(e[3]) for e in evs)
-        attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
-        tokens = eng.tokens_timed - tok0
-        dtok = st1.tokens_attended - st0.tokens_attended
-        dbtok = st1.boundary_tokens - st0.boundary_tokens
-        res = dict(label=label, step_ms=step_ms, attn_ms=attn_ms, tokens=tokens, wall=wall,
-                   clocks=clocks, launches=launches, dtok=dtok, dbtok=dbtok, req_steps=req_steps,
-                   boundaries=st1.boundaries - st0.boundaries, grows=st1.grows - st0.grows,
-                   compacts=st1.compacts - st0.compacts, denied=st1.denied - st0.denied,
-                   shrinks=st1.shrinks - st0.shrinks,
-                   moved=st1.moved_tokens - st0.moved_tokens, preempted=eng.preempted,
-                   free_pages=st1.free_top, num_pages=eng.num_pages)
-        # attention kernel: layers 1..L-1 of each timed step
-        n_attn = (L - 1) * args.steps
-        per_layer_bytes = attention_bytes(w, dtok, req_steps, dbtok)  # one layer, all steps
-        res["attn_launch_ms"] = attn_ms / n_attn if n_attn else float("nan")
-        res["attn_bytes_per_launch"] = per_layer_bytes / args.steps
-        res["attn_gbs"] = (per_layer_bytes * (L - 1) / (attn_ms * 1e-3) / 1e9) if attn_ms else 0.0
-        res["step_bytes"] = per_layer_bytes * L / args.steps
-        res["step_gbs"] = per_layer_bytes * L / (step_ms * 1e-3) / 1e9 if step_ms else 0.0
-        res["ceilings"] = measure_ceilings(eng) if label == "growpage" else None
-        res["e2e"] = (measure_e2e(eng, args.e2e_steps, args.e2e_chunk, bool(args.e2e_ramp))
-                      if (args.e2e_steps and label == "growpage") else None)
+        out = []
+        for k, (start, steps) in enumerate(windows):
+            target = start + (args.warmup if k == 0 else 0)
+            while eng.clock < target:
+                eng.prepare_inputs()
+                eng.step()
+            if k == 0 and ws > 1:
+                torch.distributed.barrier()
+            r = time_window(eng, steps, wl, sample_clocks=(k == 0), local=local)
+            r["label"], r["start"] = label, eng.clock - steps
+            if k == 0 and extras:
+                r["ceilings"] = measure_ceilings(eng, wl)
+                r["e2e"] = (measure_e2e(eng, wl, args.e2e_steps, args.e2e_chunk, bool(args.e2e_ramp))
+                            if args.e2e_steps else None)
+            out.append(r)
         eng.pool.sync()
         del eng
         torch.cuda.empty_cache()
-        return res
+        return out
 
-    def measure_ceilings(eng):
+    def measure_ceilings(eng, wl):
         """Read-only streaming of the same resident K/V through the same grid:
         paged (the attention kernel's access pattern), sequential TMA, and
         sequential plain loads; GB/s of bytes moved."""
@@ -295,7 +365,7 @@ def run_ours(args, ws, rank, local):
         slots = torch.tensor(act, dtype=torch.int32, device=dev)
         sink = torch.zeros(4, dtype=torch.int32, device=dev)
         stream = eng.pool.stream
-        L = w.num_layers
+        L = wl.num_layers
         out = {}
         for mode, name in ((0, "paged_tma"), (1, "seq_tma"), (2, "seq_ldg")):
             eng.pool.kv_read_ceiling(0, L, mode, slots, sink)      # warm
@@ -321,7 +391,7 @@ def run_ours(args, ws, rank, local):
             size = min(2 * size, chunk)
         return out
 
-    def measure_e2e(eng, k, chunk=8, ramp=True):
+    def measure_e2e(eng, wl, k, chunk=8, ramp=True):
         """Same metric through the C-ABI with each step's q, k, v copied from
         pinned host memory and its outputs copied back to pinned host memory,
         all copies inside the events.  The copies run on a second stream in
@@ -334,7 +404,7 @@ def run_ours(args, ws, rank, local):
         groups end small (little is left to copy after the last layer)."""
         stream = eng.pool.stream
         copy = torch.cuda.Stream(device=dev)
-        L = w.num_layers
+        L = wl.num_layers
         chunks = groups(L, chunk, ramp)
         out_chunks = [(L - b, L - a) for a, b in reversed(groups(L, chunk, ramp))]
         hq_ = torch.empty_like(eng.q, device="cpu").pin_memory()
@@ -391,8 +461,12 @@ def run_ours(args, ws, rank, local):
         d2h = ho_.nbytes
         return dict(value=toks / (ms * 1e-3), h2d=h2d, d2h=d2h)
 
-    gp_res = measure(gpb.GP_MODE_GROWPAGE, "growpage")
-    fk_res = None if args.no_full_kv else measure(gpb.GP_MODE_FULL_KV, "full_kv")
+    windows = [(args.preroll, args.steps)]
+    if args.late_preroll and args.late_preroll > args.preroll + args.warmup + args.steps:
+        windows.append((args.late_preroll, args.late_steps))
+    gp_runs = run_engine(w, gpb.GP_MODE_GROWPAGE, "growpage", windows, extras=True)
+    gp_res = gp_runs[0]
+    fk_runs = None if args.no_full_kv else run_engine(w, gpb.GP_MODE_FULL_KV, "full_kv", windows)
     # the review's ablation policies on the same kernels and workload; RANDOM
     # grows at GrowPage's measured grow frequency
     pol_res = {}
@@ -402,8 +476,21 @@ def run_ours(args, ws, rank, local):
                               ("inverse", gpb.GP_MODE_INVERSE, 0.0),
                               ("random", gpb.GP_MODE_RANDOM, rate),
                               ("shrink", gpb.GP_MODE_SHRINK, 0.0)):
-            pol_res[name] = measure(mode, name, rate=r)
+            pol_res[name] = run_engine(w, mode, name, windows[:1], rate=r)[0]
             pol_res[name]["rate"] = r
+    # the other workloads, each GrowPage against full KV on the same kernels
+    other = {}
+    if not args.no_workloads:
+        plan = {"llama8b_1layer": (args.preroll, args.steps),
+                "qwen3_8b_36layer_cb": (args.cb_preroll, args.cb_steps),
+                "stress_burst": (0, args.burst_steps)}
+        for name in [x for x in args.workloads.split(",") if x]:
+            wl = synth.WORKLOADS[name]
+            start, steps = plan.get(name, (args.preroll, args.steps))
+            other[name] = {"growpage": run_engine(wl, gpb.GP_MODE_GROWPAGE, "growpage",
+                                                  [(start, steps)])[0],
+                           "full_kv": run_engine(wl, gpb.GP_MODE_FULL_KV, "full_kv",
+                                                 [(start, steps)])[0]}
 
     # max over ranks of the time, sum of tokens
     t_ms, tokens = reduce_over_ranks(gp_res["step_ms"], gp_res["tokens"], dev)
@@ -455,73 +542,100 @@ def run_ours(args, ws, rank, local):
             "frac": round(gp_res["step_gbs"] / hbm_peak, 4),
             "frac_of_8tbs": round(gp_res["step_gbs"] / 8000.0, 4),
         },
-        "read_ceilings": gp_res["ceilings"],
+        "read_ceilings": gp_res.get("ceilings"),
         "gpu_launches": int(gp_res["launches"]),
         "clocks": gp_res["clocks"],
-        "growpage": {k: gp_res[k] for k in ("boundaries", "grows", "compacts", "denied", "moved",
-                                            "tokens", "req_steps", "free_pages")},
+        "growpage": summarize(gp_res, ws, hbm_peak),
     }
-    line["growpage"]["mean_resident_tokens"] = round(gp_res["dtok"] / max(1, gp_res["req_steps"]), 1)
-    if gp_res["e2e"]:
+    line["growpage"]["moved"] = int(gp_res["moved"])
+    if gp_res.get("e2e"):
         e = gp_res["e2e"]
         line["e2e"] = {"value": round(e["value"] * ws, 1), "unit": "tokens/s",
                        "h2d_bytes_per_step": int(e["h2d"]), "d2h_bytes_per_step": int(e["d2h"])}
-    if fk_res:
-        fv = fk_res["tokens"] / (fk_res["step_ms"] * 1e-3)
-        line["full_kv"] = {
-            "value": round(fv * ws, 1), "unit": "tokens/s",
-            "ms_per_step": round(fk_res["step_ms"] / args.steps, 4),
-            "attn_gbs": round(fk_res["attn_gbs"], 1),
-            "mean_resident_tokens": round(fk_res["dtok"] / max(1, fk_res["req_steps"]), 1),
-            "preempted": fk_res["preempted"], "tokens": fk_res["tokens"],
-        }
+    if fk_runs:
+        line["full_kv"] = summarize(fk_runs[0], ws, hbm_peak)
+        line["growpage_vs_full_kv"] = round(line["growpage"]["value"] / max(1e-9, line["full_kv"]["value"]), 4)
+    if len(gp_runs) > 1:
+        late = {"start_step": int(gp_runs[1]["start"]), "growpage": summarize(gp_runs[1], ws, hbm_peak)}
+        if fk_runs:
+            late["full_kv"] = summarize(fk_runs[1], ws, hbm_peak)
+            late["growpage_vs_full_kv"] = round(late["growpage"]["value"] /
+                                                max(1e-9, late["full_kv"]["value"]), 4)
+        line["late_window"] = late
     if pol_res:
         line["policies"] = {}
         for name, r in pol_res.items():
-            o = {"value": round(r["tokens"] / (r["step_ms"] * 1e-3) * ws, 1), "unit": "tokens/s",
-                 "ms_per_step": round(r["step_ms"] / args.steps, 4),
-                 "mean_resident_tokens": round(r["dtok"] / max(1, r["req_steps"]), 1)}
-            o.update({k: int(r[k]) for k in ("boundaries", "grows", "compacts", "shrinks")})
+            o = summarize(r, ws, hbm_peak)
             if name == "random":
                 o["random_grow_rate"] = round(r["rate"], 4)
             line["policies"][name] = o
+    if other:
+        line["workloads"] = {}
+        for name, rr in other.items():
+            wl = synth.WORKLOADS[name]
+            o = {"config": f"{wl.num_layers} layers, {wl.num_q_heads}q/{wl.num_kv_heads}kv, "
+                           f"d={wl.head_dim}, {wl.dtype}, batch {wl.batch}, page {wl.page_size}, "
+                           f"pool {rr['growpage']['num_pages']} pages, budget {wl.budget_pages} pages"
+                           + (f", prefix {wl.prefix_len} per {wl.prefix_group} requests, Poisson "
+                              f"{wl.arrival_rate}/s on {wl.step_seconds * 1000:.0f} ms steps, "
+                              f"{wl.total_requests} requests" if wl.prefix_len else ""),
+                 "window_start_step": int(rr["growpage"]["start"]),
+                 "growpage": summarize(rr["growpage"], ws, hbm_peak),
+                 "full_kv": summarize(rr["full_kv"], ws, hbm_peak)}
+            o["growpage_vs_full_kv"] = round(o["growpage"]["value"] / max(1e-9, o["full_kv"]["value"]), 4)
+            line["workloads"][name] = o
     return line
 
 
 # ------------------------------------------------------------ oracle arm
 
-def oracle_sample(w, seconds, max_steps=None):
-    """Time the CPU oracle on one request of the workload (all layers).
+class OracleRunner:
+    """The CPU oracle on one request of the workload (all layers), one thread.
 
     The request is admitted with a full initial budget (prompt = budget) so
-    that its first step is a boundary and every page-size-th step after it.
-    Returns (tokens/s, steps, seconds, threads).
+    that its first step is a boundary, and every page-size-th step after
+    it; `run` continues the same trajectory.
     """
-    import numpy as np
-    from demand_paged_kv_gqa_b300 import synth
-    from oracle.pool import OracleConfig, OraclePool
-    try:
-        from threadpoolctl import threadpool_limits
-        lim = threadpool_limits(1)
-    except Exception:
-        lim = None
-    torch.set_num_threads(1)
-    pl = w.budget_pages * w.page_size
-    st = synth.RequestStream(w, 0, 4096)
-    k, v = st.prompt(pl)
-    pool = OraclePool(OracleConfig.from_workload(w, num_pages=4 * w.budget_pages + 64))
-    pool.add_request(0, k.double().numpy(), v.double().numpy(), w.budget_pages)
-    steps = 0
-    t0 = time.time()
-    while True:
-        q, kk, vv = st.next_step()
-        pool.step([0], q[None].double().numpy(), kk[None].double().numpy(), vv[None].double().numpy())
-        steps += 1
-        el = time.time() - t0
-        if el >= seconds or (max_steps and steps >= max_steps):
-            break
-    del lim
-    return steps / el, steps, el, 1
+
+    def __init__(self, w):
+        from demand_paged_kv_gqa_b300 import synth
+        from oracle.pool import OracleConfig, OraclePool
+        try:
+            from threadpoolctl import threadpool_limits
+            self._lim = threadpool_limits(1)
+        except Exception:
+            self._lim = None
+        torch.set_num_threads(1)
+        self.w = w
+        pl = w.budget_pages * w.page_size
+        self.st = synth.RequestStream(w, 0, 1 << 20)
+        k, v = self.st.prompt(pl)
+        self.pool = OraclePool(OracleConfig.from_workload(w, num_pages=4 * w.budget_pages + 64,
+                                                          max_pages_per_req=4 * w.budget_pages))
+        self.pool.add_request(0, k.double().numpy(), v.double().numpy(), w.budget_pages)
+        self.steps = 0
+
+    def run(self, seconds, max_steps=None):
+        """Decode steps until `seconds` have passed (at least one); returns
+        (steps, seconds)."""
+        n, t0 = 0, time.time()
+        while True:
+            q, kk, vv = self.st.next_step()
+            self.pool.step([0], q[None].double().numpy(), kk[None].double().numpy(),
+                           vv[None].double().numpy())
+            n += 1
+            el = time.time() - t0
+            if el >= seconds or (max_steps and n >= max_steps):
+                break
+        self.steps += n
+        return n, el
+
+
+def oracle_sample(w, seconds, max_steps=None):
+    """Tokens/s of the oracle over one bounded run: (tokens/s, steps, s, threads)."""
+    r = OracleRunner(w)
+    n, el = r.run(seconds, max_steps)
+    return n / el, n, el, 1
 
 
 def run_reference(args, ws, rank):
@@ -529,18 +643,19 @@ def run_reference(args, ws, rank):
         return None
     w = workload_for(args)
     per_step = max(0.5, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
-    # warm-up then K timed samples, each a bounded run of the oracle
-    for _ in range(args.warmup):
-        oracle_sample(w, per_step / 4, max_steps=1)
-    tps, steps, secs = [], 0, 0.0
-    for _ in range(args.steps):
-        v, s, e, _ = oracle_sample(w, per_step, max_steps=4)
+    runner = OracleRunner(w)
+    for _ in range(args.warmup):          # warm-up: single decode steps, untimed
+        runner.run(0.0, max_steps=1)
+    steps, secs = 0, 0.0
+    for _ in range(args.steps):           # each timed step: a bounded slice of the trajectory
+        s, e = runner.run(per_step)
         steps += s
         secs += e
     value = steps / secs
     sample = (f"one request of {w.name} ({w.num_layers} layers, prompt = budget "
-              f"{w.budget_pages * w.page_size} tokens, boundary on its first step), "
-              f"{steps} oracle decode steps over {args.steps} samples")
+              f"{w.budget_pages * w.page_size} tokens, a boundary every {w.page_size} steps), "
+              f"one continuous trajectory: {args.warmup} warm-up steps, then {steps} oracle "
+              f"decode steps over {args.steps} samples")
     return {
         "impl": "reference",
         "metric": "decode tokens/s per B300 (GrowPage vs full-KV); % of HBM roofline",

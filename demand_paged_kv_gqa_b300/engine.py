@@ -9,13 +9,32 @@ slots, retires requests that reached their output length and refills their
 slots.  Every arithmetic step of the decode path runs in the library's
 kernels; this module only decides which slots take part.
 
+Arrivals.  A workload with an arrival rate draws Poisson arrival times on a
+virtual clock of ``step_seconds`` per decode step (``synth.poisson_arrivals``)
+and admits arrived requests first come, first served, up to its slot count
+and ``total_requests``.  Without a rate, a new request is always waiting.
+
+Shared prefixes.  A workload with ``prefix_len`` > 0 gives each group of
+``prefix_group`` consecutive requests one shared prefix (prefix caching):
+the first member to be admitted stores it (``gp_add_prefix``), every member
+references it, and the engine drops its creator reference once every member
+has been admitted, so the prefix's pages return to the pool when its last
+member leaves.  A preempted member re-admitted later re-creates it if needed.
+
+Boundaries.  Both outcomes of a boundary (grow, or compact within the
+allocation) leave P - 1 free private slots after the step's token is
+appended, so the host knows, without reading the device, how many steps
+each request has until its next boundary.  The engine counts the requests
+at a boundary in each step (``last_boundaries``).
+
 Full-KV mode (every boundary grows) cannot compact when the pool runs dry.
 There the engine preempts, as a PagedAttention server does by recomputation:
 before a step whose boundaries need more pages than are free, the most
 recently admitted requests release their pages and go back to the head of
 the queue; the tokens they had produced are subtracted from the count.
 In full-KV mode page use is a function of the step count alone, so the host
-tracks it exactly without reading the device.
+tracks it exactly without reading the device.  Its page cap per request is
+raised to hold the longest request, so that a request never starves at it.
 
 Inputs are drawn on the device by ``synth.BatchStream`` (the workload's
 recipe, batched); this module does not time anything itself but exposes
@@ -40,9 +59,18 @@ class Req:
     out_len: int
     produced: int = 0
     produced_timed: int = 0
-    n_pages: int = 0       # full-KV bookkeeping only
-    seq_priv: int = 0
-    prefix_id: int = -1
+    n_pages: int = 0       # private pages (full-KV bookkeeping)
+    seq_priv: int = 0      # private tokens (full-KV bookkeeping)
+    free_slots: int = 0    # private slots left: 0 = at a boundary at step start
+    group: int = -1        # shared-prefix group (-1: none)
+
+
+@dataclasses.dataclass
+class _Group:
+    pid: int = -1          # device prefix id, -1 while not stored
+    members: int = 0       # admitted members still holding it
+    held: bool = False     # the engine's creator reference
+    admitted: int = 0      # members admitted at least once
 
 
 class Engine:
@@ -55,18 +83,31 @@ class Engine:
         self.full_kv = mode == gpb.GP_MODE_FULL_KV
         self.device = torch.device(device)
         self.batch = batch or w.batch
+        self.P = w.page_size
+        max_out = max(w.decode_steps, w.out_max)
+        cap = None
+        if self.full_kv:
+            cap = max(w.max_pages_per_req, -(-(w.prompt_max + max_out) // self.P) + 1)
+        self.grp = w.prefix_group if w.prefix_len > 0 else 0
         self.cfg = gpb.config_for(w, mode=mode, max_requests=self.batch,
                                   num_pages=num_pages or w.num_pages, max_seq_len=max_seq_len,
-                                  random_grow_rate=random_grow_rate)
+                                  random_grow_rate=random_grow_rate, max_pages_per_req=cap,
+                                  max_prefixes=(self.batch + 2) if self.grp else None)
         self.pool = gpb.Pool(self.cfg, device=self.device)
         self.num_pages = self.cfg.num_pages
-        self.P = w.page_size
         self.seed_offset = seed_offset
         self.slots: List[Optional[Req]] = [None] * self.batch
         self.admit_order: List[int] = []          # slots, oldest first
         self.queue: collections.deque = collections.deque()
-        self.next_rid = seed_offset * 1_000_000
+        self.rid0 = seed_offset * 1_000_000
+        self.next_rid = self.rid0
+        self.total = w.total_requests or None
+        self.arrivals = (synth.poisson_arrivals(w, self.total or 1 << 16)
+                         if w.arrival_rate > 0 else None)
+        self.clock = 0                            # decode steps on the virtual clock
         self.lengths_cache: Dict[int, tuple] = {}
+        self.groups: Dict[int, _Group] = {}
+        self.prefix_pages = w.prefix_len // self.P
         self.gen = synth.BatchStream(w, self.batch, [1] * self.batch, device=self.device,
                                      seed=seed_offset)
         self.free_pages = self.num_pages          # full-KV: exact; else refreshed
@@ -75,6 +116,7 @@ class Engine:
         self.preempted = 0
         self.finished = 0
         self.steps = 0
+        self.last_boundaries = 0
         self._slots_dev = None
         self._active_key = None
         L, hq, hk, d = w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -90,37 +132,82 @@ class Engine:
             self.lengths_cache[rid] = synth.draw_lengths(self.w, 1, rid)[0]
         return self.lengths_cache[rid]
 
-    def _new_rid(self):
-        rid = self.next_rid
+    def _arrive(self):
+        """Queue the requests that have arrived by the current clock."""
+        if self.arrivals is None:
+            return                                # no clock: made on demand in fill()
+        while self.total is None or self.next_rid - self.rid0 < self.total:
+            if self.arrivals[self.next_rid - self.rid0] > self.clock:
+                return
+            self.queue.append(self.next_rid)
+            self.next_rid += 1
+
+    def _take_new(self) -> bool:
+        """Without an arrival clock a new request is always waiting."""
+        if self.arrivals is not None:
+            return False
+        if self.total is not None and self.next_rid - self.rid0 >= self.total:
+            return False
+        self.queue.append(self.next_rid)
         self.next_rid += 1
-        return rid
+        return True
 
     def _refresh_free(self):
         if not self.full_kv:
             self.free_pages = int(self.pool.stats().free_top)
 
+    def _group_of(self, rid):
+        return (rid - self.rid0) // self.grp if self.grp else -1
+
     def _admit(self, slot, rid) -> bool:
         w = self.w
         pl, T = self._lengths(rid)
         budget = max(w.budget_pages, -(-pl // self.P))
-        if self.free_pages < budget:
+        g = self._group_of(rid)
+        grp = self.groups.setdefault(g, _Group()) if g >= 0 else None
+        need = budget + (self.prefix_pages if grp is not None and grp.pid < 0 else 0)
+        if self.full_kv:
+            # keep one page per running request for its next grow, so that a
+            # request preempted for pages is not re-admitted straight away
+            need += len(self.admit_order)
+        if self.free_pages < need:
             return False
         st = synth.RequestStream(w, rid, T, device=self.device)
-        k, v = st.prompt(pl)
-        self.pool.add_request(slot, k.contiguous(), v.contiguous(), budget)
-        self.slots[slot] = Req(rid, pl, T, n_pages=budget, seq_priv=pl)
+        pid = -1
+        if grp is not None:
+            if grp.pid < 0:
+                pk, pv = synth.prefix_tensors(w, g, device=self.device)
+                grp.pid = self.pool.add_prefix(pk.contiguous(), pv.contiguous())
+                grp.held = True
+                self.free_pages -= self.prefix_pages
+            pid = grp.pid
+        if pl > 0:
+            k, v = st.prompt(pl)
+            self.pool.add_request(slot, k.contiguous(), v.contiguous(), budget, pid)
+        else:
+            self.pool.add_request(slot, None, None, budget, pid)
+        self.slots[slot] = Req(rid, pl, T, n_pages=budget, seq_priv=pl,
+                               free_slots=budget * self.P - pl, group=g)
         self.admit_order.append(slot)
         self.free_pages -= budget
         self.gen.reset_request(slot, T)
+        if grp is not None:
+            grp.members += 1
+            grp.admitted += 1
+            size = self.grp if self.total is None else min(self.grp, self.total - g * self.grp)
+            if grp.held and grp.admitted >= size:
+                self.pool.release_prefix(grp.pid)   # members keep it alive
+                grp.held = False
         return True
 
     def fill(self):
-        """Admit queued or new requests into every free slot that fits."""
+        """Admit arrived requests, first come first served, into free slots."""
+        self._arrive()
         for slot in range(self.batch):
             if self.slots[slot] is not None:
                 continue
-            if not self.queue:
-                self.queue.append(self._new_rid())
+            if not self.queue and not self._take_new():
+                break
             if not self._admit(slot, self.queue[0]):
                 break
             self.queue.popleft()
@@ -132,17 +219,27 @@ class Engine:
         self.admit_order.remove(slot)
         if self.full_kv:
             self.free_pages += r.n_pages
+        if r.group >= 0:
+            grp = self.groups[r.group]
+            grp.members -= 1
+            if grp.members == 0 and not grp.held:   # its last reference went
+                grp.pid = -1
+                if self.full_kv:
+                    self.free_pages += self.prefix_pages
         return r
 
     # ------------------------------------------------------------- stepping
     def active(self) -> List[int]:
         return [s for s in range(self.batch) if self.slots[s] is not None]
 
+    def at_boundary(self) -> List[int]:
+        """Active slots whose private pages are full at the next step's start."""
+        return [s for s in self.active() if self.slots[s].free_slots == 0]
+
     def _preempt_for_step(self):
         """Full-KV: free the newest requests until this step's grows fit."""
         while True:
-            need = sum(1 for s in self.active()
-                       if self.slots[s].seq_priv == self.slots[s].n_pages * self.P)
+            need = len(self.at_boundary())
             if need <= self.free_pages or not self.admit_order:
                 return
             slot = self.admit_order[-1]
@@ -166,16 +263,29 @@ class Engine:
             self._active_key = key
         return self._slots_dev
 
+    def drained(self) -> bool:
+        """No request active, queued or still to arrive."""
+        return (not self.active() and not self.queue and self.total is not None
+                and self.next_rid - self.rid0 >= self.total)
+
     def step(self, timed=False, before_step: Optional[Callable] = None,
              after_layer: Optional[Callable] = None, after_step: Optional[Callable] = None,
              before_layer: Optional[Callable] = None):
-        """One decode step for the active slots; returns the number of tokens."""
+        """One decode step for the active slots; returns the number of tokens.
+
+        The virtual clock advances by one step even when no request is active
+        (requests still to arrive)."""
         if self.full_kv:
             self._preempt_for_step()
         act = self.active()
         n = len(act)
+        self.clock += 1
         if n == 0:
+            self.last_boundaries = 0
+            self._refresh_free()
+            self.fill()
             return 0
+        self.last_boundaries = sum(1 for s in act if self.slots[s].free_slots == 0)
         slots_dev = self._slot_tensor(act)
         if n == self.batch:
             q, k, v = self.q, self.k, self.v
@@ -205,17 +315,24 @@ class Engine:
             r.produced += 1
             if timed:
                 r.produced_timed += 1
-            if self.full_kv:
-                if r.seq_priv == r.n_pages * self.P:
+            if r.free_slots == 0:                # a boundary: P - 1 slots left either way
+                r.free_slots = self.P - 1
+                if self.full_kv:
                     r.n_pages += 1
                     self.free_pages -= 1
-                r.seq_priv += 1
+            else:
+                r.free_slots -= 1
+            r.seq_priv += 1
             if r.produced >= r.out_len:
                 done.append(s)
         for s in done:
             self._release(s)
             self.finished += 1
-        if done or self.queue:
+        # admit when a slot was freed or a request arrived; a request waiting
+        # for pages is retried every P steps (pages move only at boundaries)
+        queued = len(self.queue)
+        self._arrive()
+        if done or len(self.queue) > queued or (queued and self.clock % self.P == 0):
             self._refresh_free()
             self.fill()
         return n

@@ -303,7 +303,8 @@ class Pool:
 
 
 def config_for(w, mode=GP_MODE_GROWPAGE, max_requests=None, num_pages=None,
-               max_seq_len=None, max_prefixes=None, random_grow_rate=0.0) -> gp_config:
+               max_seq_len=None, max_prefixes=None, random_grow_rate=0.0,
+               max_pages_per_req=None) -> gp_config:
     """gp_config for a synth.Workload."""
     max_out = max(w.decode_steps, w.out_max)
     seq = max_seq_len or (w.prefix_len + w.prompt_max + max_out + 16)
@@ -316,7 +317,7 @@ def config_for(w, mode=GP_MODE_GROWPAGE, max_requests=None, num_pages=None,
         num_layers=w.num_layers, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
         head_dim=w.head_dim, page_size=w.page_size,
         num_pages=num_pages or w.num_pages, max_requests=max_requests or w.batch,
-        max_pages_per_req=w.max_pages_per_req,
+        max_pages_per_req=max_pages_per_req or w.max_pages_per_req,
         dtype=GP_DTYPE_F32 if w.dtype == "f32" else GP_DTYPE_BF16, max_seq_len=seq,
         max_prefixes=max_prefixes, max_prefix_len=w.prefix_len, mode=mode,
         recent_window=w.recent_window, beta_s=w.beta_s, beta_l=w.beta_l, top_p=w.top_p,
