@@ -16,8 +16,11 @@
 //
 // How.  The G query heads and, at boundary steps, the two summaries form the
 // rows of one 16-row operand; each 16-token block of keys is the other
-// operand, so Q·K^T and P·V run as warp-level bf16 tensor-core products
-// (mma.sync m16n8k16, fp32 accumulation).  The contraction is a real dense
+// operand, so Q·K^T runs as warp-level bf16 tensor-core products (mma.sync
+// m16n8k16, fp32 accumulation).  The output is accumulated transposed,
+// O^T = V^T·P^T: the block's values are the 16-row operand (16 dims at a
+// time) and the softmax weights, hi and lo parts of the G heads, are the
+// 8 columns, taken straight from the score accumulators' layout.  The contraction is a real dense
 // one (G heads x d per key); the tensor pipe is used to cut the instruction
 // count per byte so that the kernel stays bound by HBM, not by issue.
 // Accuracy: bf16 operands hold fp32 values as exact-sum splits -- a query as
@@ -453,9 +456,13 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
                 const __nv_bfloat16* __restrict__ vnew, __nv_bfloat16* __restrict__ out) {
   static_assert(G == 1 || G == 2 || G == 4, "G");
   constexpr int D = kMmaD;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // The stages must start on 1024-byte boundaries (128-byte swizzle).  A
+  // CTA's dynamic shared memory starts 1024-byte aligned when, as here, the
+  // kernel declares no static shared memory; no slack is allocated for it
+  // (that keeps three CTAs per SM), and a misaligned base is reported below
+  // instead of run.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   uint8_t* ring = smem + (size_t)warp * S * kMmaStageB;
@@ -474,6 +481,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   // only what was final before this step's first attention launch (plan,
   // block tables, K/V pages).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_status(p, GP_ST_SMEM_ALIGN, (int)(smem_u32(smem_raw) & 1023u));
+    return;
+  }
   if (n <= 0 || w >= Weff) return;  // warp-uniform: warps never synchronise
   const int64_t start = p.wblk[w], end = p.wblk[w + 1];  // the plan's (weighted) share
   if (start >= end) return;
@@ -535,7 +546,12 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   // per-lane ldmatrix row offsets (within a stage): K (non-transposed) and V
   const int mi = lane >> 3, ri = lane & 7;
   const int k_tok = 8 * (mi >> 1) + ri, k_half = mi & 1;   // K: token, chunk parity
-  const int v_tok = 8 * (mi & 1) + ri, v_nt = mi >> 1;      // V: token, n-tile parity
+  // V^T as the 16 x 16 operand (rows: dims, columns: tokens), by transposing
+  // loads of V[token][dims]: matrices (tokens 0-7 | 8-15) x (dims +0 | +8)
+  const int v_tok = 8 * (mi >> 1) + ri, v_half = mi & 1;
+  // the lane whose softmax weights feed this lane's weight column: column
+  // n < G is head n (hi part), G <= n < 2G is head n - G (lo part)
+  const int p_src = ((g >= G && g < 2 * G) ? (g - G) : g) * 4 + t;
   const uint32_t ring_u32 = smem_u32(ring);
 
   bool failed = false;
@@ -593,9 +609,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     float* lgX = lgS + (g & 1) * p.logit_width;
 
     float m = -INFINITY, l = 0.f;
-    float o[16][4];
+    // O^T: o[mt][0..1] = dims 16mt + g, columns 2t, 2t+1; o[mt][2..3] = dims + 8
+    float o[8][4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     for (int64_t k = 0; k < len; ++k, ++j) {
       if (!wait_item(citems, slot)) { failed = true; break; }
@@ -637,15 +654,23 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       // the running max moves only when a score exceeds it by more than 2^8:
-      // weights stay <= 256, and the final normalisation uses the same m
-      if (mx > m + 8.0f) {
-        const float al = exp2f(m - mx);   // 0 when m == -inf
-        l *= al;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-          o[nt][0] *= al; o[nt][1] *= al; o[nt][2] *= al; o[nt][3] *= al;
+      // weights stay <= 256, and the final normalisation uses the same m.
+      // The accumulator columns of a head sit in other lanes, so the rescale
+      // is taken by the whole warp (rare: a few times per piece).
+      if (__any_sync(0xffffffffu, mx > m + 8.0f)) {
+        float al = 1.0f;
+        if (mx > m + 8.0f) {
+          al = exp2f(m - mx);             // 0 when m == -inf
+          l *= al;
+          m = mx;
         }
-        m = mx;
+        // column c holds head c mod G (columns >= 2G are zero)
+        const float a0 = __shfl_sync(0xffffffffu, al, ((2 * t) % G) * 4);
+        const float a1 = __shfl_sync(0xffffffffu, al, ((2 * t + 1) % G) * 4);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+        }
       }
       float pv[4];
 #pragma unroll
@@ -656,16 +681,20 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       uint32_t ph[4], pl[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) split2(pv[u], ph[u], pl[u]);
-      const uint32_t ap[4] = {pack2(ph[0], ph[1]), pack2(pl[0], pl[1]), pack2(ph[2], ph[3]),
-                              pack2(pl[2], pl[3])};
-      // ---- O += P · V
+      // P^T as the 16 x 8 operand: this lane's column g, tokens 2t, 2t+1 and
+      // 2t+8, 2t+9 -- hi parts for g < G, lo parts of head g - G for
+      // G <= g < 2G (fetched from that head's lane), zero beyond
+      const uint32_t xl0 = __shfl_sync(0xffffffffu, pack2(pl[0], pl[1]), p_src);
+      const uint32_t xl1 = __shfl_sync(0xffffffffu, pack2(pl[2], pl[3]), p_src);
+      const uint32_t bp0 = g < G ? pack2(ph[0], ph[1]) : (g < 2 * G ? xl0 : 0u);
+      const uint32_t bp1 = g < G ? pack2(ph[2], ph[3]) : (g < 2 * G ? xl1 : 0u);
+      // ---- O^T += V^T · P^T, 16 dims at a time
 #pragma unroll
-      for (int q2 = 0; q2 < 8; ++q2) {
-        const int ch = 2 * q2 + v_nt;     // 16-byte chunk = 8 output dims
-        uint32_t b[4];
-        ldsm_x4_t(b, sV + (ch >> 3) * 2048 + swz(v_tok, ch & 7));
-        mma_bf16(o[2 * q2], ap, b[0], b[1]);
-        mma_bf16(o[2 * q2 + 1], ap, b[2], b[3]);
+      for (int mt = 0; mt < 8; ++mt) {
+        const int ch = 2 * mt + v_half;   // 16-byte chunk = 8 dims
+        uint32_t a[4];
+        ldsm_x4_t(a, sV + (ch >> 3) * 2048 + swz(v_tok, ch & 7));
+        mma_bf16(o[mt], a, bp0, bp1);
       }
       release_item();
     }
@@ -674,13 +703,28 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     // ---- piece totals into the warp buffer: ob[g][dim], m[g], l[g]
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (head_row) {
+    {
+      // head h = column h (hi) + column G + h (lo): for G = 4 the lo columns
+      // sit two lanes up, for G = 2 one lane up, for G = 1 in the same lane
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        ob[g * D + 8 * nt + 2 * t] = o[nt][0] + o[nt][2];
-        ob[g * D + 8 * nt + 2 * t + 1] = o[nt][1] + o[nt][3];
+      for (int mt = 0; mt < 8; ++mt) {
+        float r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (G == 1) r[u] = o[mt][u & 2] + o[mt][(u & 2) + 1];
+          else r[u] = o[mt][u] + __shfl_xor_sync(0xffffffffu, o[mt][u], G == 4 ? 2 : 1);
+        }
+        const int d0 = 16 * mt + g;
+        if (G == 1) {
+          if (t == 0) { ob[d0] = r[0]; ob[d0 + 8] = r[2]; }
+        } else if (2 * t < G) {
+          ob[(2 * t) * D + d0] = r[0];
+          ob[(2 * t + 1) * D + d0] = r[1];
+          ob[(2 * t) * D + d0 + 8] = r[2];
+          ob[(2 * t + 1) * D + d0 + 8] = r[3];
+        }
       }
-      if (t == 0) {
+      if (head_row && t == 0) {
         ob[G * D + g] = m;
         ob[G * D + G + g] = l;
       }
@@ -812,7 +856,7 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
 
 size_t mma_smem_bytes() {
   return (size_t)kMmaWarps * kMmaStages * kMmaStageB + (size_t)kMmaWarps * kWarpBufFloats * 4 +
-         (size_t)kMmaWarps * kMmaStages * 8 + 1024;
+         (size_t)kMmaWarps * kMmaStages * 8;
 }
 
 // Both kernels are launched as programmatic dependents of the previous
