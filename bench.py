@@ -84,6 +84,8 @@ def parse():
                     help="continuous-batching workload: decode steps before its window "
                          "(arrivals fill the 128 slots by about step 1600)")
     ap.add_argument("--cb-steps", type=int, default=128)
+    ap.add_argument("--no-async", action="store_true",
+                    help="skip the asynchronous boundary measurement")
     ap.add_argument("--burst-steps", type=int, default=1024,
                     help="burst workload: timed steps from its first step (a burst every 16)")
     return ap.parse_args()
@@ -237,6 +239,10 @@ def time_window(eng, steps, w, sample_clocks=False, local=0):
     clk = ClockSampler(local) if sample_clocks else None
     if clk:
         clk.start()
+    # the whole window, input draws between steps included (compares the
+    # synchronous and asynchronous boundary paths on equal terms)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for _ in range(steps):
         eng.prepare_inputs()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -258,6 +264,9 @@ def time_window(eng, steps, w, sample_clocks=False, local=0):
             req_steps += n
             evs.append(e)
             nbs.append(eng.last_boundaries)
+    if eng.side is not None:
+        stream.wait_stream(eng.side)
+    w1.record(stream)
     torch.cuda.synchronize()
     clocks = clk.stop() if clk else None
     st1 = eng.pool.stats()
@@ -286,7 +295,8 @@ def time_window(eng, steps, w, sample_clocks=False, local=0):
                attn_bytes_per_launch=per_layer_bytes / nsteps,
                attn_gbs=(per_layer_bytes * n_attn / nsteps / (attn_ms * 1e-3) / 1e9) if attn_ms else 0.0,
                step_bytes=per_layer_bytes * L / nsteps,
-               step_gbs=per_layer_bytes * L / (step_ms * 1e-3) / 1e9 if step_ms else 0.0)
+               step_gbs=per_layer_bytes * L / (step_ms * 1e-3) / 1e9 if step_ms else 0.0,
+               window_ms=w0.elapsed_time(w1))
     # steps with boundaries against steps without (the boundary burst)
     bt = [(t, b) for t, b, nb in zip(step_t, bnd_t, nbs) if nb > 0]
     qt = [t for t, nb in zip(step_t, nbs) if nb == 0]
@@ -307,6 +317,7 @@ def summarize(r, ws, hbm_peak):
          "layer_call_frac": round(r["attn_gbs"] / hbm_peak, 4),
          "step_gbs": round(r["step_gbs"], 1),
          "mean_batch": round(r["req_steps"] / max(1, r["steps"]), 1),
+         "window_value": round(r["tokens"] / (r["window_ms"] * 1e-3) * ws, 1),
          "mean_resident_tokens": round(r["dtok"] / max(1, r["req_steps"]), 1)}
     o.update({k: int(r[k]) for k in ("steps", "tokens", "boundaries", "grows", "compacts",
                                      "denied", "starved", "shrinks", "preempted")})
@@ -330,10 +341,11 @@ def run_ours(args, ws, rank, local):
     w = workload_for(args)
     hbm_peak, peak_src = _load_peaks()
 
-    def run_engine(wl, mode, label, windows, rate=0.0, extras=False):
+    def run_engine(wl, mode, label, windows, rate=0.0, extras=False, async_boundary=False):
         """One engine; windows = [(decode steps before the window, timed steps)].
         The warm-up steps come right before the first window."""
-        eng = Engine(wl, mode=mode, device=dev, seed_offset=rank, random_grow_rate=rate)
+        eng = Engine(wl, mode=mode, device=dev, seed_offset=rank, random_grow_rate=rate,
+                     async_boundary=async_boundary)
         eng.fill()
         out = []
         for k, (start, steps) in enumerate(windows):
@@ -478,6 +490,12 @@ def run_ours(args, ws, rank, local):
                               ("shrink", gpb.GP_MODE_SHRINK, 0.0)):
             pol_res[name] = run_engine(w, mode, name, windows[:1], rate=r)[0]
             pol_res[name]["rate"] = r
+    # the boundary work on a second stream (gp_boundary_async), requests at a
+    # boundary sitting out one step: the default workload and the burst
+    async_res = {}
+    if not args.no_async:
+        async_res[w.name] = run_engine(w, gpb.GP_MODE_GROWPAGE, "async", windows[:1],
+                                       async_boundary=True)[0]
     # the other workloads, each GrowPage against full KV on the same kernels
     other = {}
     if not args.no_workloads:
@@ -491,6 +509,9 @@ def run_ours(args, ws, rank, local):
                                                   [(start, steps)])[0],
                            "full_kv": run_engine(wl, gpb.GP_MODE_FULL_KV, "full_kv",
                                                  [(start, steps)])[0]}
+            if name == "stress_burst" and not args.no_async:
+                async_res[name] = run_engine(wl, gpb.GP_MODE_GROWPAGE, "async", [(start, steps)],
+                                             async_boundary=True)[0]
 
     # max over ranks of the time, sum of tokens
     t_ms, tokens = reduce_over_ranks(gp_res["step_ms"], gp_res["tokens"], dev)
@@ -569,6 +590,15 @@ def run_ours(args, ws, rank, local):
             if name == "random":
                 o["random_grow_rate"] = round(r["rate"], 4)
             line["policies"][name] = o
+    if async_res:
+        line["async_boundary"] = {}
+        for name, r in async_res.items():
+            sync_r = gp_res if name == w.name else other[name]["growpage"]
+            o = {"growpage_async": summarize(r, ws, hbm_peak),
+                 "growpage_sync_window_value": summarize(sync_r, ws, hbm_peak)["window_value"]}
+            o["async_over_sync"] = round(o["growpage_async"]["window_value"] /
+                                         max(1e-9, o["growpage_sync_window_value"]), 4)
+            line["async_boundary"][name] = o
     if other:
         line["workloads"] = {}
         for name, rr in other.items():

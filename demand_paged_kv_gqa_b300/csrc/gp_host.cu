@@ -32,8 +32,9 @@ cudaError_t launch_kv_read(const PoolDev& p, const CUtensorMap* map, int layer, 
 cudaError_t launch_select(const PoolDev& p, int grid, int replan, cudaStream_t st);
 cudaError_t select_setup();
 cudaError_t select_occupancy(int* blocks);
-cudaError_t launch_decide(const PoolDev& p, cudaStream_t st);
-cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st);
+cudaError_t launch_decide(const PoolDev& p, int part, cudaStream_t st);
+cudaError_t launch_commit(const PoolDev& p, int grid, int part, cudaStream_t st);
+cudaError_t launch_release_busy(const PoolDev& p, cudaStream_t st);
 cudaError_t launch_init(const PoolDev& p, cudaStream_t st);
 cudaError_t launch_pop_pages(const PoolDev& p, int32_t* dst, int count, cudaStream_t st);
 cudaError_t launch_prefix_meta(const PoolDev& p, int pid, int npages, int len, cudaStream_t st);
@@ -64,6 +65,16 @@ struct gp_pool {
   std::vector<int> prefix_refs;  // host mirror of the device reference counts
   std::vector<char> prefix_held;
   std::vector<int> prefix_len;
+  // Plan buffers: steps alternate between two, so that a step's boundary
+  // work on a second stream (gp_boundary_async) can still read its own plan
+  // while the next step runs.  plan_set[b][k] / delta_set[b] are buffer b's
+  // eleven plan arrays and Delta accumulators; `parity` is the current one.
+  int32_t* plan_set[2][11] = {};
+  long long* delta_set[2] = {};
+  int parity = 0;
+  cudaEvent_t side_ev[2] = {nullptr, nullptr};  // boundary work of a buffer's step done
+  bool side_pending[2] = {false, false};
+  cudaEvent_t main_ev = nullptr;                // the plain part of a boundary done
 };
 
 // Work of starting a (request, head) segment in the bf16 attention kernel
@@ -145,8 +156,10 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   l->prefix_pages = take((uint64_t)c->max_prefixes * l->max_prefix_pages * 4);
   l->rope = take((uint64_t)c->max_seq_len * (D / 2) * (8 + 8 + 4 + 4));
   l->scratch = off;
-  for (int k = 0; k < 11; ++k) take((R + 1) * 4);             // plan arrays
-  take(R * 8);                                                 // plan_delta
+  for (int b = 0; b < 2; ++b) {                                // two plan buffers
+    for (int k = 0; k < 11; ++k) take((R + 1) * 4);           //   plan arrays
+    take(R * 8);                                               //   plan_delta
+  }
   take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 4) * 4);  // partials
   take(R * Hk * 4);                                            // seg_count
   take((uint64_t)gp::kMaxWorkersBound * 16);                   // wstart
@@ -156,6 +169,7 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   take(R * Hk * 4 * 4);                                        // sstage
   take(R * L * Hk * P * 4 * 4);                                // moves (up to 2P pairs)
   take(R * L * Hk * 4);                                        // moves_n
+  take(R * 4);                                                 // busy
   l->total = off;
 }
 
@@ -199,18 +213,10 @@ void fill_dev(gp_pool* p) {
   const uint64_t R = c.max_requests;
   uint64_t off = l.scratch;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = align_up(off + bytes); return b + o; };
-  d.plan_slot = (int32_t*)take((R + 1) * 4);
-  d.plan_R = (int32_t*)take((R + 1) * 4);
-  d.plan_nb = (int32_t*)take((R + 1) * 4);
-  d.plan_cum = (int32_t*)take((R + 1) * 4);
-  d.plan_flags = (int32_t*)take((R + 1) * 4);
-  d.plan_commit = (int32_t*)take((R + 1) * 4);
-  d.plan_cpos = (int32_t*)take((R + 1) * 4);
-  d.plan_dec = (int32_t*)take((R + 1) * 4);
-  d.plan_bnd = (int32_t*)take((R + 1) * 4);
-  d.plan_misc = (int32_t*)take((R + 1) * 4);
-  d.plan_pos = (int32_t*)take((R + 1) * 4);
-  d.plan_delta = (long long*)take(R * 8);
+  for (int b = 0; b < 2; ++b) {
+    for (int k = 0; k < 11; ++k) p->plan_set[b][k] = (int32_t*)take((R + 1) * 4);
+    p->delta_set[b] = (long long*)take(R * 8);
+  }
   d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 4) * 4);
   d.seg_count = (int32_t*)take(R * c.num_kv_heads * 4);
   d.wstart = (int4*)take((uint64_t)gp::kMaxWorkersBound * 16);
@@ -220,6 +226,30 @@ void fill_dev(gp_pool* p) {
   d.sstage = (float*)take(R * c.num_kv_heads * 4 * 4);
   d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 4 * 4);
   d.moves_n = (int32_t*)take(R * c.num_layers * c.num_kv_heads * 4);
+  d.busy = (int32_t*)take(R * 4);
+}
+
+// Point the device view at plan buffer b.
+void use_plan(gp_pool* p, int b) {
+  gp::PoolDev& d = p->dev;
+  int32_t** arrays[11] = {&d.plan_slot, &d.plan_R,      &d.plan_nb,   &d.plan_cum,
+                          &d.plan_flags, &d.plan_commit, &d.plan_cpos, &d.plan_dec,
+                          &d.plan_bnd,  &d.plan_misc,   &d.plan_pos};
+  for (int k = 0; k < 11; ++k) *arrays[k] = p->plan_set[b][k];
+  d.plan_delta = p->delta_set[b];
+  p->parity = b;
+}
+
+// Make the pool's stream wait for every boundary work still pending on a
+// second stream (device-side wait, no host sync).
+cudaError_t join_side(gp_pool* p) {
+  for (int b = 0; b < 2; ++b) {
+    if (!p->side_pending[b]) continue;
+    cudaError_t e = cudaStreamWaitEvent(p->stream, p->side_ev[b], 0);
+    if (e != cudaSuccess) return e;
+    p->side_pending[b] = false;
+  }
+  return cudaSuccess;
 }
 
 int sync_status(gp_pool* p) {
@@ -230,13 +260,14 @@ int sync_status(gp_pool* p) {
   if (e != cudaSuccess) return cuda_fail(p, e, "read status");
   if (st[0]) {
     char buf[200];
-    std::snprintf(buf, sizeof(buf), "device status 0x%x (info %d):%s%s%s%s%s%s", st[0], (int)st[1],
+    std::snprintf(buf, sizeof(buf), "device status 0x%x (info %d):%s%s%s%s%s%s%s", st[0], (int)st[1],
                   (st[0] & GP_ST_BAD_SLOTS) ? " bad-slot-list" : "",
                   (st[0] & GP_ST_BAD_PAGE) ? " page-out-of-range" : "",
                   (st[0] & GP_ST_TIMEOUT) ? " wait-timeout" : "",
                   (st[0] & GP_ST_STARVED) ? " full-kv-starved" : "",
                   (st[0] & GP_ST_BAD_PLAN) ? " bad-plan" : "",
-                  (st[0] & GP_ST_POS_RANGE) ? " position-beyond-max_seq_len" : "");
+                  (st[0] & GP_ST_POS_RANGE) ? " position-beyond-max_seq_len" : "",
+                  (st[0] & GP_ST_SMEM_ALIGN) ? " shared-memory-misaligned" : "");
     return fail(p, GP_ERR_DEVICE, buf);
   }
   return GP_OK;
@@ -248,6 +279,12 @@ int read_free_top(gp_pool* p, int* out) {
   if (e != cudaSuccess) return cuda_fail(p, e, "read free_top");
   return GP_OK;
 }
+
+#define GP_JOIN(pool)                                                        \
+  do {                                                                       \
+    cudaError_t _e = join_side(pool);                                        \
+    if (_e != cudaSuccess) return cuda_fail(pool, _e, "wait for second stream"); \
+  } while (0)
 
 #define GP_LAUNCH(pool, expr)                                   \
   do {                                                          \
@@ -287,6 +324,7 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   p->prefix_held.assign(cfg->max_prefixes, 0);
   p->prefix_len.assign(cfg->max_prefixes, 0);
   fill_dev(p);
+  use_plan(p, 0);
   auto bail = [&](int code) { delete p; return code; };
   cudaError_t e = cudaMemsetAsync(dev_buf, 0, l.total, p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
@@ -360,18 +398,30 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   p->commit_grid = sms * 4;
   e = cudaStreamSynchronize(p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b)
+    e = cudaEventCreateWithFlags(&p->side_ev[b], cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->main_ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    for (int b = 0; b < 2; ++b)
+      if (p->side_ev[b]) cudaEventDestroy(p->side_ev[b]);
+    return bail(GP_ERR_CUDA);
+  }
   *out = p;
   return GP_OK;
 }
 
 int gp_destroy_pool(gp_pool* pool) {
   if (!pool) return GP_ERR_INVALID;
+  for (int b = 0; b < 2; ++b)
+    if (pool->side_ev[b]) cudaEventDestroy(pool->side_ev[b]);
+  if (pool->main_ev) cudaEventDestroy(pool->main_ev);
   delete pool;
   return GP_OK;
 }
 
 int gp_set_stream(gp_pool* pool, void* stream) {
   if (!pool) return GP_ERR_INVALID;
+  GP_JOIN(pool);
   pool->stream = (cudaStream_t)stream;
   return GP_OK;
 }
@@ -391,6 +441,7 @@ int gp_add_prefix(gp_pool* pool, const void* k_prefix, const void* v_prefix, int
   if (len <= 0 || len % c.page_size || len > c.max_prefix_len || !k_prefix || !v_prefix)
     return fail(pool, GP_ERR_INVALID, "prefix length must be a positive multiple of page_size <= max_prefix_len");
   if (len >= c.max_seq_len) return fail(pool, GP_ERR_INVALID, "prefix beyond max_seq_len");
+  GP_JOIN(pool);
   int pid = -1;
   for (int k = 0; k < c.max_prefixes; ++k)
     if (pool->prefix_refs[k] == 0) { pid = k; break; }
@@ -417,6 +468,7 @@ int gp_release_prefix(gp_pool* pool, int32_t prefix_id) {
   if (!pool) return GP_ERR_INVALID;
   if (prefix_id < 0 || prefix_id >= pool->cfg.max_prefixes || !pool->prefix_held[prefix_id])
     return fail(pool, GP_ERR_INVALID, "prefix not held");
+  GP_JOIN(pool);
   GP_LAUNCH(pool, gp::launch_release_prefix(pool->dev, prefix_id, pool->stream));
   pool->prefix_held[prefix_id] = 0;
   pool->prefix_refs[prefix_id] -= 1;
@@ -445,6 +497,7 @@ int gp_add_request(gp_pool* pool, int32_t slot, const void* k_prompt, const void
   }
   if ((long long)plen + prompt_len >= c.max_seq_len)
     return fail(pool, GP_ERR_INVALID, "position beyond max_seq_len");
+  GP_JOIN(pool);
   int free_top = 0;
   int rc = read_free_top(pool, &free_top);
   if (rc) return rc;
@@ -475,6 +528,15 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
   if (((uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)out) % 16)
     return fail(pool, GP_ERR_INVALID, "q, k_new, v_new and out must be 16-byte aligned");
   if (layer == 0) {
+    // steps alternate between the two plan buffers; this one was last used
+    // two steps ago, whose boundary work may still run on a second stream
+    const int b = pool->parity ^ 1;
+    if (pool->side_pending[b]) {
+      cudaError_t e = cudaStreamWaitEvent(pool->stream, pool->side_ev[b], 0);
+      if (e != cudaSuccess) return cuda_fail(pool, e, "wait for second stream");
+      pool->side_pending[b] = false;
+    }
+    use_plan(pool, b);
     GP_LAUNCH(pool, gp::launch_plan(pool->dev, n, slots_dev, 1, pool->stream));
     pool->step_n = n;
     pool->step_slots = slots_dev;
@@ -503,14 +565,51 @@ int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev) {
     return fail(pool, GP_ERR_INVALID, "gp_boundary must get the step's slot list");
   pool->next_layer = 0;
   if (n == 0) return GP_OK;
+  GP_JOIN(pool);  // pages are popped below: after any earlier step's boundary work
   if (pool->cfg.mode != GP_MODE_FULL_KV)
     GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 0, pool->stream));
-  GP_LAUNCH(pool, gp::launch_decide(pool->dev, pool->stream));
+  GP_LAUNCH(pool, gp::launch_decide(pool->dev, gp::kPartAll, pool->stream));
   // SHRINK: the requests that release a page drop 2P tokens, not P; their
   // plans are redone once the decisions are known
   if (pool->cfg.mode == GP_MODE_SHRINK)
     GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 1, pool->stream));
-  GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, pool->stream));
+  GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, gp::kPartAll, pool->stream));
+  return GP_OK;
+}
+
+int gp_boundary_async(gp_pool* pool, int32_t n, const int32_t* slots_dev, void* side_stream) {
+  if (!pool) return GP_ERR_INVALID;
+  if (pool->next_layer != pool->cfg.num_layers)
+    return fail(pool, GP_ERR_INVALID, "gp_boundary_async before all layers of the step");
+  if (n != pool->step_n || slots_dev != pool->step_slots)
+    return fail(pool, GP_ERR_INVALID, "gp_boundary_async must get the step's slot list");
+  cudaStream_t side = (cudaStream_t)side_stream;
+  if (!side || side == pool->stream)
+    return fail(pool, GP_ERR_INVALID, "gp_boundary_async needs a second stream");
+  pool->next_layer = 0;
+  if (n == 0) return GP_OK;
+  const int b = pool->parity;
+  cudaError_t e;
+  // the requests not at a boundary: decision-free bookkeeping and their
+  // token appended, on the pool's stream; those at a boundary are marked busy
+  GP_LAUNCH(pool, gp::launch_decide(pool->dev, gp::kPartPlain, pool->stream));
+  GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, gp::kPartPlain, pool->stream));
+  e = cudaEventRecord(pool->main_ev, pool->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(side, pool->main_ev, 0);
+  // one step's boundary work after the previous one's (page pops in step order)
+  if (e == cudaSuccess && pool->side_pending[b ^ 1]) e = cudaStreamWaitEvent(side, pool->side_ev[b ^ 1], 0);
+  if (e != cudaSuccess) return cuda_fail(pool, e, "order the second stream");
+  // the requests at a boundary, on the second stream
+  if (pool->cfg.mode != GP_MODE_FULL_KV)
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 0, side));
+  GP_LAUNCH(pool, gp::launch_decide(pool->dev, gp::kPartBoundary, side));
+  if (pool->cfg.mode == GP_MODE_SHRINK)
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 1, side));
+  GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, gp::kPartBoundary, side));
+  GP_LAUNCH(pool, gp::launch_release_busy(pool->dev, side));
+  e = cudaEventRecord(pool->side_ev[b], side);
+  if (e != cudaSuccess) return cuda_fail(pool, e, "record second stream");
+  pool->side_pending[b] = true;
   return GP_OK;
 }
 
@@ -519,6 +618,7 @@ int gp_free(gp_pool* pool, int32_t slot) {
   if (pool->next_layer != 0) return fail(pool, GP_ERR_INVALID, "free inside a step");
   if (slot < 0 || slot >= pool->cfg.max_requests || !pool->slot_active[slot])
     return fail(pool, GP_ERR_INVALID, "slot not active");
+  GP_JOIN(pool);
   GP_LAUNCH(pool, gp::launch_free(pool->dev, slot, pool->stream));
   pool->slot_active[slot] = 0;
   const int pid = pool->slot_prefix[slot];
@@ -535,6 +635,7 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
   if (layer0 < 0 || count < 1 || layer0 + count > pool->cfg.num_layers || mode < 0 || mode > 2 ||
       n < 0 || n > pool->cfg.max_requests || !sink_dev || (n > 0 && !slots_dev))
     return fail(pool, GP_ERR_INVALID, "bad read-ceiling arguments");
+  GP_JOIN(pool);
   GP_LAUNCH(pool, gp::launch_plan(pool->dev, n, slots_dev, 0, pool->stream));
   const int wpc = gp::ceiling_warps_per_cta();
   const int grid = (pool->dev.num_workers + wpc - 1) / wpc;
@@ -625,11 +726,13 @@ int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int3
 
 int gp_sync(gp_pool* pool) {
   if (!pool) return GP_ERR_INVALID;
+  GP_JOIN(pool);
   return sync_status(pool);
 }
 
 int gp_clear_status(gp_pool* pool, uint32_t* status_out, int32_t* info_out) {
   if (!pool) return GP_ERR_INVALID;
+  GP_JOIN(pool);
   cudaError_t e = cudaStreamSynchronize(pool->stream);
   uint32_t st[2] = {0u, 0u};  // status, status_info (adjacent in gp_ctrl)
   if (e == cudaSuccess) e = cudaMemcpy(st, &pool->dev.ctrl->status, 8, cudaMemcpyDeviceToHost);
@@ -644,6 +747,7 @@ int gp_clear_status(gp_pool* pool, uint32_t* status_out, int32_t* info_out) {
 
 int gp_get_stats(gp_pool* pool, gp_ctrl* out) {
   if (!pool || !out) return GP_ERR_INVALID;
+  GP_JOIN(pool);
   cudaError_t e = cudaStreamSynchronize(pool->stream);
   if (e == cudaSuccess) e = cudaMemcpy(out, pool->dev.ctrl, sizeof(gp_ctrl), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(pool, e, "gp_get_stats");
@@ -653,6 +757,7 @@ int gp_get_stats(gp_pool* pool, gp_ctrl* out) {
 int gp_get_request(gp_pool* pool, int32_t slot, gp_req_meta* meta, int32_t* block_table, int32_t cap) {
   if (!pool || !meta || slot < 0 || slot >= pool->cfg.max_requests || cap < 0)
     return GP_ERR_INVALID;
+  GP_JOIN(pool);
   cudaError_t e = cudaStreamSynchronize(pool->stream);
   if (e == cudaSuccess)
     e = cudaMemcpy(meta, pool->dev.req + slot, sizeof(gp_req_meta), cudaMemcpyDeviceToHost);
@@ -670,6 +775,7 @@ int gp_get_state(gp_pool* pool, gp_state_view* out) {
   const gp_config& c = pool->cfg;
   const gp::PoolDev& d = pool->dev;
   const size_t R = (size_t)c.max_requests;
+  GP_JOIN(pool);
   cudaError_t e = cudaStreamSynchronize(pool->stream);
   auto copy = [&](void* dst, const void* src, size_t bytes) {
     if (e == cudaSuccess && dst) e = cudaMemcpy(dst, src, bytes, cudaMemcpyDeviceToHost);

@@ -87,7 +87,16 @@ struct PoolDev {
   // scratch: compaction moves
   int32_t* moves;         // [max_req][L][Hk][P][2] (dst, src) private slots
   int32_t* moves_n;       // [max_req][L][Hk]
+  // asynchronous boundary work: 1 while a request's boundary work of an
+  // earlier step still runs on the second stream (the plan refuses it)
+  int32_t* busy;          // [max_req]
 };
+
+// Which requests a boundary-phase kernel (decide, commit) handles: every
+// request of the step, only those not at a boundary (their token appended on
+// the pool's stream), or only those at a boundary (their boundary work on the
+// second stream).
+enum Part : int32_t { kPartAll = 0, kPartPlain = 1, kPartBoundary = 2 };
 
 // ------------------------------------------------------------ helpers ---
 

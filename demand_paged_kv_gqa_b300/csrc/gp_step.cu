@@ -17,6 +17,9 @@
 //   commit_kernel   per (request, layer, kv head): the step's folded
 //                   summaries made current, compaction moves, then the
 //                   staged token written into its slot.
+// For the asynchronous boundary path, decide and commit run twice: once on
+// the pool's stream for the requests not at a boundary, once on a second
+// stream for those at a boundary (which sit out the next step).
 //
 // Method: "GrowPage: On-Demand KV Budgeting for Efficient LLM Reasoning
 // Serving" -- abstract (capacity boundaries; compress within the current
@@ -88,6 +91,11 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
     if (i < n) {
       const int slot = slots[i];
       bool ok = (unsigned)slot < (unsigned)p.max_req;
+      if (ok) {  // boundary work still running on the second stream: refused
+        int b;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(b) : "l"(p.busy + slot) : "memory");
+        ok = b == 0;
+      }
       if (ok) ok = p.req[slot].active != 0;
       if (ok && i > 0) ok = slots[i - 1] < slot;
       if (ok && p.req[slot].pos >= p.max_seq_len) {
@@ -670,7 +678,7 @@ __device__ __forceinline__ uint64_t splitmix64(uint64_t x) {
   return z ^ (z >> 31);
 }
 
-__global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
+__global__ void __launch_bounds__(1024) decide_kernel(PoolDev p, int part) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ int s_warp[33];
@@ -686,10 +694,15 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
     const int i = base + threadIdx.x;
     int wg = 0, want = 0, at_b = 0, slot = 0;
     gp_req_meta m;
+    bool mine = false;
     if (i < n) {
       slot = p.plan_slot[i];
-      m = p.req[slot];
       at_b = (p.plan_flags[i] & kPlanBoundary) != 0;
+      mine = part == kPartAll || (part == kPartBoundary) == (at_b != 0);
+      if (part == kPartPlain && at_b) p.busy[slot] = 1;  // its work goes to the second stream
+    }
+    if (mine) {
+      m = p.req[slot];
       if (at_b) {
         const double delta = (double)p.plan_delta[i];
         switch (p.mode) {
@@ -708,7 +721,7 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
     }
     int total;
     const int rank = block_excl_scan(wg, s_warp, &total);
-    if (i < n) {
+    if (mine) {
       const int C = m.n_pages * p.P;
       int dec, commit;
       if (wg && rank < avail) {
@@ -758,7 +771,7 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
       p.req[slot] = m;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && part != kPartPlain) {  // the plain part never pops
       const int g = total < avail ? total : avail;
       atomicSub(&p.ctrl->free_top, g);
     }
@@ -767,7 +780,7 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
   // Pages released by SHRINK go on the free stack after every pop of the
   // step, in ascending slot order: a page released now is not handed out
   // before the next step (its tokens are still read by the commit's moves).
-  if (p.mode == GP_MODE_SHRINK) {
+  if (p.mode == GP_MODE_SHRINK && part != kPartPlain) {
     for (int base = 0; base < n; base += blockDim.x) {
       if (threadIdx.x == 0) s_avail = p.ctrl->free_top;
       __syncthreads();
@@ -788,14 +801,27 @@ __global__ void __launch_bounds__(1024) decide_kernel(PoolDev p) {
       __syncthreads();
     }
   }
-  if (threadIdx.x == 0) {
-    p.ctrl->boundaries += (long long)s_cnt[0];
-    p.ctrl->grows += (long long)s_cnt[1];
-    p.ctrl->compacts += (long long)s_cnt[2];
-    p.ctrl->denied += (long long)s_cnt[3];
-    p.ctrl->starved += (long long)s_cnt[4];
-    p.ctrl->shrinks += (long long)s_cnt[5];
+  if (threadIdx.x == 0 && part != kPartPlain) {  // the two parts may run concurrently
+    atomicAdd((unsigned long long*)&p.ctrl->boundaries, s_cnt[0]);
+    atomicAdd((unsigned long long*)&p.ctrl->grows, s_cnt[1]);
+    atomicAdd((unsigned long long*)&p.ctrl->compacts, s_cnt[2]);
+    atomicAdd((unsigned long long*)&p.ctrl->denied, s_cnt[3]);
+    atomicAdd((unsigned long long*)&p.ctrl->starved, s_cnt[4]);
+    atomicAdd((unsigned long long*)&p.ctrl->shrinks, s_cnt[5]);
   }
+}
+
+// End of a step's boundary work on the second stream: its requests may take
+// part in steps again.  Runs after the commit kernel has completed, so the
+// release makes every write of the boundary work visible to a plan kernel
+// that reads the flag with acquire.
+__global__ void release_busy_kernel(PoolDev p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int n = p.plan_misc[0];
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    if (p.plan_flags[i] & kPlanBoundary)
+      asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p.busy + p.plan_slot[i]), "r"(0)
+                   : "memory");
 }
 
 // -------------------------------------------------------------- commit ---
@@ -812,7 +838,7 @@ __device__ __forceinline__ uint8_t* slot_row(const PoolDev& p, const int32_t* bt
          (size_t)h * p.head_bytes + (size_t)(s % p.P) * rowb;
 }
 
-__global__ void __launch_bounds__(256) commit_kernel(PoolDev p) {
+__global__ void __launch_bounds__(256) commit_kernel(PoolDev p, int part) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int n = p.plan_misc[0];
@@ -826,6 +852,9 @@ __global__ void __launch_bounds__(256) commit_kernel(PoolDev p) {
     const int i = item / (p.L * p.Hk);
     const int rem = item % (p.L * p.Hk);
     const int layer = rem / p.Hk, h = rem % p.Hk;
+    if (part != kPartAll &&
+        (part == kPartBoundary) != ((p.plan_flags[i] & kPlanBoundary) != 0))
+      continue;
     const int slot = p.plan_slot[i];
     const int dec = p.plan_dec[i];
     const int commit = p.plan_commit[i];
@@ -1047,11 +1076,14 @@ cudaError_t select_occupancy(int* blocks) {
 cudaError_t launch_select(const PoolDev& p, int grid, int replan, cudaStream_t st) {
   return launch_pdl(select_kernel, grid, kSelThreads, kSelSmemBytes, st, p, replan);
 }
-cudaError_t launch_decide(const PoolDev& p, cudaStream_t st) {
-  return launch_pdl(decide_kernel, 1, 1024, 0, st, p);
+cudaError_t launch_decide(const PoolDev& p, int part, cudaStream_t st) {
+  return launch_pdl(decide_kernel, 1, 1024, 0, st, p, part);
 }
-cudaError_t launch_commit(const PoolDev& p, int grid, cudaStream_t st) {
-  return launch_pdl(commit_kernel, grid, 256, 0, st, p);
+cudaError_t launch_commit(const PoolDev& p, int grid, int part, cudaStream_t st) {
+  return launch_pdl(commit_kernel, grid, 256, 0, st, p, part);
+}
+cudaError_t launch_release_busy(const PoolDev& p, cudaStream_t st) {
+  return launch_pdl(release_busy_kernel, 1, 256, 0, st, p);
 }
 cudaError_t launch_init(const PoolDev& p, cudaStream_t st) {
   init_kernel<<<256, 256, 0, st>>>(p);

@@ -77,7 +77,7 @@ class Engine:
     def __init__(self, w: synth.Workload, mode=gpb.GP_MODE_GROWPAGE, device="cuda",
                  num_pages: Optional[int] = None, batch: Optional[int] = None,
                  seed_offset: int = 0, max_seq_len: Optional[int] = None,
-                 random_grow_rate: float = 0.0):
+                 random_grow_rate: float = 0.0, async_boundary: bool = False):
         self.w = w
         self.mode = mode
         self.full_kv = mode == gpb.GP_MODE_FULL_KV
@@ -117,6 +117,10 @@ class Engine:
         self.finished = 0
         self.steps = 0
         self.last_boundaries = 0
+        # asynchronous boundary work: the requests at a boundary in a step get
+        # their boundary work on a second stream and sit out the next step
+        self.side = torch.cuda.Stream(device=self.device) if async_boundary else None
+        self.out_of_step = set()
         self._slots_dev = None
         self._active_key = None
         L, hq, hk, d = w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -217,6 +221,7 @@ class Engine:
         self.pool.free(slot)
         self.slots[slot] = None
         self.admit_order.remove(slot)
+        self.out_of_step.discard(slot)
         if self.full_kv:
             self.free_pages += r.n_pages
         if r.group >= 0:
@@ -232,9 +237,13 @@ class Engine:
     def active(self) -> List[int]:
         return [s for s in range(self.batch) if self.slots[s] is not None]
 
+    def stepping(self) -> List[int]:
+        """Active slots that take part in the next step."""
+        return [s for s in self.active() if s not in self.out_of_step]
+
     def at_boundary(self) -> List[int]:
-        """Active slots whose private pages are full at the next step's start."""
-        return [s for s in self.active() if self.slots[s].free_slots == 0]
+        """Slots of the next step whose private pages are full at its start."""
+        return [s for s in self.stepping() if self.slots[s].free_slots == 0]
 
     def _preempt_for_step(self):
         """Full-KV: free the newest requests until this step's grows fit."""
@@ -277,11 +286,19 @@ class Engine:
         (requests still to arrive)."""
         if self.full_kv:
             self._preempt_for_step()
-        act = self.active()
+        act = self.stepping()
         n = len(act)
         self.clock += 1
         if n == 0:
+            if self.side is not None and self.out_of_step:
+                # the library counts steps by calls: a step with no request
+                # still separates the boundary work from the requests' return
+                empty = torch.zeros(0, dtype=torch.int32, device=self.device)
+                for l in range(self.w.num_layers):
+                    self.pool.decode_step(l, empty, None, None, None, None)
+                self.pool.boundary_async(empty, self.side)
             self.last_boundaries = 0
+            self.out_of_step = set()
             self._refresh_free()
             self.fill()
             return 0
@@ -301,9 +318,14 @@ class Engine:
             self.pool.decode_step(l, slots_dev, q[l], k[l], v[l], self.out[l, :n])
             if after_layer:
                 after_layer(l)
-        self.pool.boundary(slots_dev)
+        if self.side is not None:
+            self.pool.boundary_async(slots_dev, self.side)
+        else:
+            self.pool.boundary(slots_dev)
         if after_step:
             after_step()
+        if self.side is not None:
+            self.out_of_step = {s for s in act if self.slots[s].free_slots == 0}
         # host bookkeeping
         self.steps += 1
         self.tokens += n

@@ -86,6 +86,7 @@ def _load():
         "gp_add_request": (ctypes.c_int, [P, I32, P, P, I32, I32, I32]),
         "gp_decode_step": (ctypes.c_int, [P, I32, I32, P, P, P, P, P]),
         "gp_boundary": (ctypes.c_int, [P, I32, P]),
+        "gp_boundary_async": (ctypes.c_int, [P, I32, P, P]),
         "gp_free": (ctypes.c_int, [P, I32]),
         "gp_sync": (ctypes.c_int, [P]),
         "gp_clear_status": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32),
@@ -206,6 +207,12 @@ class Pool:
 
     def boundary(self, slots: torch.Tensor):
         self._check(lib.gp_boundary(self.h, slots.numel(), _ptr(slots)))
+
+    def boundary_async(self, slots: torch.Tensor, side: torch.cuda.Stream):
+        """gp_boundary_async: the boundary requests' work on `side`; they sit
+        out the next step."""
+        self._check(lib.gp_boundary_async(self.h, slots.numel(), _ptr(slots),
+                                          ctypes.c_void_p(side.cuda_stream)))
 
     def free(self, slot: int):
         self._check(lib.gp_free(self.h, slot))

@@ -62,6 +62,8 @@ extern "C" {
                                     counted in gp_ctrl.starved instead       */
 #define GP_ST_BAD_PLAN     0x10u /* inconsistent compaction plan            */
 #define GP_ST_POS_RANGE    0x20u /* a request reached max_seq_len            */
+#define GP_ST_SMEM_ALIGN   0x40u /* attention kernel skipped: its shared
+                                    memory was not 1024-byte aligned         */
 
 /* ---- configuration --------------------------------------------------- */
 #define GP_DTYPE_F32   0
@@ -292,6 +294,32 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n,
  * Asynchronous. */
 int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev);
 
+/* gp_boundary with the boundary work made asynchronous.  Follows the
+ * evolve.pub review of "GrowPage: On-Demand KV Budgeting for Efficient LLM
+ * Reasoning Serving", "Frequently asked questions": GrowPage builds on
+ * Zipage's machinery, including its asynchronous compression.  The pages
+ * say no more; this is a reading: a request at a boundary sits out the next
+ * step while its boundary work runs beside that step.
+ *   - on the pool's stream: the requests not at a boundary are finished
+ *     (their staged token appended), so the next step can start at once;
+ *   - on side_stream (a cudaStream_t other than the pool's): for the
+ *     requests at a boundary, everything gp_boundary does for them -- Top-p
+ *     working sets, Delta, the grow / compact decision (growth served in
+ *     ascending slot order), the compaction moves and the staged token.
+ * Results are those of gp_boundary.  The requests that were at a boundary
+ * must not be in the next step's slot list (the plan kernel refuses a
+ * request whose boundary work is still running: GP_ST_BAD_SLOTS, step
+ * dropped); from the step after they may take part again, and that step's
+ * first gp_decode_step makes the pool's stream wait for the work on the
+ * device (no host sync).  Steps are counted by calls: if no request is left
+ * for the next step, call it anyway with n = 0 (every layer, then
+ * gp_boundary_async or gp_boundary).  Every other call that reads or changes the pool
+ * between steps (admission, gp_free, prefixes, SYNC calls, the read
+ * ceiling, gp_set_stream) first makes the pool's stream wait for it too.
+ * A later step's boundary work is ordered after an earlier one's, even on
+ * another side stream.  Asynchronous. */
+int gp_boundary_async(gp_pool* pool, int32_t n, const int32_t* slots_dev, void* side_stream);
+
 /* Release a request: its private pages are pushed in block-table order; a
  * prefix whose last reference goes is pushed too.  Asynchronous. */
 int gp_free(gp_pool* pool, int32_t slot);
@@ -355,7 +383,9 @@ int gp_sync(gp_pool* pool);
  *   GP_ST_TIMEOUT: a bounded wait gave up; that step's outputs are
  *     incomplete;
  *   GP_ST_BAD_PAGE: an out-of-range page id was read as page 0; the
- *     affected request's contents are undefined.
+ *     affected request's contents are undefined;
+ *   GP_ST_SMEM_ALIGN: the attention kernel did not run; that step's
+ *     outputs are undefined.
  * SYNC. */
 int gp_clear_status(gp_pool* pool, uint32_t* status_out, int32_t* info_out);
 

@@ -271,7 +271,13 @@ class Scenario:
     """
 
     def __init__(self, w, max_requests, num_pages, mode=gpb.GP_MODE_GROWPAGE, compare_all=True,
-                 gen_device="cpu", max_seq_len=None, max_prefixes=0, tol=None, oracle_pages=None):
+                 gen_device="cpu", max_seq_len=None, max_prefixes=0, tol=None, oracle_pages=None,
+                 side=None, record=False):
+        """``side``: a second torch stream; steps then end with
+        gp_boundary_async on it.  ``record``: keep every step's slot list,
+        inputs and outputs (device tensors) in ``self.trace``."""
+        self.side = side
+        self.trace = [] if record else None
         self.w = w
         self.full_kv = mode == gpb.GP_MODE_FULL_KV
         self.cfg = gpb.config_for(w, mode=mode, max_requests=max_requests, num_pages=num_pages,
@@ -326,10 +332,21 @@ class Scenario:
             self.ora.free_request(slot)
             self.cmp.discard(slot)
 
-    def step(self, check=True):
+    def step(self, check=True, exclude=()):
+        """One step of the active requests not in ``exclude``; returns the
+        slots that were at a boundary (of the compared requests)."""
         w, rep = self.w, self.rep
         L, hk, hq, d, P = w.num_layers, w.num_kv_heads, w.num_q_heads, w.head_dim, w.page_size
-        slots = sorted(self.active)
+        slots = sorted(s for s in self.active if s not in exclude)
+        if not slots:
+            if self.side is not None:   # an empty step still counts as a step
+                empty = torch.zeros(0, dtype=torch.int32, device=self.dev)
+                for l in range(L):
+                    self.pool.decode_step(l, empty, None, None, None, None)
+                self.pool.boundary_async(empty, self.side)
+                if self.trace is not None:
+                    self.trace.append(([], None, None, None, []))
+            return set()
         qs, ks, vs = [], [], []
         for s in slots:
             q, k, v = self.active[s].next_step()
@@ -344,9 +361,14 @@ class Scenario:
             self.pool.decode_step(l, slots_dev, q[:, l].contiguous(), k[:, l].contiguous(),
                                   v[:, l].contiguous(), o)
             outs.append(o)
-        self.pool.boundary(slots_dev)
+        if self.side is not None:
+            self.pool.boundary_async(slots_dev, self.side)
+        else:
+            self.pool.boundary(slots_dev)
+        if self.trace is not None:
+            self.trace.append((list(slots), q, k, v, outs))
         self.pool.sync()
-        cslots = sorted(self.cmp)
+        cslots = sorted(s for s in self.cmp if s in slots)
         idx = [slots.index(s) for s in cslots]
         metas, bts = {}, {}
         for s in cslots:
@@ -364,17 +386,20 @@ class Scenario:
                     tok_pos = self.pool.region("tok_pos")
                     pos = _private_positions(tok_pos, bts[s][m.n_pre_pages:], m.seq_priv - 1, L, hk, P)
                     self.arb.gpu_kept[s] = [[set(pos[l, h].tolist()) for h in range(hk)] for l in range(L)]
+        bnd = set()
         if cslots:
             qc = q[idx].double().cpu().numpy()
             kc = k[idx].double().cpu().numpy()
             vc = v[idx].double().cpu().numpy()
             res = self.ora.step(cslots, qc, kc, vc, arbiter=self.arb)
             rep.steps += 1
+            bnd = set(res["records"])
             if check:
                 out_g = torch.stack([o[idx].float().cpu() for o in outs], 1).double().numpy()
                 self._compare(res, cslots, out_g, metas, bts, tok_pos)
         for s in cslots:
             self.prev_nb[s] = metas[s].n_boundaries
+        return bnd
 
     def _compare(self, res, cslots, out_g, metas, bts, tok_pos):
         w, rep = self.w, self.rep

@@ -318,3 +318,60 @@ def test_full_kv_stops_at_the_page_cap(env, shape):
     for s in h.slots:
         m, _ = h.pool.request(s)
         assert m.n_pages == w.max_pages_per_req and m.n_starved > 0
+
+
+@pytest.mark.parametrize("mode_name", ["GROWPAGE", "FULL_KV"])
+def test_async_boundary_work(env, mode_name):
+    # gp_boundary_async: the requests at a boundary get their boundary work
+    # on a second stream and sit out the next step.  Checked step by step
+    # against the oracle (which simply leaves them out of that step); then a
+    # twin pool replays the same steps with no host sync between them, so the
+    # second stream really runs beside the next step, and must end
+    # bit-identical: every output of every step, block tables, token
+    # positions, the free stack and the summaries.
+    H, gp, synth = env
+    mode = getattr(gp, "GP_MODE_" + mode_name)
+    w = synth.WORKLOADS["llama8b_1layer"].replace(num_layers=2, prompt_min=100, prompt_max=200,
+                                                  budget_pages=8, max_pages_per_req=16)
+    side = torch.cuda.Stream()
+    sc = H.Scenario(w, max_requests=6, num_pages=200, mode=mode, side=side, record=True)
+    for s in range(6):
+        sc.admit(s, s, budget_pages=8)
+    out_of_step = set()
+    for _ in range(150):
+        bnd = sc.step(exclude=out_of_step)
+        if sc.rep.failures:
+            break
+        out_of_step = bnd
+        sc.ora.check_invariants()
+    _check(sc.rep)
+    assert sc.rep.boundaries > 30
+    twin = gp.Pool(sc.cfg)
+    for s in range(6):
+        pl, T = synth.draw_lengths(w, 1, s)[0]
+        k, v = synth.RequestStream(w, s, T).prompt(pl)
+        twin.add_request(s, k.cuda().contiguous(), v.cuda().contiguous(), 8)
+    side2 = torch.cuda.Stream()
+    outs = []
+    for slots, q, k, v, _ in sc.trace:
+        sd = torch.tensor(slots, dtype=torch.int32, device="cuda")
+        step_out = []
+        for l in range(w.num_layers):
+            if not slots:
+                twin.decode_step(l, sd, None, None, None, None)
+                continue
+            o = torch.empty(len(slots), w.num_q_heads, w.head_dim, dtype=w.torch_dtype, device="cuda")
+            twin.decode_step(l, sd, q[:, l].contiguous(), k[:, l].contiguous(),
+                             v[:, l].contiguous(), o)
+            step_out.append(o)
+        twin.boundary_async(sd, side2)
+        outs.append(step_out)
+    twin.sync()
+    for (_, _, _, _, ref), got in zip(sc.trace, outs):
+        for a, b in zip(ref, got):
+            assert torch.equal(a, b)
+    a, b = sc.pool.state(tok_pos=True), twin.state(tok_pos=True)
+    assert [bytes(m) for m in a["req"]] == [bytes(m) for m in b["req"]]
+    for key in ("block", "free_stack", "tok_pos"):
+        assert np.array_equal(a[key], b[key]), key
+    assert torch.equal(sc.pool.region("summary"), twin.region("summary"))
