@@ -84,6 +84,8 @@ def parse():
                     help="continuous-batching workload: decode steps before its window "
                          "(arrivals fill the 128 slots by about step 1600)")
     ap.add_argument("--cb-steps", type=int, default=128)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay of the one-layer workload")
     ap.add_argument("--no-async", action="store_true",
                     help="skip the asynchronous boundary measurement")
     ap.add_argument("--burst-steps", type=int, default=1024,
@@ -219,19 +221,21 @@ def _load_peaks():
     return 6400.0, "fallback"
 
 
-def time_window(eng, steps, w, sample_clocks=False, local=0):
+def time_window(eng, steps, w, sample_clocks=False, local=0, layer_events=True):
     """Time `steps` decode steps of an engine with CUDA events on its stream.
 
     Events per step: before the step, after layer 0, after the last layer,
     after the boundary call.  The layer-call time is taken over layers
     1..L-1 (for a 1-layer stack: the whole step before the boundary call,
-    plan kernel included).  Returns the window's counters and times.
+    plan kernel included).  With layer_events False (a step replayed as one
+    CUDA graph) only the step's ends are timed.  Returns the window's counters
+    and times.
     """
     stream = eng.pool.stream
     L = w.num_layers
     torch.cuda.synchronize()
     st0 = eng.pool.stats()
-    launches0 = eng.pool.launch_count()
+    launches0 = eng.pool.launch_count() + eng.graph_launches
     tok0 = eng.tokens_timed
     pre0 = eng.preempted
     evs, nbs = [], []
@@ -259,7 +263,8 @@ def time_window(eng, steps, w, sample_clocks=False, local=0):
         def after():
             e[3].record(stream)
 
-        n = eng.step(timed=True, before_step=before, after_layer=after_layer, after_step=after)
+        n = eng.step(timed=True, before_step=before, after_step=after,
+                     after_layer=after_layer if layer_events else None)
         if n:
             req_steps += n
             evs.append(e)
@@ -271,8 +276,10 @@ def time_window(eng, steps, w, sample_clocks=False, local=0):
     clocks = clk.stop() if clk else None
     st1 = eng.pool.stats()
     step_t = [e[0].elapsed_time(e[3]) for e in evs]
-    bnd_t = [e[2].elapsed_time(e[3]) for e in evs]
-    if L > 1:
+    bnd_t = [e[2].elapsed_time(e[3]) for e in evs] if layer_events else [0.0] * len(evs)
+    if not layer_events:
+        attn_ms, n_attn = 0.0, 0
+    elif L > 1:
         attn_ms = sum(e[1].elapsed_time(e[2]) for e in evs)
         n_attn = (L - 1) * len(evs)
     else:
@@ -284,7 +291,8 @@ def time_window(eng, steps, w, sample_clocks=False, local=0):
     nsteps = max(1, len(evs))
     per_layer_bytes = attention_bytes(w, dtok, req_steps, dbtok)   # one layer, all steps
     res = dict(steps=len(evs), step_ms=step_ms, attn_ms=attn_ms, tokens=eng.tokens_timed - tok0,
-               clocks=clocks, launches=eng.pool.launch_count() - launches0, dtok=dtok,
+               clocks=clocks, launches=eng.pool.launch_count() + eng.graph_launches - launches0,
+               dtok=dtok,
                dbtok=dbtok, req_steps=req_steps,
                boundaries=st1.boundaries - st0.boundaries, grows=st1.grows - st0.grows,
                compacts=st1.compacts - st0.compacts, denied=st1.denied - st0.denied,
@@ -341,11 +349,12 @@ def run_ours(args, ws, rank, local):
     w = workload_for(args)
     hbm_peak, peak_src = _load_peaks()
 
-    def run_engine(wl, mode, label, windows, rate=0.0, extras=False, async_boundary=False):
+    def run_engine(wl, mode, label, windows, rate=0.0, extras=False, async_boundary=False,
+                   graph=False):
         """One engine; windows = [(decode steps before the window, timed steps)].
         The warm-up steps come right before the first window."""
         eng = Engine(wl, mode=mode, device=dev, seed_offset=rank, random_grow_rate=rate,
-                     async_boundary=async_boundary)
+                     async_boundary=async_boundary, use_graph=graph)
         eng.fill()
         out = []
         for k, (start, steps) in enumerate(windows):
@@ -355,7 +364,8 @@ def run_ours(args, ws, rank, local):
                 eng.step()
             if k == 0 and ws > 1:
                 torch.distributed.barrier()
-            r = time_window(eng, steps, wl, sample_clocks=(k == 0), local=local)
+            r = time_window(eng, steps, wl, sample_clocks=(k == 0), local=local,
+                            layer_events=not graph)
             r["label"], r["start"] = label, eng.clock - steps
             if k == 0 and extras:
                 r["ceilings"] = measure_ceilings(eng, wl)
@@ -509,6 +519,15 @@ def run_ours(args, ws, rank, local):
                                                   [(start, steps)])[0],
                            "full_kv": run_engine(wl, gpb.GP_MODE_FULL_KV, "full_kv",
                                                  [(start, steps)])[0]}
+            if name == "llama8b_1layer" and not args.no_graph:
+                # a one-layer step is too short to hide the host's launches:
+                # the same steps replayed as one CUDA graph each
+                for key, mode in (("growpage_graph", gpb.GP_MODE_GROWPAGE),
+                                  ("full_kv_graph", gpb.GP_MODE_FULL_KV)):
+                    try:
+                        other[name][key] = run_engine(wl, mode, key, [(start, steps)], graph=True)[0]
+                    except Exception as ex:  # capture refused: report it, keep the rest
+                        other[name][key + "_error"] = str(ex)[:200]
             if name == "stress_burst" and not args.no_async:
                 async_res[name] = run_engine(wl, gpb.GP_MODE_GROWPAGE, "async", [(start, steps)],
                                              async_boundary=True)[0]
@@ -613,6 +632,15 @@ def run_ours(args, ws, rank, local):
                  "growpage": summarize(rr["growpage"], ws, hbm_peak),
                  "full_kv": summarize(rr["full_kv"], ws, hbm_peak)}
             o["growpage_vs_full_kv"] = round(o["growpage"]["value"] / max(1e-9, o["full_kv"]["value"]), 4)
+            for key in ("growpage_graph", "full_kv_graph"):
+                if key in rr:
+                    o[key] = summarize(rr[key], ws, hbm_peak)
+                    o[key]["gpu_launches"] = int(rr[key]["launches"])
+                elif key + "_error" in rr:
+                    o[key] = {"unavailable": rr[key + "_error"]}
+            if "growpage_graph" in rr and "full_kv_graph" in rr:
+                o["graph_growpage_vs_full_kv"] = round(o["growpage_graph"]["value"] /
+                                                       max(1e-9, o["full_kv_graph"]["value"]), 4)
             line["workloads"][name] = o
     return line
 
