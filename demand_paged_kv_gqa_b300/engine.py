@@ -36,6 +36,13 @@ In full-KV mode page use is a function of the step count alone, so the host
 tracks it exactly without reading the device.  Its page cap per request is
 raised to hold the longest request, so that a request never starves at it.
 
+Graphs.  With ``use_graph``, a step in which every slot takes part is
+captured once as a CUDA graph (all layers and the boundary call) and
+replayed: the slot list and the q / k / v / out buffers are then the same
+tensors every step, and everything else the step reads lives in the pool's
+device state.  This removes the host's launch cost from steps too short to
+hide it (a single layer).
+
 Inputs are drawn on the device by ``synth.BatchStream`` (the workload's
 recipe, batched); this module does not time anything itself but exposes
 hooks (``before_step`` / ``after_layer`` / ``after_step``) for events.
@@ -77,7 +84,8 @@ class Engine:
     def __init__(self, w: synth.Workload, mode=gpb.GP_MODE_GROWPAGE, device="cuda",
                  num_pages: Optional[int] = None, batch: Optional[int] = None,
                  seed_offset: int = 0, max_seq_len: Optional[int] = None,
-                 random_grow_rate: float = 0.0, async_boundary: bool = False):
+                 random_grow_rate: float = 0.0, async_boundary: bool = False,
+                 use_graph: bool = False):
         self.w = w
         self.mode = mode
         self.full_kv = mode == gpb.GP_MODE_FULL_KV
@@ -121,6 +129,10 @@ class Engine:
         # their boundary work on a second stream and sit out the next step
         self.side = torch.cuda.Stream(device=self.device) if async_boundary else None
         self.out_of_step = set()
+        self.use_graph = use_graph and not async_boundary
+        self._graph = None
+        self.graph_launches = 0     # library launches replayed through the graph
+        self._graph_per_step = 0
         self._slots_dev = None
         self._active_key = None
         L, hq, hk, d = w.num_layers, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -272,6 +284,24 @@ class Engine:
             self._active_key = key
         return self._slots_dev
 
+    def _replay(self, slots_dev):
+        """One full step through the captured graph (captured on first use)."""
+        if self._graph is None:
+            L = self.w.num_layers
+            home = self.pool.stream
+            g = torch.cuda.CUDAGraph()
+            n0 = self.pool.launch_count()
+            with torch.cuda.graph(g):
+                self.pool.set_stream(torch.cuda.current_stream())
+                for l in range(L):
+                    self.pool.decode_step(l, slots_dev, self.q[l], self.k[l], self.v[l], self.out[l])
+                self.pool.boundary(slots_dev)
+            self.pool.set_stream(home)
+            self._graph = g
+            self._graph_per_step = self.pool.launch_count() - n0
+        self._graph.replay()
+        self.graph_launches += self._graph_per_step
+
     def drained(self) -> bool:
         """No request active, queued or still to arrive."""
         return (not self.active() and not self.queue and self.total is not None
@@ -312,16 +342,19 @@ class Engine:
         L = self.w.num_layers
         if before_step:
             before_step()
-        for l in range(L):
-            if before_layer:
-                before_layer(l)
-            self.pool.decode_step(l, slots_dev, q[l], k[l], v[l], self.out[l, :n])
-            if after_layer:
-                after_layer(l)
-        if self.side is not None:
-            self.pool.boundary_async(slots_dev, self.side)
+        if self.use_graph and n == self.batch and not (before_layer or after_layer):
+            self._replay(slots_dev)
         else:
-            self.pool.boundary(slots_dev)
+            for l in range(L):
+                if before_layer:
+                    before_layer(l)
+                self.pool.decode_step(l, slots_dev, q[l], k[l], v[l], self.out[l, :n])
+                if after_layer:
+                    after_layer(l)
+            if self.side is not None:
+                self.pool.boundary_async(slots_dev, self.side)
+            else:
+                self.pool.boundary(slots_dev)
         if after_step:
             after_step()
         if self.side is not None:

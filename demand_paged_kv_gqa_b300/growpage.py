@@ -220,6 +220,11 @@ class Pool:
     def sync(self):
         self._check(lib.gp_sync(self.h))
 
+    def set_stream(self, stream: torch.cuda.Stream):
+        """Enqueue later calls on `stream` (gp_set_stream)."""
+        self._check(lib.gp_set_stream(self.h, ctypes.c_void_p(stream.cuda_stream)))
+        self.stream = stream
+
     def clear_status(self):
         """Read and clear the device status word: (GP_ST_* bits, info)."""
         st, info = ctypes.c_uint32(0), ctypes.c_int32(0)

@@ -331,7 +331,7 @@ def test_async_boundary_work(env, mode_name):
     # positions, the free stack and the summaries.
     H, gp, synth = env
     mode = getattr(gp, "GP_MODE_" + mode_name)
-    w = synth.WORKLOADS["llama8b_1layer"].replace(num_layers=2, prompt_min=100, prompt_max=200,
+    w = synth.WORKLOADS["llama8b_1layer"].replace(num_layers=2, prompt_min=60, prompt_max=128,
                                                   budget_pages=8, max_pages_per_req=16)
     side = torch.cuda.Stream()
     sc = H.Scenario(w, max_requests=6, num_pages=200, mode=mode, side=side, record=True)

@@ -157,3 +157,34 @@ def test_stress_burst_full_size_sampled(env):
     assert st.boundaries == 256 * 3
     del sc
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode_name", ["GROWPAGE", "FULL_KV"])
+def test_graph_replay_equals_eager_steps(env, mode_name):
+    # Steps replayed as one captured CUDA graph each end bit-identical to the
+    # same steps launched call by call: outputs, request metadata, block
+    # tables, token positions, summaries (one Llama-3-8B-shaped layer, 16
+    # requests, boundaries, grows, compactions and refills on the way).
+    import numpy as np
+    from demand_paged_kv_gqa_b300.engine import Engine
+    H, gp, synth = env
+    mode = getattr(gp, "GP_MODE_" + mode_name)
+    w = synth.WORKLOADS["llama8b_1layer"].replace(decode_steps=300, num_pages=2048)
+    runs = []
+    for graph in (False, True):
+        eng = Engine(w, mode=mode, use_graph=graph)
+        eng.fill()
+        for _ in range(400):
+            eng.prepare_inputs()
+            eng.step()
+        eng.pool.sync()
+        runs.append(eng)
+    a, b = runs
+    assert b.graph_launches > 0 and b.finished == a.finished > 0
+    assert torch.equal(a.out, b.out)
+    sa, sb = a.pool.state(tok_pos=True), b.pool.state(tok_pos=True)
+    assert [bytes(m) for m in sa["req"]] == [bytes(m) for m in sb["req"]]
+    for key in ("block", "free_stack", "tok_pos"):
+        assert np.array_equal(sa[key], sb[key]), key
+    assert torch.equal(a.pool.region("summary"), b.pool.region("summary"))
+    assert sa["ctrl"].boundaries == sb["ctrl"].boundaries > 0
