@@ -375,3 +375,17 @@ def test_async_boundary_work(env, mode_name):
     for key in ("block", "free_stack", "tok_pos"):
         assert np.array_equal(a[key], b[key]), key
     assert torch.equal(sc.pool.region("summary"), twin.region("summary"))
+
+
+@pytest.mark.parametrize("mode_name", ["GROWPAGE", "SHRINK"])
+def test_twelve_layers(env, mode_name):
+    # a deeper stack than the other full comparisons: 12 layers, 4 requests,
+    # every step, request, layer and head against the oracle
+    H, gp, synth = env
+    mode = getattr(gp, "GP_MODE_" + mode_name)
+    w = synth.WORKLOADS["llama8b_1layer"].replace(num_layers=12, prompt_min=100, prompt_max=128,
+                                                  budget_pages=8, max_pages_per_req=16)
+    h = H.Harness(w, 4, mode=mode, budget_pages=8)
+    rep = h.run(80)
+    _check(rep)
+    assert rep.boundaries >= 12
