@@ -62,8 +62,11 @@ __device__ __forceinline__ void store_row(T* row, int sigma, const float (&f)[Gm
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
 
+// Block `blk` of (request i, kv head h) covers the request's resident tokens
+// base + 16*blk .. base + 16*blk + 15 (base: a shared prefix attended
+// elsewhere, else 0).
 struct Cursor {
-  int i, h, blk, nb, slot;
+  int i, h, blk, nb, slot, base;
 };
 
 __device__ __forceinline__ int find_req(const int32_t* cum, int n, int64_t x) {
@@ -81,12 +84,14 @@ __device__ __forceinline__ void cursor_at(const PoolDev& p, int n, int64_t b, Cu
   const int nb = p.plan_nb[i];
   const int64_t r = b - (int64_t)p.Hk * p.plan_cum[i];
   c.i = i; c.nb = nb; c.h = (int)(r / nb); c.blk = (int)(r % nb); c.slot = p.plan_slot[i];
+  c.base = p.plan_base[i];
 }
 
 // Cursor at worker w's first block, as the plan kernel laid it out.
 __device__ __forceinline__ void cursor_start(const PoolDev& p, int64_t w, Cursor& c) {
   const int4 s = p.wstart[w];
   c.i = s.x; c.h = s.y >> 20; c.blk = s.y & 0xfffff; c.nb = s.z; c.slot = s.w;
+  c.base = p.plan_base[s.x];
 }
 
 // 32 consecutive block-table entries of one request, one per lane, so that
@@ -97,7 +102,7 @@ struct PageWin {
 };
 
 __device__ __forceinline__ int page_of(const PoolDev& p, PageWin& win, const Cursor& c, int lane) {
-  const int pidx = (c.blk * kBlockTok) / p.P;  // entry: prefix pages first, then private
+  const int pidx = (c.base + c.blk * kBlockTok) / p.P;  // entry: prefix pages first, then private
   if (c.slot != win.slot || pidx < win.base || pidx >= win.base + 32) {
     win.slot = c.slot;
     win.base = pidx;
@@ -117,7 +122,7 @@ __device__ __forceinline__ void cursor_next(const PoolDev& p, Cursor& c) {
     c.blk = 0;
     if (++c.h == p.Hk) {
       c.h = 0; ++c.i;
-      c.nb = p.plan_nb[c.i]; c.slot = p.plan_slot[c.i];
+      c.nb = p.plan_nb[c.i]; c.slot = p.plan_slot[c.i]; c.base = p.plan_base[c.i];
     }
   }
 }

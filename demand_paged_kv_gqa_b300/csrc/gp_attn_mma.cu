@@ -159,10 +159,10 @@ constexpr int kWarpBufFloats = ((kObFloats + kObxFloats + 3) / 4) * 4;
 // cursor crossing into the next request reads registers, not memory.
 struct PlanWin {
   int base = -(1 << 30);
-  int nb = 1, slot = 0, R = 0, flags = 0, pos = 0;
+  int nb = 1, slot = 0, R = 0, flags = 0, pos = 0, tb = 0;
 };
 struct PlanEntry {
-  int nb, slot, R, flags, pos;
+  int nb, slot, R, flags, pos, tb;  // tb: first resident token the kernel attends
 };
 
 __device__ __forceinline__ PlanEntry plan_at(const PoolDev& p, PlanWin& w, int i, int n, int lane) {
@@ -171,9 +171,9 @@ __device__ __forceinline__ PlanEntry plan_at(const PoolDev& p, PlanWin& w, int i
     const int k = i + lane;
     if (k < n) {
       w.nb = p.plan_nb[k]; w.slot = p.plan_slot[k]; w.R = p.plan_R[k];
-      w.flags = p.plan_flags[k]; w.pos = p.plan_pos[k];
+      w.flags = p.plan_flags[k]; w.pos = p.plan_pos[k]; w.tb = p.plan_base[k];
     } else {
-      w.nb = 1; w.slot = 0; w.R = 0; w.flags = 0; w.pos = 0;
+      w.nb = 1; w.slot = 0; w.R = 0; w.flags = 0; w.pos = 0; w.tb = 0;
     }
   }
   const int src = i - w.base;
@@ -183,6 +183,7 @@ __device__ __forceinline__ PlanEntry plan_at(const PoolDev& p, PlanWin& w, int i
   e.R = __shfl_sync(0xffffffffu, w.R, src);
   e.flags = __shfl_sync(0xffffffffu, w.flags, src);
   e.pos = __shfl_sync(0xffffffffu, w.pos, src);
+  e.tb = __shfl_sync(0xffffffffu, w.tb, src);
   return e;
 }
 
@@ -195,6 +196,7 @@ __device__ __forceinline__ void walk_next(const PoolDev& p, PlanWin& w, Cursor& 
         const PlanEntry e = plan_at(p, w, c.i, n, lane);
         c.nb = e.nb;
         c.slot = e.slot;
+        c.base = e.tb;
       }
     }
   }
@@ -448,6 +450,172 @@ __device__ __forceinline__ void finish_mma(const PoolDev& p, int i, int h,
   }
 }
 
+// One 16-token block of keys and values (a ring stage at sK: K then V) for
+// the 16 operand rows afr: scores, the boundary summary scores (rows 4/5,
+// written to lgX[t0 + token] for tokens below nvalid when `score`), the
+// online softmax of the G head rows (running max m, sum l, log2 domain) and
+// O^T += V^T · P^T into o.
+template <int G>
+__device__ __forceinline__ void attend_block(const uint32_t (&afr)[8][4], float (&o)[8][4], float& m,
+                                             float& l, uint32_t sK, int t0, int nvalid, bool score,
+                                             float* lgX, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const bool head_row = g < G;
+  const int mi = lane >> 3, ri = lane & 7;
+  const int k_tok = 8 * (mi >> 1) + ri, k_half = mi & 1;   // K: token, chunk parity
+  // V^T as the 16 x 16 operand (rows: dims, columns: tokens), by transposing
+  // loads of V[token][dims]: matrices (tokens 0-7 | 8-15) x (dims +0 | +8)
+  const int v_tok = 8 * (mi >> 1) + ri, v_half = mi & 1;
+  // the lane whose softmax weights feed this lane's weight column: column
+  // n < G is head n (hi part), G <= n < 2G is head n - G (lo part)
+  const int p_src = ((g >= G && g < 2 * G) ? (g - G) : g) * 4 + t;
+  const uint32_t sV = sK + 4096;
+  // ---- scores: S[16 rows][16 tokens] = A · K^T
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int ch = 2 * kk + k_half;   // 16-byte chunk of the key row
+    uint32_t b[4];
+    ldsm_x4(b, sK + (ch >> 3) * 2048 + swz(k_tok, ch & 7));
+    mma_bf16(c0, afr[kk], b[0], b[1]);
+    mma_bf16(c1, afr[kk], b[2], b[3]);
+  }
+  // this thread's tokens of the block: 2t, 2t+1, 8+2t, 9+2t
+  float sv[4] = {c0[0] + c0[2], c0[1] + c0[3], c1[0] + c1[2], c1[1] + c1[3]};
+  const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+  // summary scores: rows 4/5 (+ rows 12/13 in the same thread) plus the
+  // lo rows 6/7 held 8 lanes up
+  if (score) {
+    float other[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) other[u] = __shfl_xor_sync(0xffffffffu, sv[u], 8);
+    if (g == 4 || g == 5) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (tok[u] < nvalid) lgX[t0 + tok[u]] = sv[u] + other[u];
+    }
+  }
+  // ---- online softmax (log2 domain) for head row g
+  float mx = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (!head_row || tok[u] >= nvalid) sv[u] = -INFINITY;
+    mx = fmaxf(mx, sv[u]);
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  // the running max moves only when a score exceeds it by more than 2^8:
+  // weights stay <= 256, and the final normalisation uses the same m.
+  // The accumulator columns of a head sit in other lanes, so the rescale
+  // is taken by the whole warp (rare: a few times per piece).
+  if (__any_sync(0xffffffffu, mx > m + 8.0f)) {
+    float al = 1.0f;
+    if (mx > m + 8.0f) {
+      al = exp2f(m - mx);             // 0 when m == -inf
+      l *= al;
+      m = mx;
+    }
+    // column c holds head c mod G (columns >= 2G are zero)
+    const float a0 = __shfl_sync(0xffffffffu, al, ((2 * t) % G) * 4);
+    const float a1 = __shfl_sync(0xffffffffu, al, ((2 * t + 1) % G) * 4);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
+    }
+  }
+  float pv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    pv[u] = (sv[u] == -INFINITY) ? 0.f : exp2f(sv[u] - m);
+    l += pv[u];
+  }
+  uint32_t ph[4], pl[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) split2(pv[u], ph[u], pl[u]);
+  // P^T as the 16 x 8 operand: this lane's column g, tokens 2t, 2t+1 and
+  // 2t+8, 2t+9 -- hi parts for g < G, lo parts of head g - G for
+  // G <= g < 2G (fetched from that head's lane), zero beyond
+  const uint32_t xl0 = __shfl_sync(0xffffffffu, pack2(pl[0], pl[1]), p_src);
+  const uint32_t xl1 = __shfl_sync(0xffffffffu, pack2(pl[2], pl[3]), p_src);
+  const uint32_t bp0 = g < G ? pack2(ph[0], ph[1]) : (g < 2 * G ? xl0 : 0u);
+  const uint32_t bp1 = g < G ? pack2(ph[2], ph[3]) : (g < 2 * G ? xl1 : 0u);
+  // ---- O^T += V^T · P^T, 16 dims at a time
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int ch = 2 * mt + v_half;   // 16-byte chunk = 8 dims
+    uint32_t a[4];
+    ldsm_x4_t(a, sV + (ch >> 3) * 2048 + swz(v_tok, ch & 7));
+    mma_bf16(o[mt], a, bp0, bp1);
+  }
+}
+
+// A piece's totals into the warp buffer ob: [G][D] unnormalised output,
+// then m[G] (log2 domain), l[G].  l is reduced over the row's four lanes.
+template <int G>
+__device__ __forceinline__ void piece_totals(const float (&o)[8][4], float m, float l, float* ob,
+                                             int lane) {
+  constexpr int D = kMmaD;
+  const int g = lane >> 2, t = lane & 3;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  // head h = column h (hi) + column G + h (lo): for G = 4 the lo columns
+  // sit two lanes up, for G = 2 one lane up, for G = 1 in the same lane
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    float r[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (G == 1) r[u] = o[mt][u & 2] + o[mt][(u & 2) + 1];
+      else r[u] = o[mt][u] + __shfl_xor_sync(0xffffffffu, o[mt][u], G == 4 ? 2 : 1);
+    }
+    const int d0 = 16 * mt + g;
+    if (G == 1) {
+      if (t == 0) { ob[d0] = r[0]; ob[d0 + 8] = r[2]; }
+    } else if (2 * t < G) {
+      ob[(2 * t) * D + d0] = r[0];
+      ob[(2 * t + 1) * D + d0] = r[1];
+      ob[(2 * t) * D + d0 + 8] = r[2];
+      ob[(2 * t + 1) * D + d0 + 8] = r[3];
+    }
+  }
+  if (g < G && t == 0) {
+    ob[G * D + g] = m;
+    ob[G * D + G + g] = l;
+  }
+}
+
+// Merge the shared-prefix states of (request i, kv head h) -- one per prefix
+// range, written by prefix_attn_kernel -- into a piece's totals in ob.
+template <int G>
+__device__ __forceinline__ void merge_prefix(const PoolDev& p, int i, int h, float* ob, int lane) {
+  constexpr int D = kMmaD, PW = G * (D + 4);
+  const int nr = p.prefix_batch ? p.pranges[i] : 0;
+  if (nr <= 0) return;
+  const float* ps = p.pstate + ((size_t)i * p.Hk + h) * p.max_pranges * PW;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float m = ob[G * D + g], l = ob[G * D + G + g];
+    float4 acc = *reinterpret_cast<const float4*>(ob + g * D + 4 * lane);
+    for (int r = 0; r < nr; ++r) {
+      const float* pr = ps + (size_t)r * PW + g * (D + 4);
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pr + D));
+      const float4 ov = __ldcg(reinterpret_cast<const float4*>(pr) + lane);
+      if (ml.x == -INFINITY) continue;
+      const float mn = fmaxf(m, ml.x);
+      const float al = (m == -INFINITY) ? 0.f : exp2f(m - mn);
+      const float be = exp2f(ml.x - mn);
+      l = l * al + ml.y * be;
+      acc.x = acc.x * al + ov.x * be; acc.y = acc.y * al + ov.y * be;
+      acc.z = acc.z * al + ov.z * be; acc.w = acc.w * al + ov.w * be;
+      m = mn;
+    }
+    __syncwarp();
+    *reinterpret_cast<float4*>(ob + g * D + 4 * lane) = acc;
+    if (lane == 0) { ob[G * D + g] = m; ob[G * D + G + g] = l; }
+  }
+  __syncwarp();
+}
+
 // ----------------------------------------------------------- attention ---
 template <int G, int S>
 __global__ void __launch_bounds__(kMmaWarps * 32)
@@ -464,7 +632,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
+  const int g = lane >> 2;
   uint8_t* ring = smem + (size_t)warp * S * kMmaStageB;
   float* ob = reinterpret_cast<float*>(smem + (size_t)kMmaWarps * S * kMmaStageB) + warp * kWarpBufFloats;
   float* obx = ob + kObFloats;
@@ -543,15 +711,6 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   }
   while (pitems < S && emit(true)) {}
 
-  // per-lane ldmatrix row offsets (within a stage): K (non-transposed) and V
-  const int mi = lane >> 3, ri = lane & 7;
-  const int k_tok = 8 * (mi >> 1) + ri, k_half = mi & 1;   // K: token, chunk parity
-  // V^T as the 16 x 16 operand (rows: dims, columns: tokens), by transposing
-  // loads of V[token][dims]: matrices (tokens 0-7 | 8-15) x (dims +0 | +8)
-  const int v_tok = 8 * (mi >> 1) + ri, v_half = mi & 1;
-  // the lane whose softmax weights feed this lane's weight column: column
-  // n < G is head n (hi part), G <= n < 2G is head n - G (lo part)
-  const int p_src = ((g >= G && g < 2 * G) ? (g - G) : g) * 4 + t;
   const uint32_t ring_u32 = smem_u32(ring);
 
   bool failed = false;
@@ -604,7 +763,6 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       if (cc.blk == 0) segment_duties<G>(p, layer, i, h, slot, pe.flags, in, obx, lane);
       release_item();
     }
-    const bool head_row = g < G;
     float* lgS = p.logits + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * p.logit_width;
     float* lgX = lgS + (g & 1) * p.logit_width;
 
@@ -616,121 +774,18 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
 
     for (int64_t k = 0; k < len; ++k, ++j) {
       if (!wait_item(citems, slot)) { failed = true; break; }
-      const uint32_t sK = ring_u32 + (uint32_t)(citems % S) * kMmaStageB, sV = sK + 4096;
-      // ---- scores: S[16 rows][16 tokens] = A · K^T
-      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const int ch = 2 * kk + k_half;   // 16-byte chunk of the key row
-        uint32_t b[4];
-        ldsm_x4(b, sK + (ch >> 3) * 2048 + swz(k_tok, ch & 7));
-        mma_bf16(c0, afr[kk], b[0], b[1]);
-        mma_bf16(c1, afr[kk], b[2], b[3]);
-      }
-      // this thread's tokens of the block: 2t, 2t+1, 8+2t, 9+2t
-      float sv[4] = {c0[0] + c0[2], c0[1] + c0[3], c1[0] + c1[2], c1[1] + c1[3]};
-      const int t0 = (cc.blk + (int)k) * kBlockTok;
-      const int nvalid = R - t0;
-      const int tok[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
-      // summary scores: rows 4/5 (+ rows 12/13 in the same thread) plus the
-      // lo rows 6/7 held 8 lanes up
-      if (score) {
-        float other[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) other[u] = __shfl_xor_sync(0xffffffffu, sv[u], 8);
-        if (g == 4 || g == 5) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (tok[u] < nvalid) lgX[t0 + tok[u]] = sv[u] + other[u];
-        }
-      }
-      // ---- online softmax (log2 domain) for head row g
-      float mx = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (!head_row || tok[u] >= nvalid) sv[u] = -INFINITY;
-        mx = fmaxf(mx, sv[u]);
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      // the running max moves only when a score exceeds it by more than 2^8:
-      // weights stay <= 256, and the final normalisation uses the same m.
-      // The accumulator columns of a head sit in other lanes, so the rescale
-      // is taken by the whole warp (rare: a few times per piece).
-      if (__any_sync(0xffffffffu, mx > m + 8.0f)) {
-        float al = 1.0f;
-        if (mx > m + 8.0f) {
-          al = exp2f(m - mx);             // 0 when m == -inf
-          l *= al;
-          m = mx;
-        }
-        // column c holds head c mod G (columns >= 2G are zero)
-        const float a0 = __shfl_sync(0xffffffffu, al, ((2 * t) % G) * 4);
-        const float a1 = __shfl_sync(0xffffffffu, al, ((2 * t + 1) % G) * 4);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
-        }
-      }
-      float pv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        pv[u] = (sv[u] == -INFINITY) ? 0.f : exp2f(sv[u] - m);
-        l += pv[u];
-      }
-      uint32_t ph[4], pl[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) split2(pv[u], ph[u], pl[u]);
-      // P^T as the 16 x 8 operand: this lane's column g, tokens 2t, 2t+1 and
-      // 2t+8, 2t+9 -- hi parts for g < G, lo parts of head g - G for
-      // G <= g < 2G (fetched from that head's lane), zero beyond
-      const uint32_t xl0 = __shfl_sync(0xffffffffu, pack2(pl[0], pl[1]), p_src);
-      const uint32_t xl1 = __shfl_sync(0xffffffffu, pack2(pl[2], pl[3]), p_src);
-      const uint32_t bp0 = g < G ? pack2(ph[0], ph[1]) : (g < 2 * G ? xl0 : 0u);
-      const uint32_t bp1 = g < G ? pack2(ph[2], ph[3]) : (g < 2 * G ? xl1 : 0u);
-      // ---- O^T += V^T · P^T, 16 dims at a time
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int ch = 2 * mt + v_half;   // 16-byte chunk = 8 dims
-        uint32_t a[4];
-        ldsm_x4_t(a, sV + (ch >> 3) * 2048 + swz(v_tok, ch & 7));
-        mma_bf16(o[mt], a, bp0, bp1);
-      }
+      const uint32_t sK = ring_u32 + (uint32_t)(citems % S) * kMmaStageB;
+      const int t0 = pe.tb + (cc.blk + (int)k) * kBlockTok;
+      attend_block<G>(afr, o, m, l, sK, t0, R - t0, score, lgX, lane);
       release_item();
     }
     if (failed) break;
 
     // ---- piece totals into the warp buffer: ob[g][dim], m[g], l[g]
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    {
-      // head h = column h (hi) + column G + h (lo): for G = 4 the lo columns
-      // sit two lanes up, for G = 2 one lane up, for G = 1 in the same lane
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        float r[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          if (G == 1) r[u] = o[mt][u & 2] + o[mt][(u & 2) + 1];
-          else r[u] = o[mt][u] + __shfl_xor_sync(0xffffffffu, o[mt][u], G == 4 ? 2 : 1);
-        }
-        const int d0 = 16 * mt + g;
-        if (G == 1) {
-          if (t == 0) { ob[d0] = r[0]; ob[d0 + 8] = r[2]; }
-        } else if (2 * t < G) {
-          ob[(2 * t) * D + d0] = r[0];
-          ob[(2 * t + 1) * D + d0] = r[1];
-          ob[(2 * t) * D + d0 + 8] = r[2];
-          ob[(2 * t + 1) * D + d0 + 8] = r[3];
-        }
-      }
-      if (head_row && t == 0) {
-        ob[G * D + g] = m;
-        ob[G * D + G + g] = l;
-      }
-    }
+    piece_totals<G>(o, m, l, ob, lane);
     __syncwarp();
     if (full) {
+      merge_prefix<G>(p, i, h, ob, lane);  // the shared prefix, attended beforehand
       finish_mma<G>(p, i, h, out, ob, obx, lane);
     } else {
       // a cut (request, head): leave this piece's state for combine_kernel
@@ -801,15 +856,22 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
     lsum[g] = 0.f;
     acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
   }
-  // online merge over the parts, four at a time with all their loads issued first
+  // online merge over the parts, four at a time with all their loads issued
+  // first: the workers' states, then the shared-prefix ranges' states
   constexpr int CH = 4;
-  for (int base = 0; base < nparts; base += CH) {
+  const int nr = p.prefix_batch ? p.pranges[i] : 0;
+  const float* pst = p.pstate + ((size_t)i * p.Hk + h) * p.max_pranges * PW;
+  auto part_or_prefix = [&](int k) -> const float* {
+    return k < nparts ? part_of(k) : pst + (size_t)(k - nparts) * PW;
+  };
+  const int ntot = nparts + nr;
+  for (int base = 0; base < ntot; base += CH) {
     float2 ml[CH][G];
     float4 ov[CH][G];
 #pragma unroll
     for (int u = 0; u < CH; ++u) {
-      const bool ok = base + u < nparts;
-      const float* pk = part_of(ok ? base + u : base);
+      const bool ok = base + u < ntot;
+      const float* pk = part_or_prefix(ok ? base + u : base);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         ml[u][g] = ok ? __ldcg(reinterpret_cast<const float2*>(pk + g * (D + 4) + D))
@@ -854,6 +916,206 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
   }
 }
 
+// ------------------------------------------------------ shared prefixes ---
+//
+// prefix_attn_kernel: the attention of the step's requests over the shared
+// prefixes they use, computed once per group instead of once per request.
+// A unit is (prefix, chunk of up to kPrefChunk of its members in this step,
+// kv head, range of kPrefRangeBlocks 16-token blocks).  The CTA's four warps
+// share one ring of K/V blocks, so each prefix block is read from HBM once
+// per chunk; warp w runs members w and w + 4 through the same tensor-core
+// steps as the attention kernel (attend_block).  Each member leaves, per
+// range, its unnormalised output, running max (log2 domain) and sum per
+// query head in pstate[member][head][range]; the attention kernel (uncut
+// segments) or combine_kernel (cut ones) merges them.  A member at a
+// boundary also gets its summary scores of the prefix tokens.  Every wait is
+// bounded and on the CTA's own copies.
+constexpr int kPrefWarps = 4;
+constexpr int kPrefStages = 3;
+// per member: q rows [G][kQPitch] bf16, the summaries before the step, the
+// rotary rows of its position (fp32), the summaries after the fold
+constexpr int kPmQ = 0, kPmS = 1088, kPmC32 = 2112, kPmS32 = 2368, kPmSF = 2624;
+constexpr int kPrefMemberB = 3648;
+
+size_t prefix_smem_bytes() {
+  return (size_t)kPrefStages * kMmaStageB + (size_t)kPrefWarps * 2 * kPrefMemberB +
+         (size_t)kPrefWarps * kObFloats * 4 + (size_t)kPrefStages * 8;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kPrefWarps * 32)
+prefix_attn_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
+                   const __nv_bfloat16* __restrict__ q) {
+  constexpr int D = kMmaD, S = kPrefStages, PW = G * (D + 4);
+  // stages on 1024-byte boundaries (128-byte swizzle); see attn_mma_kernel
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* ring = smem_raw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* const after_ring = smem_raw + (size_t)S * kMmaStageB;
+  uint8_t* mbuf = after_ring + (size_t)warp * 2 * kPrefMemberB;
+  float* ob = reinterpret_cast<float*>(after_ring + (size_t)kPrefWarps * 2 * kPrefMemberB) +
+              warp * kObFloats;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(after_ring + (size_t)kPrefWarps * 2 * kPrefMemberB +
+                                               (size_t)kPrefWarps * kObFloats * 4);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_status(p, GP_ST_SMEM_ALIGN, (int)(smem_u32(smem_raw) & 1023u));
+    return;
+  }
+  const int units = p.plan_misc[3];  // final before the step's first attention launch
+  if ((int)blockIdx.x >= units) return;
+  // the units' prefix table, once per CTA (final before the step's first launch)
+  __shared__ int s_ucum[kMaxPrefixBatch + 1];
+  const int np = p.max_prefixes;
+  for (int k = threadIdx.x; k <= np; k += blockDim.x) s_ucum[k] = p.unit_cum[k];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // q, the summaries and the score rows belong to earlier kernels
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint32_t ring_u32 = smem_u32(ring);
+  int64_t issued = 0, used = 0;  // ring items over the CTA's life (issued: thread 0)
+  bool failed = false;
+  for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
+    // the unit: the prefix whose units contain u, then chunk, head, range
+    int lo = 0, hi = np - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_ucum[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    const int pid = lo;
+    const int npb = p.prefix[pid].len / kBlockTok;
+    const int nr = (npb + kPrefRangeBlocks - 1) / kPrefRangeBlocks;
+    int local = u - s_ucum[pid];
+    const int r = local % nr;
+    local /= nr;
+    const int h = local % p.Hk;
+    const int m0 = (local / p.Hk) * kPrefChunk;
+    const int cs = min(kPrefChunk, p.pref_cnt[pid] - m0);
+    const int b0 = r * kPrefRangeBlocks;
+    const int nblk = min(npb - b0, kPrefRangeBlocks);
+    const int32_t* ppages = p.prefix_pages + (size_t)pid * p.max_prefix_pages;
+    auto issue = [&](int b) {  // thread 0: block b of the prefix into the next stage
+      const int s = (int)(issued % S);
+      int page = ppages[(b * kBlockTok) / p.P];
+      if ((unsigned)page >= (unsigned)p.num_pages) {
+        set_status(p, GP_ST_BAD_PAGE, page);
+        page = 0;
+      }
+      const int row = (((page * p.L + layer) * p.Hk + h) * 2) * p.P + ((b * kBlockTok) % p.P);
+      uint8_t* st = ring + s * kMmaStageB;
+      fence_proxy_async_smem();
+      mbar_expect_tx(&bars[s], kMmaStageB);
+      tma_load_2d(st, &kvmap, 0, row, &bars[s]);
+      tma_load_2d(st + 2048, &kvmap, 64, row, &bars[s]);
+      tma_load_2d(st + 4096, &kvmap, 0, row + p.P, &bars[s]);
+      tma_load_2d(st + 6144, &kvmap, 64, row + p.P, &bars[s]);
+      ++issued;
+    };
+    if (threadIdx.x == 0)
+      for (int b = 0; b < min(nblk, S); ++b) issue(b0 + b);
+    // this warp's members: chunk positions warp and warp + kPrefWarps
+    int mi[2], mslot[2], mflags[2];
+    bool has[2];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int k = warp + kPrefWarps * kk;
+      has[kk] = k < cs;
+      mi[kk] = has[kk] ? p.pmem[p.pref_off[pid] + m0 + k] : 0;
+      mslot[kk] = has[kk] ? p.plan_slot[mi[kk]] : 0;
+      mflags[kk] = has[kk] ? p.plan_flags[mi[kk]] : 0;
+      if (!has[kk]) continue;
+      uint8_t* mb = mbuf + kk * kPrefMemberB;
+      for (int x = lane; x < G * 16; x += 32) {  // q rows, 16 chunks of 16 bytes each
+        const int row = x >> 4, c = x & 15;
+        *reinterpret_cast<uint4*>(mb + kPmQ + row * kQPitch * 2 + c * 16) =
+            *reinterpret_cast<const uint4*>(q + ((size_t)mi[kk] * p.Hq + h * G + row) * D + c * 8);
+      }
+      const float4* srow = reinterpret_cast<const float4*>(
+          p.summary + ((((size_t)mslot[kk] * p.L + layer) * p.Hk + h) * 2) * D);
+      for (int x = lane; x < 2 * D / 4; x += 32) reinterpret_cast<float4*>(mb + kPmS)[x] = srow[x];
+      if (p.rope) {  // cos in lanes 0-15, sin in lanes 16-31 (D/2 floats each)
+        const size_t at = (size_t)p.plan_pos[mi[kk]] * (D / 2);
+        const float4* src = reinterpret_cast<const float4*>((lane < 16 ? p.cos32 : p.sin32) + at);
+        reinterpret_cast<float4*>(mb + (lane < 16 ? kPmC32 : kPmS32))[lane & 15] = src[lane & 15];
+      }
+    }
+    __syncwarp();
+    uint32_t afr[2][8][4];
+    float* lg[2];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      uint8_t* mb = mbuf + kk * kPrefMemberB;
+      PieceIn in;
+      in.q = reinterpret_cast<const __nv_bfloat16*>(mb + kPmQ);
+      in.k = nullptr;
+      in.v = nullptr;
+      in.s = reinterpret_cast<const float*>(mb + kPmS);
+      in.c32 = reinterpret_cast<const float*>(mb + kPmC32);
+      in.s32 = reinterpret_cast<const float*>(mb + kPmS32);
+      in.c64 = nullptr;
+      in.s64 = nullptr;
+      in.sf = reinterpret_cast<float*>(mb + kPmSF);
+      if (has[kk] && (mflags[kk] & kPlanScore)) {  // the summaries after this step's fold
+        fold_rows<G>(p, in, mflags[kk], lane, reinterpret_cast<float*>(mb + kPmSF));
+        __syncwarp();
+      }
+      if (has[kk]) {
+        build_rows<G>(p, in, mflags[kk], lane, afr[kk]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) afr[kk][c][0] = afr[kk][c][1] = afr[kk][c][2] = afr[kk][c][3] = 0u;
+      }
+      lg[kk] = p.logits + ((((size_t)mslot[kk] * p.L + layer) * p.Hk + h) * 2) * p.logit_width +
+               ((lane >> 2) & 1) * p.logit_width;
+    }
+    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+    float o[2][8][4];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) o[kk][mt][0] = o[kk][mt][1] = o[kk][mt][2] = o[kk][mt][3] = 0.f;
+    for (int jb = 0; jb < nblk; ++jb) {
+      const int s = (int)(used % S);
+      const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((used / S) & 1), kWaitLimitNs);
+      if (__syncthreads_or(!ok)) {
+        if (threadIdx.x == 0) set_status(p, GP_ST_TIMEOUT, -1);
+        failed = true;
+        break;
+      }
+      const uint32_t sK = ring_u32 + (uint32_t)s * kMmaStageB;
+      const int t0 = (b0 + jb) * kBlockTok;  // prefix tokens: every one resident
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk)
+        if (has[kk])  // warp-uniform
+          attend_block<G>(afr[kk], o[kk], m[kk], l[kk], sK, t0, 1 << 30,
+                          (mflags[kk] & kPlanScore) != 0, lg[kk], lane);
+      __syncthreads();  // every warp is done with stage s
+      ++used;
+      if (threadIdx.x == 0 && jb + S < nblk) issue(b0 + jb + S);
+    }
+    if (failed) break;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      if (!has[kk]) continue;
+      piece_totals<G>(o[kk], m[kk], l[kk], ob, lane);
+      __syncwarp();
+      float* dst = p.pstate + (((size_t)mi[kk] * p.Hk + h) * p.max_pranges + r) * PW;
+      for (int x = lane; x < G * D; x += 32) dst[(x / D) * (D + 4) + (x % D)] = ob[x];
+      if (lane < 2 * G) dst[(lane % G) * (D + 4) + D + lane / G] = ob[G * D + lane];
+      __syncwarp();
+    }
+    __syncthreads();  // the member buffers are reused by the next unit
+  }
+  if (failed && threadIdx.x == 0) {
+    // let this CTA's copies in flight land before it exits
+    for (int64_t c = used; c < issued; ++c)
+      (void)mbar_wait_bounded(&bars[c % S], (uint32_t)((c / S) & 1), kWaitLimitNs);
+  }
+}
+
 size_t mma_smem_bytes() {
   return (size_t)kMmaWarps * kMmaStages * kMmaStageB + (size_t)kMmaWarps * kWarpBufFloats * 4 +
          (size_t)kMmaWarps * kMmaStages * 8;
@@ -879,10 +1141,16 @@ static cudaLaunchConfig_t pdl_config(cudaLaunchAttribute* attr, dim3 grid, dim3 
 template <int G>
 static cudaError_t launch_mma_t(const PoolDev& p, const CUtensorMap* map, int layer, int n,
                                 const void* q, const void* k, const void* v, void* out, int grid,
-                                cudaStream_t st) {
+                                bool prefix, cudaStream_t st) {
   cudaLaunchAttribute attr[1];
+  cudaError_t e = cudaSuccess;
+  if (prefix) {  // the shared prefixes first; the attention kernel merges their states
+    cudaLaunchConfig_t c0 = pdl_config(attr, dim3(grid), dim3(kPrefWarps * 32), prefix_smem_bytes(), st);
+    e = cudaLaunchKernelEx(&c0, prefix_attn_kernel<G>, *map, p, layer, (const __nv_bfloat16*)q);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t c1 = pdl_config(attr, dim3(grid), dim3(kMmaWarps * 32), mma_smem_bytes(), st);
-  cudaError_t e = cudaLaunchKernelEx(&c1, attn_mma_kernel<G, kMmaStages>, *map, p, layer,
+  e = cudaLaunchKernelEx(&c1, attn_mma_kernel<G, kMmaStages>, *map, p, layer,
                                      (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                                      (const __nv_bfloat16*)v, (__nv_bfloat16*)out);
   if (e != cudaSuccess) return e;
@@ -898,18 +1166,22 @@ static cudaError_t occupancy_mma_t(int* blocks) {
   const size_t smem = mma_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefix_attn_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)prefix_smem_bytes());
+  if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, kern, kMmaWarps * 32, smem);
 }
 
 int mma_warps_per_cta() { return kMmaWarps; }
 
-// Two launches: attn_mma_kernel, then combine_kernel.
+// Two launches, attn_mma_kernel then combine_kernel, or three with the
+// shared-prefix kernel in front of them.
 cudaError_t launch_attention_mma(const PoolDev& p, const CUtensorMap* map, int layer, int n,
                                  const void* q, const void* k, const void* v, void* out, int grid,
-                                 cudaStream_t st) {
-  if (p.G == 1) return launch_mma_t<1>(p, map, layer, n, q, k, v, out, grid, st);
-  if (p.G == 2) return launch_mma_t<2>(p, map, layer, n, q, k, v, out, grid, st);
-  if (p.G == 4) return launch_mma_t<4>(p, map, layer, n, q, k, v, out, grid, st);
+                                 bool prefix, cudaStream_t st) {
+  if (p.G == 1) return launch_mma_t<1>(p, map, layer, n, q, k, v, out, grid, prefix, st);
+  if (p.G == 2) return launch_mma_t<2>(p, map, layer, n, q, k, v, out, grid, prefix, st);
+  if (p.G == 4) return launch_mma_t<4>(p, map, layer, n, q, k, v, out, grid, prefix, st);
   return cudaErrorInvalidValue;
 }
 

@@ -21,7 +21,7 @@ cudaError_t launch_attention(const PoolDev& p, int layer, const void* q, const v
 cudaError_t attention_occupancy(const PoolDev& p, int* blocks);
 cudaError_t launch_attention_mma(const PoolDev& p, const CUtensorMap* map, int layer, int n,
                                  const void* q, const void* k, const void* v, void* out, int grid,
-                                 cudaStream_t st);
+                                 bool prefix, cudaStream_t st);
 cudaError_t attention_mma_occupancy(const PoolDev& p, int* blocks);
 int mma_warps_per_cta();
 cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count, cudaStream_t st);
@@ -65,11 +65,12 @@ struct gp_pool {
   std::vector<int> prefix_refs;  // host mirror of the device reference counts
   std::vector<char> prefix_held;
   std::vector<int> prefix_len;
+  int prefixed_active = 0;  // active requests that use a shared prefix
   // Plan buffers: steps alternate between two, so that a step's boundary
   // work on a second stream (gp_boundary_async) can still read its own plan
   // while the next step runs.  plan_set[b][k] / delta_set[b] are buffer b's
-  // eleven plan arrays and Delta accumulators; `parity` is the current one.
-  int32_t* plan_set[2][11] = {};
+  // twelve plan arrays and Delta accumulators; `parity` is the current one.
+  int32_t* plan_set[2][12] = {};
   long long* delta_set[2] = {};
   int parity = 0;
   cudaEvent_t side_ev[2] = {nullptr, nullptr};  // boundary work of a buffer's step done
@@ -97,6 +98,20 @@ int fail(gp_pool* p, int code, const std::string& msg) {
 
 int cuda_fail(gp_pool* p, cudaError_t e, const char* what) {
   return fail(p, GP_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Shared prefixes are attended once per group of requests (bf16 pages,
+// head_dim 128, the tensor-core path) when the pool holds prefixes.  Built
+// with GP_PREFIX_BATCH=0, every request attends its prefix itself.
+#ifndef GP_PREFIX_BATCH
+#define GP_PREFIX_BATCH 1
+#endif
+bool prefix_batch_on(const gp_config* c) {
+  return GP_PREFIX_BATCH && c->dtype == GP_DTYPE_BF16 && c->head_dim == 128 && c->max_prefixes > 0 &&
+         c->max_prefixes <= gp::kMaxPrefixBatch && c->max_prefix_len > 0;
+}
+int prefix_ranges_max(const gp_config* c) {
+  return (c->max_prefix_len / gp::kBlockTok + gp::kPrefRangeBlocks - 1) / gp::kPrefRangeBlocks;
 }
 
 const char* check_config(const gp_config* c) {
@@ -157,7 +172,7 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   l->rope = take((uint64_t)c->max_seq_len * (D / 2) * (8 + 8 + 4 + 4));
   l->scratch = off;
   for (int b = 0; b < 2; ++b) {                                // two plan buffers
-    for (int k = 0; k < 11; ++k) take((R + 1) * 4);           //   plan arrays
+    for (int k = 0; k < 12; ++k) take((R + 1) * 4);           //   plan arrays
     take(R * 8);                                               //   plan_delta
   }
   take((uint64_t)gp::kMaxWorkersBound * 2 * G * (D + 4) * 4);  // partials
@@ -170,6 +185,15 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   take(R * L * Hk * P * 4 * 4);                                // moves (up to 2P pairs)
   take(R * L * Hk * 4);                                        // moves_n
   take(R * 4);                                                 // busy
+  if (prefix_batch_on(c)) {                                    // shared prefixes
+    const uint64_t NP = c->max_prefixes;
+    take(R * 4);                                               //   pmem
+    take(R * 4);                                               //   pranges
+    take(NP * 4);                                              //   pref_off
+    take(NP * 4);                                              //   pref_cnt
+    take((NP + 1) * 4);                                        //   unit_cum
+    take(R * Hk * (uint64_t)prefix_ranges_max(c) * G * (D + 4) * 4);  // pstate
+  }
   l->total = off;
 }
 
@@ -214,7 +238,7 @@ void fill_dev(gp_pool* p) {
   uint64_t off = l.scratch;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = align_up(off + bytes); return b + o; };
   for (int b = 0; b < 2; ++b) {
-    for (int k = 0; k < 11; ++k) p->plan_set[b][k] = (int32_t*)take((R + 1) * 4);
+    for (int k = 0; k < 12; ++k) p->plan_set[b][k] = (int32_t*)take((R + 1) * 4);
     p->delta_set[b] = (long long*)take(R * 8);
   }
   d.partials = (float*)take((uint64_t)gp::kMaxWorkersBound * 2 * d.G * (c.head_dim + 4) * 4);
@@ -227,15 +251,26 @@ void fill_dev(gp_pool* p) {
   d.moves = (int32_t*)take(R * c.num_layers * c.num_kv_heads * c.page_size * 4 * 4);
   d.moves_n = (int32_t*)take(R * c.num_layers * c.num_kv_heads * 4);
   d.busy = (int32_t*)take(R * 4);
+  if (prefix_batch_on(&c)) {
+    const uint64_t NP = c.max_prefixes;
+    d.prefix_batch = 1;
+    d.max_pranges = prefix_ranges_max(&c);
+    d.pmem = (int32_t*)take(R * 4);
+    d.pranges = (int32_t*)take(R * 4);
+    d.pref_off = (int32_t*)take(NP * 4);
+    d.pref_cnt = (int32_t*)take(NP * 4);
+    d.unit_cum = (int32_t*)take((NP + 1) * 4);
+    d.pstate = (float*)take(R * c.num_kv_heads * (uint64_t)d.max_pranges * d.G * (c.head_dim + 4) * 4);
+  }
 }
 
 // Point the device view at plan buffer b.
 void use_plan(gp_pool* p, int b) {
   gp::PoolDev& d = p->dev;
-  int32_t** arrays[11] = {&d.plan_slot, &d.plan_R,      &d.plan_nb,   &d.plan_cum,
+  int32_t** arrays[12] = {&d.plan_slot, &d.plan_R,      &d.plan_nb,   &d.plan_cum,
                           &d.plan_flags, &d.plan_commit, &d.plan_cpos, &d.plan_dec,
-                          &d.plan_bnd,  &d.plan_misc,   &d.plan_pos};
-  for (int k = 0; k < 11; ++k) *arrays[k] = p->plan_set[b][k];
+                          &d.plan_bnd,  &d.plan_misc,   &d.plan_pos,  &d.plan_base};
+  for (int k = 0; k < 12; ++k) *arrays[k] = p->plan_set[b][k];
   d.plan_delta = p->delta_set[b];
   p->parity = b;
 }
@@ -512,7 +547,10 @@ int gp_add_request(gp_pool* pool, int32_t slot, const void* k_prompt, const void
   if (rc) return rc;
   pool->slot_active[slot] = 1;
   pool->slot_prefix[slot] = prefix_id;
-  if (prefix_id >= 0) pool->prefix_refs[prefix_id] += 1;
+  if (prefix_id >= 0) {
+    pool->prefix_refs[prefix_id] += 1;
+    pool->prefixed_active += 1;
+  }
   return GP_OK;
 }
 
@@ -545,9 +583,10 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
   }
   if (n > 0) {
     if (pool->use_mma) {
+      const bool prefix = pool->dev.prefix_batch && pool->prefixed_active > 0;
       GP_LAUNCH(pool, gp::launch_attention_mma(pool->dev, &pool->kvmap, layer, n, q, k_new, v_new,
-                                               out, pool->attn_grid, pool->stream));
-      pool->launches += 1;  // attention and combine kernels
+                                               out, pool->attn_grid, prefix, pool->stream));
+      pool->launches += prefix ? 2 : 1;  // attention and combine (and shared-prefix) kernels
     }
     else
       GP_LAUNCH(pool, gp::launch_attention(pool->dev, layer, q, k_new, v_new, out, pool->attn_grid,
@@ -622,7 +661,10 @@ int gp_free(gp_pool* pool, int32_t slot) {
   GP_LAUNCH(pool, gp::launch_free(pool->dev, slot, pool->stream));
   pool->slot_active[slot] = 0;
   const int pid = pool->slot_prefix[slot];
-  if (pid >= 0) pool->prefix_refs[pid] -= 1;
+  if (pid >= 0) {
+    pool->prefix_refs[pid] -= 1;
+    pool->prefixed_active -= 1;
+  }
   pool->slot_prefix[slot] = -1;
   return GP_OK;
 }
@@ -648,7 +690,7 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
 
 // ---- read ceiling without caller scratch -------------------------------
 //
-// Scratch of gp_kv_read_ceiling_static: the step plan (eleven arrays of
+// Scratch of gp_kv_read_ceiling_static: the step plan (twelve arrays of
 // kStaticMaxRequests + 1 ints, the Delta accumulators), the per-worker
 // start cursors and the per-worker first blocks.  It is a file-scope device array, so every GPU that loads
 // the library holds these bytes until the process exits.
@@ -657,7 +699,7 @@ constexpr int kStaticMaxRequests = 1024;
 constexpr size_t kStaticPlanArrayBytes = ((size_t)(kStaticMaxRequests + 1) * 4 + 255) / 256 * 256;
 constexpr size_t kStaticDeltaBytes = (size_t)kStaticMaxRequests * 8;
 constexpr size_t kStaticWblkBytes = ((size_t)(gp::kMaxWorkersBound + 1) * 4 + 255) / 256 * 256;
-constexpr size_t kStaticBytes = 11 * kStaticPlanArrayBytes + kStaticDeltaBytes +
+constexpr size_t kStaticBytes = 12 * kStaticPlanArrayBytes + kStaticDeltaBytes +
                                 (size_t)gp::kMaxWorkersBound * 16 + kStaticWblkBytes;
 }  // namespace
 
@@ -707,13 +749,13 @@ int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int3
   if (e != cudaSuccess) return cuda_fail(pool, e, "cudaGetSymbolAddress(g_static_scratch)");
   // the pool's view with its per-call scratch moved into the static array
   gp::PoolDev d = pool->dev;
-  int32_t** arrays[11] = {&d.plan_slot, &d.plan_R,    &d.plan_nb,  &d.plan_cum,
+  int32_t** arrays[12] = {&d.plan_slot, &d.plan_R,    &d.plan_nb,  &d.plan_cum,
                           &d.plan_flags, &d.plan_commit, &d.plan_cpos, &d.plan_dec,
-                          &d.plan_bnd,  &d.plan_misc, &d.plan_pos};
-  for (int k = 0; k < 11; ++k) *arrays[k] = (int32_t*)(base + k * kStaticPlanArrayBytes);
-  d.plan_delta = (long long*)(base + 11 * kStaticPlanArrayBytes);
-  d.wstart = (int4*)(base + 11 * kStaticPlanArrayBytes + kStaticDeltaBytes);
-  d.wblk = (int32_t*)(base + 11 * kStaticPlanArrayBytes + kStaticDeltaBytes +
+                          &d.plan_bnd,  &d.plan_misc, &d.plan_pos, &d.plan_base};
+  for (int k = 0; k < 12; ++k) *arrays[k] = (int32_t*)(base + k * kStaticPlanArrayBytes);
+  d.plan_delta = (long long*)(base + 12 * kStaticPlanArrayBytes);
+  d.wstart = (int4*)(base + 12 * kStaticPlanArrayBytes + kStaticDeltaBytes);
+  d.wblk = (int32_t*)(base + 12 * kStaticPlanArrayBytes + kStaticDeltaBytes +
                       (size_t)gp::kMaxWorkersBound * 16);
   d.seginfo = nullptr;  // not written by the plan in measurement calls
   GP_LAUNCH(pool, gp::launch_plan(d, n, slots_dev, 0, pool->stream));

@@ -65,7 +65,10 @@ struct PoolDev {
   int32_t* plan_dec;      // [max_req] decision of this step
   int32_t* plan_bnd;      // [max_req] indices i of scoring boundaries
   int32_t* plan_pos;      // [max_req] position of the step's token
-  int32_t* plan_misc;     // [0] n, [1] n scoring boundaries, [2] total blocks/Hk
+  int32_t* plan_misc;     // [0] n, [1] n scoring boundaries, [2] total blocks/Hk,
+                          // [3] shared-prefix units
+  int32_t* plan_base;     // [max_req] resident tokens the attention kernel skips (a
+                          // shared prefix handled by prefix_attn_kernel), else 0
   long long* plan_delta;  // [max_req] Delta accumulators
   // scratch: attention split-K
   float* partials;        // [num_workers][2][G][D + 2]
@@ -90,7 +93,24 @@ struct PoolDev {
   // asynchronous boundary work: 1 while a request's boundary work of an
   // earlier step still runs on the second stream (the plan refuses it)
   int32_t* busy;          // [max_req]
+  // shared prefixes (bf16 attention path): the attention over a prefix is
+  // computed once per group of the step's requests that share it
+  int32_t prefix_batch;   // 1: enabled
+  int32_t max_pranges;    // prefix ranges per request at most
+  int32_t* pmem;          // [max_req] plan indices grouped by prefix
+  int32_t* pranges;       // [max_req] prefix ranges of request i (0: none)
+  int32_t* pref_off;      // [max_prefixes] first member of prefix k in pmem
+  int32_t* pref_cnt;      // [max_prefixes] members of prefix k in this step
+  int32_t* unit_cum;      // [max_prefixes + 1] first unit of prefix k
+  float* pstate;          // [max_req][Hk][max_pranges][G][D + 4] attention state of
+                          // each prefix range: output, then max (log2), sum
 };
+
+// Shared-prefix work: a unit is (prefix, chunk of up to kPrefChunk members,
+// kv head, range of kPrefRangeBlocks 16-token blocks).
+constexpr int kPrefChunk = 8;
+constexpr int kPrefRangeBlocks = 64;
+constexpr int kMaxPrefixBatch = 512;  // prefixes the plan kernel groups (in shared memory)
 
 // Which requests a boundary-phase kernel (decide, commit) handles: every
 // request of the step, only those not at a boundary (their token appended on

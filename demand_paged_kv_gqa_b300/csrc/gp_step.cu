@@ -106,13 +106,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
         s_bad = 1;
         set_status(p, GP_ST_BAD_SLOTS, i);
         p.plan_slot[i] = 0; p.plan_R[i] = 0; p.plan_nb[i] = 1; p.plan_flags[i] = 0;
-        p.plan_pos[i] = 0;
+        p.plan_pos[i] = 0; p.plan_base[i] = 0;
         nb = 1;
       } else {
         const gp_req_meta m = p.req[slot];
         const int R = m.n_pre_pages * p.P + m.seq_priv;
-        nb = (R + kBlockTok - 1) / kBlockTok;
+        // a shared prefix is attended by prefix_attn_kernel, once per group
+        // of requests sharing it: the attention kernel starts after it
+        const int base = (count && p.prefix_batch && m.prefix_id >= 0 && m.n_pre_pages > 0)
+                             ? m.n_pre_pages * p.P : 0;
+        nb = (R - base + kBlockTok - 1) / kBlockTok;
         if (nb < 1) nb = 1;
+        p.plan_base[i] = base;
         const bool at_b = m.seq_priv == m.n_pages * p.P;
         int flags = 0;
         if (at_b) flags |= kPlanBoundary;
@@ -196,12 +201,50 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
       p.seginfo[k] = make_int4(wf, wl, s_wblk[wf] != sb ? 1 : 0, 0);
     }
   }
+  // Shared-prefix units: the step's requests grouped by prefix (pmem, in an
+  // arbitrary order inside a group: each member's result is its own), then
+  // per prefix ceil(members / kPrefChunk) chunks x Hk heads x ranges of
+  // kPrefRangeBlocks blocks, laid end to end (unit_cum).
+  __shared__ int s_pcnt[kMaxPrefixBatch];
+  int punits = 0;
+  const bool batch = count && p.prefix_batch && !s_bad && n > 0;
+  if (batch) {
+    const int np = p.max_prefixes;  // <= kMaxPrefixBatch when batching is on
+    for (int k = threadIdx.x; k < np; k += blockDim.x) s_pcnt[k] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x)
+      if (p.plan_base[i] > 0) p.pranges[i] = atomicAdd(&s_pcnt[p.req[p.plan_slot[i]].prefix_id], 1);
+    __syncthreads();
+    int tot_m, tot_u;
+    const int k = threadIdx.x;  // np <= blockDim.x
+    const int cnt = k < np ? s_pcnt[k] : 0;
+    const int nr = (k < np && cnt) ? (p.prefix[k].len / kBlockTok + kPrefRangeBlocks - 1) / kPrefRangeBlocks : 0;
+    const int units = cnt ? ((cnt + kPrefChunk - 1) / kPrefChunk) * p.Hk * nr : 0;
+    const int off = block_excl_scan(cnt, s_warp, &tot_m);
+    const int uoff = block_excl_scan(units, s_warp, &tot_u);
+    if (k < np) { p.pref_off[k] = off; p.pref_cnt[k] = cnt; p.unit_cum[k] = uoff; }
+    if (k == 0) p.unit_cum[np] = tot_u;
+    punits = tot_u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      if (p.plan_base[i] > 0) {
+        const int pid = p.req[p.plan_slot[i]].prefix_id;
+        p.pmem[p.pref_off[pid] + p.pranges[i]] = i;
+        p.pranges[i] = (p.prefix[pid].len / kBlockTok + kPrefRangeBlocks - 1) / kPrefRangeBlocks;
+      } else {
+        p.pranges[i] = 0;
+      }
+    }
+  } else if (count && !s_bad && p.prefix_batch) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) p.pranges[i] = 0;
+  }
   if (threadIdx.x == 0) {
     p.plan_cum[n] = carry;
     const int good = s_bad ? 0 : n;
     p.plan_misc[0] = good;
     p.plan_misc[1] = s_bad ? 0 : bcarry;
     p.plan_misc[2] = carry;
+    p.plan_misc[3] = punits;
     if (count) {  // a rejected step (bad slot list) is not counted
       p.ctrl->plan_n = good;
       if (!s_bad) {

@@ -352,7 +352,7 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
  *     next layer): the step's outputs and decisions do not change;
  *   - the per-call scratch (the step plan of the n requests and the start
  *     cursor and first block of every attention worker) lives in a file-scope
- *     device array of this library, about 155 KB, which every GPU that loads the library
+ *     device array of this library, about 160 KB, which every GPU that loads the library
  *     keeps until the process exits; nothing of it needs clearing, as each
  *     call writes all the scratch it reads;
  *   - n may not exceed 1024 (GP_ERR_INVALID with a message otherwise);
