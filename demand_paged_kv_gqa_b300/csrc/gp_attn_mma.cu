@@ -455,28 +455,44 @@ __device__ __forceinline__ void finish_mma(const PoolDev& p, int i, int h,
 // written to lgX[t0 + token] for tokens below nvalid when `score`), the
 // online softmax of the G head rows (running max m, sum l, log2 domain) and
 // O^T += V^T · P^T into o.
-template <int G>
-__device__ __forceinline__ void attend_block(const uint32_t (&afr)[8][4], float (&o)[8][4], float& m,
-                                             float& l, uint32_t sK, int t0, int nvalid, bool score,
-                                             float* lgX, int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  const bool head_row = g < G;
+// This lane's shared-memory offsets (inside a ring stage) of the 16
+// ldmatrix loads of one block: [0..7] the keys, [8..15] the values.  They
+// depend on the lane only, so a kernel computes them once.
+struct LdsmOffsets {
+  uint32_t k[8], v[8];
+};
+__device__ __forceinline__ LdsmOffsets ldsm_offsets(int lane) {
   const int mi = lane >> 3, ri = lane & 7;
   const int k_tok = 8 * (mi >> 1) + ri, k_half = mi & 1;   // K: token, chunk parity
   // V^T as the 16 x 16 operand (rows: dims, columns: tokens), by transposing
   // loads of V[token][dims]: matrices (tokens 0-7 | 8-15) x (dims +0 | +8)
   const int v_tok = 8 * (mi >> 1) + ri, v_half = mi & 1;
+  LdsmOffsets o;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const int ch = 2 * kk + k_half;   // 16-byte chunk of the key row
+    o.k[kk] = (uint32_t)((ch >> 3) * 2048) + swz(k_tok, ch & 7);
+    const int cv = 2 * kk + v_half;   // 16-byte chunk = 8 dims
+    o.v[kk] = 4096u + (uint32_t)((cv >> 3) * 2048) + swz(v_tok, cv & 7);
+  }
+  return o;
+}
+
+template <int G>
+__device__ __forceinline__ void attend_block(const uint32_t (&afr)[8][4], float (&o)[8][4], float& m,
+                                             float& l, uint32_t sK, int t0, int nvalid, bool score,
+                                             float* lgX, const LdsmOffsets& lo, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  const bool head_row = g < G;
   // the lane whose softmax weights feed this lane's weight column: column
   // n < G is head n (hi part), G <= n < 2G is head n - G (lo part)
   const int p_src = ((g >= G && g < 2 * G) ? (g - G) : g) * 4 + t;
-  const uint32_t sV = sK + 4096;
   // ---- scores: S[16 rows][16 tokens] = A · K^T
   float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const int ch = 2 * kk + k_half;   // 16-byte chunk of the key row
     uint32_t b[4];
-    ldsm_x4(b, sK + (ch >> 3) * 2048 + swz(k_tok, ch & 7));
+    ldsm_x4(b, sK + lo.k[kk]);
     mma_bf16(c0, afr[kk], b[0], b[1]);
     mma_bf16(c1, afr[kk], b[2], b[3]);
   }
@@ -542,9 +558,8 @@ __device__ __forceinline__ void attend_block(const uint32_t (&afr)[8][4], float 
   // ---- O^T += V^T · P^T, 16 dims at a time
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    const int ch = 2 * mt + v_half;   // 16-byte chunk = 8 dims
     uint32_t a[4];
-    ldsm_x4_t(a, sV + (ch >> 3) * 2048 + swz(v_tok, ch & 7));
+    ldsm_x4_t(a, sK + lo.v[mt]);
     mma_bf16(o[mt], a, bp0, bp1);
   }
 }
@@ -712,6 +727,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   while (pitems < S && emit(true)) {}
 
   const uint32_t ring_u32 = smem_u32(ring);
+  const LdsmOffsets lofs = ldsm_offsets(lane);
 
   bool failed = false;
   int64_t citems = 0;
@@ -776,7 +792,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       if (!wait_item(citems, slot)) { failed = true; break; }
       const uint32_t sK = ring_u32 + (uint32_t)(citems % S) * kMmaStageB;
       const int t0 = pe.tb + (cc.blk + (int)k) * kBlockTok;
-      attend_block<G>(afr, o, m, l, sK, t0, R - t0, score, lgX, lane);
+      attend_block<G>(afr, o, m, l, sK, t0, R - t0, score, lgX, lofs, lane);
       release_item();
     }
     if (failed) break;
@@ -976,6 +992,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int lay
   // q, the summaries and the score rows belong to earlier kernels
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint32_t ring_u32 = smem_u32(ring);
+  const LdsmOffsets lofs = ldsm_offsets(lane);
   int64_t issued = 0, used = 0;  // ring items over the CTA's life (issued: thread 0)
   bool failed = false;
   for (int u = blockIdx.x; u < units && !failed; u += gridDim.x) {
@@ -1091,7 +1108,7 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int lay
       for (int kk = 0; kk < 2; ++kk)
         if (has[kk])  // warp-uniform
           attend_block<G>(afr[kk], o[kk], m[kk], l[kk], sK, t0, 1 << 30,
-                          (mflags[kk] & kPlanScore) != 0, lg[kk], lane);
+                          (mflags[kk] & kPlanScore) != 0, lg[kk], lofs, lane);
       __syncthreads();  // every warp is done with stage s
       ++used;
       if (threadIdx.x == 0 && jb + S < nblk) issue(b0 + jb + S);
