@@ -123,9 +123,10 @@ __device__ __forceinline__ uint32_t swz(int r, int lc) {
 __device__ __forceinline__ void issue_block_tma(const PoolDev& p, const CUtensorMap* map, int layer,
                                                 const Cursor& c, int page, uint8_t* stage,
                                                 uint64_t* bar) {
-  const int t0 = c.blk * kBlockTok;
+  const int t0 = c.base + c.blk * kBlockTok;  // resident token of the block's first row
+  const int in_page = p.P_log2 >= 0 ? (t0 & (p.P - 1)) : t0 % p.P;
   // row of the pool viewed as [num_pages * L * Hk * 2 * P][d]
-  const int row = (((page * p.L + layer) * p.Hk + c.h) * 2) * p.P + (t0 % p.P);
+  const int row = (((page * p.L + layer) * p.Hk + c.h) * 2) * p.P + in_page;
   mbar_expect_tx(bar, kMmaStageB);
   tma_load_2d(stage, map, 0, row, bar);
   tma_load_2d(stage + 2048, map, 64, row, bar);
@@ -146,9 +147,11 @@ constexpr int kMetaV = 1344;    // the step's new value, bf16
 constexpr int kMetaS = 1600;    // short and long summary before this step, fp32
 constexpr int kMetaC32 = 2624;  // rotary cos / sin rows of the position, fp32
 constexpr int kMetaS32 = 2880;
-constexpr int kMetaC64 = 3136;  // the same rows in fp64
-constexpr int kMetaS64 = 3648;
-constexpr int kMetaSF = 4352;   // written in place: both summaries after this step's fold
+constexpr int kMetaC32lo = 3136;  // their fp32 residuals (cos, sin: c32 + c32lo ~ fp64)
+constexpr int kMetaS32lo = 3392;
+constexpr int kMetaC64 = 3648;  // the fp64 rows (the rare pairs the fp32 evaluation leaves open)
+constexpr int kMetaS64 = 4160;
+constexpr int kMetaSF = 4672;   // written in place: both summaries after this step's fold
 
 // Per-warp extra buffer (after ob): the staged-token score of each query
 // head and the staged value (fp32), for finishing a piece in place.
@@ -187,6 +190,66 @@ __device__ __forceinline__ PlanEntry plan_at(const PoolDev& p, PlanWin& w, int i
   return e;
 }
 
+// Block-table windows for the producer: the window in use and the one it
+// will need next, loaded when the current one is installed, so that crossing
+// into it (the next 32 pages of a segment, the next head's or the next
+// request's first pages) is a register swap instead of a dependent load.
+struct PageWinAhead {
+  int slot = -1, base = 0, page = 0;     // entries base .. base+31 of slot's table, one per lane
+  int nslot = -1, nbase = 0, npage = 0;  // the expected next window (nslot -1: none)
+};
+
+__device__ __forceinline__ int page_index(const PoolDev& p, int tok) {
+  return p.P_log2 >= 0 ? (tok >> p.P_log2) : tok / p.P;
+}
+
+__device__ __forceinline__ int load_window(const PoolDev& p, int slot, int base, int lane) {
+  const int e = base + lane;
+  return e < p.block_width ? p.block[(size_t)slot * p.block_width + e] : 0;
+}
+
+// The window the cursor's walk needs after (c.slot, base): the segment's next
+// 32 pages; else the next head's first window (the same table) unless it is
+// this one; else the next request's first window, when its plan entry is in
+// the plan window w.  False when unknown.  Warp-uniform.
+__device__ __forceinline__ bool next_window(const PoolDev& p, const PlanWin& w, const Cursor& c,
+                                            int base, int n, int& nslot, int& nbase) {
+  const int last = page_index(p, c.base + (c.nb - 1) * kBlockTok);
+  if (base + 32 <= last) { nslot = c.slot; nbase = base + 32; return true; }
+  const int first = page_index(p, c.base);
+  if (c.h + 1 < p.Hk && first != base) { nslot = c.slot; nbase = first; return true; }
+  const int i1 = c.i + 1;
+  if (i1 >= n || i1 < w.base || i1 >= w.base + 32) return false;
+  nslot = __shfl_sync(0xffffffffu, w.slot, i1 - w.base);
+  nbase = page_index(p, __shfl_sync(0xffffffffu, w.tb, i1 - w.base));
+  return true;
+}
+
+// Page id of the cursor's block; all lanes call it with the same cursor.
+__device__ __forceinline__ int page_of_ahead(const PoolDev& p, PageWinAhead& win, const PlanWin& w,
+                                             const Cursor& c, int n, int lane) {
+  const int pidx = page_index(p, c.base + c.blk * kBlockTok);  // prefix pages first, then private
+  if (c.slot != win.slot || pidx < win.base || pidx >= win.base + 32) {
+    if (c.slot == win.nslot && pidx >= win.nbase && pidx < win.nbase + 32) {
+      win.slot = win.nslot; win.base = win.nbase; win.page = win.npage;
+    } else {
+      win.slot = c.slot; win.base = pidx; win.page = load_window(p, c.slot, pidx, lane);
+    }
+    int ns, nb;
+    if (next_window(p, w, c, win.base, n, ns, nb)) {
+      win.nslot = ns; win.nbase = nb; win.npage = load_window(p, ns, nb, lane);
+    } else {
+      win.nslot = -1;
+    }
+  }
+  int page = __shfl_sync(0xffffffffu, win.page, pidx - win.base);
+  if ((unsigned)page >= (unsigned)p.num_pages) {
+    if (lane == 0) set_status(p, GP_ST_BAD_PAGE, c.slot);
+    page = 0;
+  }
+  return page;
+}
+
 __device__ __forceinline__ void walk_next(const PoolDev& p, PlanWin& w, Cursor& c, int n, int lane) {
   if (++c.blk == c.nb) {
     c.blk = 0;
@@ -208,7 +271,7 @@ __device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, i
                                            const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
                                            uint8_t* st, uint64_t* bar) {
   constexpr int D = kMmaD;
-  const uint32_t bytes = G * D * 2 + 2 * D * 2 + 2 * D * 4 + (p.rope ? D * 4 + D * 8 : 0);
+  const uint32_t bytes = G * D * 2 + 2 * D * 2 + 2 * D * 4 + (p.rope ? 2 * D * 4 + D * 8 : 0);
   mbar_expect_tx(bar, bytes);
 #pragma unroll
   for (int g = 0; g < G; ++g)
@@ -219,6 +282,8 @@ __device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, i
   if (p.rope) {
     bulk_g2s(st + kMetaC32, p.cos32 + (size_t)pos * (D / 2), D * 2, bar);
     bulk_g2s(st + kMetaS32, p.sin32 + (size_t)pos * (D / 2), D * 2, bar);
+    bulk_g2s(st + kMetaC32lo, p.cos32lo + (size_t)pos * (D / 2), D * 2, bar);
+    bulk_g2s(st + kMetaS32lo, p.sin32lo + (size_t)pos * (D / 2), D * 2, bar);
     bulk_g2s(st + kMetaC64, p.cos64 + (size_t)pos * (D / 2), D * 4, bar);
     bulk_g2s(st + kMetaS64, p.sin64 + (size_t)pos * (D / 2), D * 4, bar);
   }
@@ -232,7 +297,9 @@ struct PieceIn {
   const float* s;          // [2][d] before this step
   const float* c32;
   const float* s32;
-  const double* c64;
+  const float* c32lo;      // fp32 residuals of the rotary rows
+  const float* s32lo;
+  const double* c64;       // the fp64 rotary rows
   const double* s64;
   const float* sf;         // [2][d] after this step's fold (set when needed)
 };
@@ -367,21 +434,53 @@ __device__ void segment_duties(const PoolDev& p, int layer, int i, int h, int sl
   load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(in.k), sigma, kst);
   load_row<__nv_bfloat16, Gm>(reinterpret_cast<const uint8_t*>(in.v), sigma, vraw);
   if (p.rope) {
+    // x·c - y·s and y·c + x·s rounded once to bf16, as in fp64.  The lane
+    // slice sigma holds 8 pairs (dims 8·sigma + e and +64, e < 8); lane
+    // (grp, sigma) rotates pairs 2·grp and 2·grp + 1 -- by the certified fp32
+    // evaluation, or the fp64 expression for a pair it leaves open -- and the
+    // 8 results are gathered from the lanes (e / 2, sigma) by shuffles.
+    static_assert(H2 == 8, "8 rotate-half pairs per lane slice");
+    uint32_t rot[2];
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+      float x = kst[jj], y = kst[jj + H2];
+#pragma unroll
+      for (int g2 = 1; g2 < 4; ++g2)
+        if (grp == g2) { x = kst[2 * g2 + jj]; y = kst[2 * g2 + jj + H2]; }
+      const int di = 8 * sigma + 2 * grp + jj;
+      const float c1 = in.c32[di], c2 = in.c32lo[di], s1 = in.s32[di], s2 = in.s32lo[di];
+      uint16_t ra, rb;
+      if (!(rope_bf16_certified(x, y, c1, c2, -s1, -s2, ra) &&
+            rope_bf16_certified(y, x, c1, c2, s1, s2, rb))) {
+        const double c = in.c64[di], sn = in.s64[di];
+        const double xd = (double)x, yd = (double)y;
+        ra = f64_to_bf16_rne(__dsub_rn(__dmul_rn(xd, c), __dmul_rn(yd, sn)));
+        rb = f64_to_bf16_rne(__dadd_rn(__dmul_rn(yd, c), __dmul_rn(xd, sn)));
+      }
+      rot[jj] = (uint32_t)ra | ((uint32_t)rb << 16);
+    }
 #pragma unroll
     for (int e = 0; e < H2; ++e) {
-      const int di = dim_of<Gm>(e, sigma);
-      const double c = in.c64[di], s = in.s64[di];
-      const double x = (double)kst[e], y = (double)kst[e + H2];
-      const double ra = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, s));
-      const double rb = __dadd_rn(__dmul_rn(y, c), __dmul_rn(x, s));
-      kst[e] = __uint_as_float((uint32_t)f64_to_bf16_rne(ra) << 16);
-      kst[e + H2] = __uint_as_float((uint32_t)f64_to_bf16_rne(rb) << 16);
+      const uint32_t v = __shfl_sync(0xffffffffu, rot[e & 1], (e >> 1) * 8 + sigma);
+      kst[e] = __uint_as_float(v << 16);
+      kst[e + H2] = __uint_as_float(v & 0xffff0000u);
     }
   }
   if (grp == 0) {
-    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(p.staging) + srow * D;
-    store_row<__nv_bfloat16, Gm>(st, sigma, kst);  // exact: already on the bf16 grid
-    store_row<__nv_bfloat16, Gm>(st + D, sigma, vraw);
+    // both rows with 16-byte stores: elements 8c .. 8c+7 are the 16-byte
+    // chunk c·8 + sigma of the row (all values already on the bf16 grid)
+    uint8_t* st = p.staging + srow * D * 2;
+#pragma unroll
+    for (int c = 0; c < Gm::VEC; ++c) {
+      uint32_t wk[4], wv[4];
+#pragma unroll
+      for (int k2 = 0; k2 < 4; ++k2) {
+        wk[k2] = (__float_as_uint(kst[c * 8 + 2 * k2]) >> 16) | (__float_as_uint(kst[c * 8 + 2 * k2 + 1]) & 0xffff0000u);
+        wv[k2] = (__float_as_uint(vraw[c * 8 + 2 * k2]) >> 16) | (__float_as_uint(vraw[c * 8 + 2 * k2 + 1]) & 0xffff0000u);
+      }
+      *reinterpret_cast<uint4*>(st + (c * 8 + sigma) * 16) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+      *reinterpret_cast<uint4*>(st + D * 2 + (c * 8 + sigma) * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
 #pragma unroll
     for (int e = 0; e < NE; ++e) obx[4 + dim_of<Gm>(e, sigma)] = vraw[e];
   }
@@ -683,9 +782,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   Cursor pc;
   cursor_start(p, w, pc);
   PlanWin pwin, cwin;
-  PageWin win;
+  PageWinAhead win;
   const int first_seg = pc.i * p.Hk + pc.h;
   const int i_first = pc.i, h_first = pc.h;
+  (void)plan_at(p, pwin, pc.i, n, lane);  // lets the first page window see the next request
   int64_t pblk = start;   // next block to issue
   bool pmeta = false;     // next item is a meta item
   int64_t pitems = 1;     // items issued (item 0, the first meta, comes after the wait)
@@ -702,7 +802,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       }
       pmeta = false;
     } else {
-      const int page = page_of(p, win, pc, lane);
+      const int page = page_of_ahead(p, win, pwin, pc, n, lane);
       if (lane == 0) {
         fence_proxy_async_smem();
         issue_block_tma(p, &kvmap, layer, pc, page, st, &bars[s]);
@@ -767,6 +867,8 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       in.s = reinterpret_cast<const float*>(st + kMetaS);
       in.c32 = reinterpret_cast<const float*>(st + kMetaC32);
       in.s32 = reinterpret_cast<const float*>(st + kMetaS32);
+      in.c32lo = reinterpret_cast<const float*>(st + kMetaC32lo);
+      in.s32lo = reinterpret_cast<const float*>(st + kMetaS32lo);
       in.c64 = reinterpret_cast<const double*>(st + kMetaC64);
       in.s64 = reinterpret_cast<const double*>(st + kMetaS64);
       float* sf = reinterpret_cast<float*>(ring + (citems % S) * kMmaStageB + kMetaSF);
@@ -1072,6 +1174,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int lay
       in.s = reinterpret_cast<const float*>(mb + kPmS);
       in.c32 = reinterpret_cast<const float*>(mb + kPmC32);
       in.s32 = reinterpret_cast<const float*>(mb + kPmS32);
+      in.c32lo = nullptr;
+      in.s32lo = nullptr;
       in.c64 = nullptr;
       in.s64 = nullptr;
       in.sf = reinterpret_cast<float*>(mb + kPmSF);

@@ -169,7 +169,7 @@ void compute_layout(const gp_config* c, gp_layout* l) {
   l->ctrl = take(sizeof(gp_ctrl));
   l->prefix = take((uint64_t)c->max_prefixes * sizeof(gp_prefix_meta));
   l->prefix_pages = take((uint64_t)c->max_prefixes * l->max_prefix_pages * 4);
-  l->rope = take((uint64_t)c->max_seq_len * (D / 2) * (8 + 8 + 4 + 4));
+  l->rope = take((uint64_t)c->max_seq_len * (D / 2) * (8 + 8 + 4 + 4 + 4 + 4));
   l->scratch = off;
   for (int b = 0; b < 2; ++b) {                                // two plan buffers
     for (int k = 0; k < 12; ++k) take((R + 1) * 4);           //   plan arrays
@@ -204,6 +204,9 @@ void fill_dev(gp_pool* p) {
   std::memset(&d, 0, sizeof(d));
   d.L = c.num_layers; d.Hq = c.num_q_heads; d.Hk = c.num_kv_heads; d.D = c.head_dim;
   d.G = c.num_q_heads / c.num_kv_heads; d.P = c.page_size;
+  d.P_log2 = -1;
+  for (int k = 0; k < 31; ++k)
+    if (c.page_size == (1 << k)) d.P_log2 = k;
   d.num_pages = c.num_pages; d.max_req = c.max_requests; d.max_pages_per_req = c.max_pages_per_req;
   d.max_prefixes = c.max_prefixes; d.max_prefix_pages = l.max_prefix_pages;
   d.block_width = l.block_width; d.logit_width = l.logit_width; d.max_seq_len = c.max_seq_len;
@@ -234,6 +237,8 @@ void fill_dev(gp_pool* p) {
   d.sin64 = d.cos64 + tab;
   d.cos32 = (const float*)(d.sin64 + tab);
   d.sin32 = d.cos32 + tab;
+  d.cos32lo = d.sin32 + tab;
+  d.sin32lo = d.cos32lo + tab;
   const uint64_t R = c.max_requests;
   uint64_t off = l.scratch;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = align_up(off + bytes); return b + o; };
@@ -364,11 +369,12 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   cudaError_t e = cudaMemsetAsync(dev_buf, 0, l.total, p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   if (cfg->rope_theta != 0.0) {
-    // fp64 table from the C library (pow, cos, sin); fp32 copies rounded once
+    // fp64 table from the C library (pow, cos, sin); fp32 copies rounded
+    // once, and the fp32 residuals fp32(x64 - x32) (the difference is exact)
     const int H = cfg->head_dim / 2;
     const size_t tab = (size_t)cfg->max_seq_len * H;
     std::vector<double> c64(tab), s64(tab);
-    std::vector<float> c32(tab), s32(tab);
+    std::vector<float> c32(tab), s32(tab), c32lo(tab), s32lo(tab);
     std::vector<double> inv(H);
     for (int i = 0; i < H; ++i) inv[i] = std::pow(cfg->rope_theta, -(2.0 * i) / cfg->head_dim);
     for (int pos = 0; pos < cfg->max_seq_len; ++pos)
@@ -379,12 +385,16 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
         s64[k] = std::sin(a);
         c32[k] = (float)c64[k];
         s32[k] = (float)s64[k];
+        c32lo[k] = (float)(c64[k] - (double)c32[k]);
+        s32lo[k] = (float)(s64[k] - (double)s32[k]);
       }
     const gp::PoolDev& d = p->dev;
     e = cudaMemcpyAsync((void*)d.cos64, c64.data(), tab * 8, cudaMemcpyHostToDevice, p->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin64, s64.data(), tab * 8, cudaMemcpyHostToDevice, p->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.cos32, c32.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
     if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin32, s32.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.cos32lo, c32lo.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin32lo, s32lo.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
     if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   }

@@ -29,6 +29,7 @@ constexpr int32_t kPlanScore = 4;     // boundary in GROWPAGE mode: score summar
 struct PoolDev {
   // configuration
   int32_t L, Hq, Hk, D, G, P;
+  int32_t P_log2;         // log2(P) when P is a power of two, else -1
   int32_t num_pages, max_req, max_pages_per_req, max_prefixes, max_prefix_pages;
   int32_t block_width, logit_width, max_seq_len, dtype, mode, recent_window;
   int32_t num_workers;
@@ -54,6 +55,8 @@ struct PoolDev {
   const double* sin64;
   const float* cos32;
   const float* sin32;
+  const float* cos32lo;   // fp32(cos64 - cos32): cos32 + cos32lo carries ~48 bits
+  const float* sin32lo;
   // scratch: per-step plan
   int32_t* plan_slot;     // [max_req] slot of request i
   int32_t* plan_R;        // [max_req] resident tokens (prefix + private)
@@ -160,6 +163,65 @@ __device__ __forceinline__ uint16_t f64_to_bf16_rne(double x) {
   double s = fabs(x) * 0x1p133;
   double r = rint(s);
   return sign | (uint16_t)r;
+}
+
+// One output of a rotate-half RoPE pair for a bf16 key, rounded once to bf16:
+// the value a·c + b·w of bf16 inputs a, b and fp64 table values c, w, as the
+// fp64 expression fl(fl(a·c) + fl(b·w)) followed by f64_to_bf16_rne would give
+// it (w = -s for x·c - y·s, w = s for y·c + x·s), without fp64 arithmetic.
+// c and w arrive as fp32 pairs (c1 + c2, w1 + w2 with c1 = fl32(c),
+// c2 = fl32(c - c1), so |c - c1 - c2| <= 2^-48 |c1|).  With M = |a| + |b|:
+//   - a·c1 = p1 + e1 exactly (Dekker's product via fma), b·w1 = q1 + f1;
+//     s + t = p1 + q1 exactly (Knuth's two-sum);
+//   - lo = t + ((e1 + f1) + (p2 + q2)), p2 = fl(a·c2), q2 = fl(b·w2): four
+//     roundings of terms below 3·2^-24 M, two product roundings and the
+//     dropped c, w residuals keep |s + lo - (a·c + b·w)| <= 9·2^-48 M;
+//   - the fp64 expression is within 2^-52 M (1 + 2^-50) of a·c + b·w.
+// So when s + lo lies more than 2^-44 M = 16·2^-48 M inside the rounding
+// interval of its bf16 neighbour B (distances taken after an exact Sterbenz
+// subtraction and one rounding), the fp64 expression rounds to B as well.
+// Returns false otherwise (that close to a rounding boundary, tiny or huge
+// inputs, non-finite values): the caller evaluates the fp64 expression.
+__device__ __forceinline__ bool rope_bf16_certified(float a, float b, float c1, float c2, float w1,
+                                                    float w2, uint16_t& out) {
+  if (a == 0.f && b == 0.f) {
+    // fl(a·c) and fl(b·w) are zeros carrying the products' signs; their sum
+    // is -0 only when both are -0 (round to nearest)
+    const uint32_t na = (__float_as_uint(a) ^ __float_as_uint(c1)) >> 31;
+    const uint32_t nb = (__float_as_uint(b) ^ __float_as_uint(w1)) >> 31;
+    out = (na & nb) ? 0x8000u : 0u;
+    return true;
+  }
+  const float M = __fadd_rn(fabsf(a), fabsf(b));
+  if (!(M >= 0x1p-60f && M <= 0x1p120f)) return false;  // NaN fails too
+  // a·c1 = p1 + e1 and b·w1 = q1 + f1 exactly; a·c2, b·w2 rounded
+  const float p1 = __fmul_rn(a, c1), e1 = __fmaf_rn(a, c1, -p1);
+  const float q1 = __fmul_rn(b, w1), f1 = __fmaf_rn(b, w1, -q1);
+  const float p2 = __fmul_rn(a, c2), q2 = __fmul_rn(b, w2);
+  // s + t = p1 + q1 exactly
+  const float s = __fadd_rn(p1, q1);
+  const float sb = __fsub_rn(s, p1);
+  const float t = __fadd_rn(__fsub_rn(p1, __fsub_rn(s, sb)), __fsub_rn(q1, sb));
+  const float lo = __fadd_rn(t, __fadd_rn(__fadd_rn(e1, f1), __fadd_rn(p2, q2)));
+  // hi + r = s + lo exactly
+  const float hi = __fadd_rn(s, lo);
+  const float hb_ = __fsub_rn(hi, s);
+  const float r = __fadd_rn(__fsub_rn(s, __fsub_rn(hi, hb_)), __fsub_rn(lo, hb_));
+  const float ah = fabsf(hi);
+  if (!(ah >= 0x1p-100f)) return false;
+  const float ar = hi < 0.f ? -r : r;  // |value| = ah + ar
+  // B: |hi| rounded to nearest-even on the bf16 grid; its two neighbours
+  const uint32_t hbits = __float_as_uint(ah);
+  const uint32_t rb = (hbits + 0x7fffu + ((hbits >> 16) & 1u)) >> 16;
+  const float B = __uint_as_float(rb << 16);
+  const float up = __fmul_rn(__fadd_rn(B, __uint_as_float((rb + 1u) << 16)), 0.5f);
+  const float dn = __fmul_rn(__fadd_rn(B, __uint_as_float((rb - 1u) << 16)), 0.5f);
+  const float margin = __fmul_rn(M, 0x1p-44f);
+  const float d_up = __fsub_rn(__fsub_rn(up, ah), ar);
+  const float d_dn = __fadd_rn(__fsub_rn(ah, dn), ar);
+  if (!(d_up > margin && d_dn > margin)) return false;
+  out = (uint16_t)(rb | (hi < 0.f ? 0x8000u : 0u));
+  return true;
 }
 
 template <typename T> struct ElemIO;

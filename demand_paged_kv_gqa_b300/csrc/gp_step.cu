@@ -1014,7 +1014,9 @@ __global__ void admit_kernel(PoolDev p, int slot, int budget, int prefix_id, int
 
 // Store tokens 0..count-1 of k, v ([L][count][Hk][d], keys not yet rotated)
 // into the pages listed in `pages` (token t -> page t/P, slot t%P), keys
-// rotated to position pos0 + t in fp64 and rounded once to the dtype.
+// rotated to position pos0 + t in fp64 and rounded once to the dtype (bf16:
+// by rope_bf16_certified, which gives the same bits without fp64 arithmetic
+// except for the rare pairs it leaves open).
 template <typename T>
 __global__ void write_tokens_kernel(PoolDev p, const int32_t* pages, const T* k, const T* v,
                                     int count, int pos0) {
@@ -1035,6 +1037,20 @@ __global__ void write_tokens_kernel(PoolDev p, const int32_t* pages, const T* k,
     const T* srcv = v + (((size_t)layer * count + t) * p.Hk + h) * D;
     const int pos = pos0 + t;
     for (int e = lane; e < H; e += 32) {
+      if constexpr (sizeof(T) == 2) {
+        if (p.rope) {  // the certified fp32 evaluation of the fp64 expression below
+          const size_t at = (size_t)pos * H + e;
+          const float x = ElemIO<T>::load(src, e), y = ElemIO<T>::load(src, e + H);
+          const float c1 = p.cos32[at], c2 = p.cos32lo[at], s1 = p.sin32[at], s2 = p.sin32lo[at];
+          uint16_t ra, rb;
+          if (rope_bf16_certified(x, y, c1, c2, -s1, -s2, ra) &&
+              rope_bf16_certified(y, x, c1, c2, s1, s2, rb)) {
+            reinterpret_cast<uint16_t*>(dst)[e] = ra;
+            reinterpret_cast<uint16_t*>(dst)[e + H] = rb;
+            continue;
+          }
+        }
+      }
       const double x = (double)ElemIO<T>::load(src, e), y = (double)ElemIO<T>::load(src, e + H);
       double a = x, b = y;
       if (p.rope) {

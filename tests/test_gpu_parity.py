@@ -389,3 +389,77 @@ def test_twelve_layers(env, mode_name):
     rep = h.run(80)
     _check(rep)
     assert rep.boundaries >= 12
+
+
+def test_key_rotation_bits_equal_fp64_definition(env):
+    # The staged key of a step and the stored prompt keys are rotated to
+    # their positions and rounded once to bf16, bit for bit as the fp64
+    # expression of the oracle gives them.  The kernels evaluate it in fp32
+    # with a certified error bound and fall back to fp64 where the bound
+    # cannot decide the rounding: the inputs mix ordinary keys, pairs with
+    # heavy cancellation (x·c close to y·s), tiny, huge and zero keys (the
+    # fallback), at positions up to 60k.
+    H, gp, synth = env
+    from oracle import numerics as nm
+    L, hq, hk, d, P = 1, 32, 8, 128, 16
+    theta = 500000.0
+    cfg = gp.make_config(num_layers=L, num_q_heads=hq, num_kv_heads=hk, head_dim=d, page_size=P,
+                         num_pages=8192, max_requests=16, max_pages_per_req=4096,
+                         dtype=torch.bfloat16, max_seq_len=65536, rope_theta=theta,
+                         top_p=0.9, recent_window=64)
+    pool = gp.Pool(cfg)
+    rng = np.random.default_rng(20261203)
+    table = nm.RopeTable(theta, d)
+    prompt_lens = [1, 2, 17, 100, 333, 1000, 4097, 9000, 30000, 60000, 5, 64]
+    n = len(prompt_lens)
+    dev = torch.device("cuda")
+
+    def bf16(x):
+        return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+    prompts = []
+    for s, pl in enumerate(prompt_lens):
+        k = bf16(rng.standard_normal((L, pl, hk, d)) * 2.0)
+        v = bf16(rng.standard_normal((L, pl, hk, d)))
+        pool.add_request(s, k.to(dev), v.to(dev), budget_pages=(pl + P - 1) // P + 1)
+        prompts.append(k)
+    pos = [pool.request(s)[0].pos for s in range(n)]
+    h2 = d // 2
+    knew = rng.standard_normal((n, hk, d)).astype(np.float64)
+    knew[1] *= 1e-25                     # tiny: the fp64 fallback
+    knew[2] *= 1e25                      # huge
+    knew[3, :4] = 0.0                    # zero rows, signed zeros
+    knew[3, 4:6] = -0.0
+    knew[3, 6, ::2] = -0.0
+    knew[4, :, ::3] *= 1e-30             # mixed inside a row
+    for s in (5, 6, 7, 8, 9):            # x·c - y·s much smaller than |x| + |y|
+        c, sn = table(pos[s])
+        x = nm.round_bf16(knew[s, :, :h2])
+        ok = np.abs(sn) > 1e-3
+        y = nm.round_bf16(x * c / np.where(ok, sn, 1.0))
+        knew[s, :, :h2] = x
+        knew[s, :, h2:] = np.where(ok, y, knew[s, :, h2:])
+    kd = bf16(knew).to(dev)
+    q = bf16(rng.standard_normal((n, hq, d))).to(dev)
+    v = bf16(rng.standard_normal((n, hk, d))).to(dev)
+    out = torch.empty(n, hq, d, dtype=torch.bfloat16, device=dev)
+    slots = torch.arange(n, dtype=torch.int32, device=dev)
+    pool.decode_step(0, slots, q, kd, v, out)
+    pool.sync()
+    got = pool.region("staging")[:n, 0, :, 0].float().cpu().double().numpy()
+    kin = kd.float().cpu().double().numpy()
+    for s in range(n):
+        want = nm.round_bf16(nm.rope_apply(kin[s], table, pos[s]))
+        bad = np.argwhere(got[s] != want)
+        assert bad.size == 0, f"slot {s} position {pos[s]}: staged key differs at {bad[:4].tolist()}"
+    # the prompt keys in the pages (admission), token t at position t
+    kv = pool.region("kv")
+    for s, pl in enumerate(prompt_lens):
+        m, bt = pool.request(s)
+        pages = torch.as_tensor(bt[m.n_pre_pages: m.n_pre_pages + (pl + P - 1) // P], dtype=torch.long)
+        rows = kv.index_select(0, pages.to(dev))[:, 0, :, 0].float().cpu().double().numpy()
+        stored = rows.transpose(0, 2, 1, 3).reshape(-1, hk, d)[:pl]         # [token][head][d]
+        kp = prompts[s][0].float().double().numpy()
+        for t in sorted({0, min(1, pl - 1), pl // 2, pl - 1}):
+            want = nm.round_bf16(nm.rope_apply(kp[t], table, t))
+            assert np.array_equal(stored[t], want), f"slot {s}: prompt key {t} differs"
