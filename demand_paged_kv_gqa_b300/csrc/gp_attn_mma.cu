@@ -55,6 +55,11 @@ constexpr int kMmaStageB = 8192;           // 16 tokens x (K 4 KiB + V 4 KiB)
 #ifndef GP_MMA_STAGES
 #define GP_MMA_STAGES 3
 #endif
+// 1: the attention kernel merges a cut (request, head) itself, in the piece
+// that completes it last; 0: combine_kernel merges them after the kernel.
+#ifndef GP_INKERNEL_MERGE
+#define GP_INKERNEL_MERGE 0
+#endif
 constexpr int kMmaWarps = GP_MMA_WARPS;
 constexpr int kMmaStages = GP_MMA_STAGES;
 constexpr int kObFloats = 4 * (kMmaD + 2);  // per-warp merge buffer: [G<=4][D] + m + l
@@ -554,6 +559,15 @@ __device__ __forceinline__ void finish_mma(const PoolDev& p, int i, int h,
 // written to lgX[t0 + token] for tokens below nvalid when `score`), the
 // online softmax of the G head rows (running max m, sum l, log2 domain) and
 // O^T += V^T · P^T into o.
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22, flushes subnormal results to 0, 2^-inf = 0).  The softmax weights
+// it produces are split into bf16 hi + lo parts (16 bits) right after.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // This lane's shared-memory offsets (inside a ring stage) of the 16
 // ldmatrix loads of one block: [0..7] the keys, [8..15] the values.  They
 // depend on the lane only, so a kernel computes them once.
@@ -626,7 +640,7 @@ __device__ __forceinline__ void attend_block(const uint32_t (&afr)[8][4], float 
   if (__any_sync(0xffffffffu, mx > m + 8.0f)) {
     float al = 1.0f;
     if (mx > m + 8.0f) {
-      al = exp2f(m - mx);             // 0 when m == -inf
+      al = ex2_approx(m - mx);        // 0 when m == -inf
       l *= al;
       m = mx;
     }
@@ -641,7 +655,7 @@ __device__ __forceinline__ void attend_block(const uint32_t (&afr)[8][4], float 
   float pv[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    pv[u] = (sv[u] == -INFINITY) ? 0.f : exp2f(sv[u] - m);
+    pv[u] = (sv[u] == -INFINITY) ? 0.f : ex2_approx(sv[u] - m);
     l += pv[u];
   }
   uint32_t ph[4], pl[4];
@@ -731,224 +745,18 @@ __device__ __forceinline__ void merge_prefix(const PoolDev& p, int i, int h, flo
 }
 
 // ----------------------------------------------------------- attention ---
-template <int G, int S>
-__global__ void __launch_bounds__(kMmaWarps * 32)
-attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
-                const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ knew,
-                const __nv_bfloat16* __restrict__ vnew, __nv_bfloat16* __restrict__ out) {
-  static_assert(G == 1 || G == 2 || G == 4, "G");
-  constexpr int D = kMmaD;
-  // The stages must start on 1024-byte boundaries (128-byte swizzle).  A
-  // CTA's dynamic shared memory starts 1024-byte aligned when, as here, the
-  // kernel declares no static shared memory; no slack is allocated for it
-  // (that keeps three CTAs per SM), and a misaligned base is reported below
-  // instead of run.
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2;
-  uint8_t* ring = smem + (size_t)warp * S * kMmaStageB;
-  float* ob = reinterpret_cast<float*>(smem + (size_t)kMmaWarps * S * kMmaStageB) + warp * kWarpBufFloats;
-  float* obx = ob + kObFloats;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kMmaWarps * S * kMmaStageB +
-                                               (size_t)kMmaWarps * kWarpBufFloats * 4) + warp * S;
-
-  const int n = p.plan_misc[0];
-  const int64_t Tb = (int64_t)p.plan_misc[2] * p.Hk;
-  const int64_t W = (int64_t)gridDim.x * kMmaWarps;
-  const int64_t Weff = W < Tb ? W : Tb;
-  const int64_t w = (int64_t)blockIdx.x * kMmaWarps + warp;
-  // Programmatic dependent launch: the next kernel in the stream may start
-  // its own prologue now.  Everything before griddepcontrol.wait below reads
-  // only what was final before this step's first attention launch (plan,
-  // block tables, K/V pages).
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (smem_u32(smem_raw) & 1023u) {
-    if (threadIdx.x == 0) set_status(p, GP_ST_SMEM_ALIGN, (int)(smem_u32(smem_raw) & 1023u));
-    return;
-  }
-  if (n <= 0 || w >= Weff) return;  // warp-uniform: warps never synchronise
-  const int64_t start = p.wblk[w], end = p.wblk[w + 1];  // the plan's (weighted) share
-  if (start >= end) return;
-
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-    fence_barrier_init();
-  }
-  __syncwarp();
-
-  // ---- the warp's item sequence: the blocks of its range, with a meta item
-  // in front of every piece.  Item c lives in stage c % S.  Producer state:
-  Cursor pc;
-  cursor_start(p, w, pc);
-  PlanWin pwin, cwin;
-  PageWinAhead win;
-  const int first_seg = pc.i * p.Hk + pc.h;
-  const int i_first = pc.i, h_first = pc.h;
-  (void)plan_at(p, pwin, pc.i, n, lane);  // lets the first page window see the next request
-  int64_t pblk = start;   // next block to issue
-  bool pmeta = false;     // next item is a meta item
-  int64_t pitems = 1;     // items issued (item 0, the first meta, comes after the wait)
-  auto emit = [&](bool allow_meta) -> bool {
-    if (pblk >= end && !pmeta) return false;
-    if (pmeta && !allow_meta) return false;
-    const int s = (int)(pitems % S);
-    uint8_t* st = ring + s * kMmaStageB;
-    if (pmeta) {
-      const PlanEntry e = plan_at(p, pwin, pc.i, n, lane);
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue_meta<G>(p, layer, pc.i, pc.h, e.slot, e.pos, q, knew, vnew, st, &bars[s]);
-      }
-      pmeta = false;
-    } else {
-      const int page = page_of_ahead(p, win, pwin, pc, n, lane);
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        issue_block_tma(p, &kvmap, layer, pc, page, st, &bars[s]);
-      }
-      if (++pblk < end) {
-        walk_next(p, pwin, pc, n, lane);
-        if (pc.blk == 0) pmeta = true;
-      }
-    }
-    ++pitems;
-    return true;
-  };
-  // prologue: blocks only (meta items read this step's inputs)
-  while (pitems < S && emit(false)) {}
-  // The step's inputs, the split-K scratch and the outputs belong to earlier
-  // kernels: wait for them.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  {
-    const PlanEntry e = plan_at(p, pwin, i_first, n, lane);
-    if (lane == 0) issue_meta<G>(p, layer, i_first, h_first, e.slot, e.pos, q, knew, vnew, ring, &bars[0]);
-  }
-  while (pitems < S && emit(true)) {}
-
-  const uint32_t ring_u32 = smem_u32(ring);
-  const LdsmOffsets lofs = ldsm_offsets(lane);
-
-  bool failed = false;
-  int64_t citems = 0;
-  auto wait_item = [&](int64_t c, int slot) -> bool {
-    const int s = (int)(c % S);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[s], (uint32_t)((c / S) & 1),
-                                                              kWaitLimitNs));
-    if (!ok && lane == 0) set_status(p, GP_ST_TIMEOUT, slot);
-    return ok;
-  };
-  auto release_item = [&]() {
-    __syncwarp();
-    ++citems;
-    if (pitems < citems + S) emit(true);
-  };
-
-  Cursor cc;
-  cursor_start(p, w, cc);
-  int64_t j = start;
-  while (j < end && !failed) {
-    const int i = cc.i, h = cc.h, slot = cc.slot, nb = cc.nb;
-    const int64_t len = ((int64_t)(nb - cc.blk) < end - j) ? (int64_t)(nb - cc.blk) : end - j;
-    const bool full = (cc.blk == 0) && (len == nb);
-    const PlanEntry pe = plan_at(p, cwin, i, n, lane);
-    const int R = pe.R;
-    const bool score = (pe.flags & kPlanScore) != 0;
-
-    // ---- operand rows, and the once-per-(request, head) duties
-    uint32_t afr[8][4];
-    {
-      if (!wait_item(citems, slot)) { failed = true; break; }
-      const uint8_t* st = ring + (citems % S) * kMmaStageB;
-      PieceIn in;
-      in.q = reinterpret_cast<const __nv_bfloat16*>(st + kMetaQ);
-      in.k = reinterpret_cast<const __nv_bfloat16*>(st + kMetaK);
-      in.v = reinterpret_cast<const __nv_bfloat16*>(st + kMetaV);
-      in.s = reinterpret_cast<const float*>(st + kMetaS);
-      in.c32 = reinterpret_cast<const float*>(st + kMetaC32);
-      in.s32 = reinterpret_cast<const float*>(st + kMetaS32);
-      in.c32lo = reinterpret_cast<const float*>(st + kMetaC32lo);
-      in.s32lo = reinterpret_cast<const float*>(st + kMetaS32lo);
-      in.c64 = reinterpret_cast<const double*>(st + kMetaC64);
-      in.s64 = reinterpret_cast<const double*>(st + kMetaS64);
-      float* sf = reinterpret_cast<float*>(ring + (citems % S) * kMmaStageB + kMetaSF);
-      in.sf = sf;
-      if (score || cc.blk == 0) {  // the folded summaries are needed
-        fold_rows<G>(p, in, pe.flags, lane, sf);
-        __syncwarp();
-      }
-      build_rows<G>(p, in, pe.flags, lane, afr);
-      if (cc.blk == 0) segment_duties<G>(p, layer, i, h, slot, pe.flags, in, obx, lane);
-      release_item();
-    }
-    float* lgS = p.logits + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * p.logit_width;
-    float* lgX = lgS + (g & 1) * p.logit_width;
-
-    float m = -INFINITY, l = 0.f;
-    // O^T: o[mt][0..1] = dims 16mt + g, columns 2t, 2t+1; o[mt][2..3] = dims + 8
-    float o[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-    for (int64_t k = 0; k < len; ++k, ++j) {
-      if (!wait_item(citems, slot)) { failed = true; break; }
-      const uint32_t sK = ring_u32 + (uint32_t)(citems % S) * kMmaStageB;
-      const int t0 = pe.tb + (cc.blk + (int)k) * kBlockTok;
-      attend_block<G>(afr, o, m, l, sK, t0, R - t0, score, lgX, lofs, lane);
-      release_item();
-    }
-    if (failed) break;
-
-    // ---- piece totals into the warp buffer: ob[g][dim], m[g], l[g]
-    piece_totals<G>(o, m, l, ob, lane);
-    __syncwarp();
-    if (full) {
-      merge_prefix<G>(p, i, h, ob, lane);  // the shared prefix, attended beforehand
-      finish_mma<G>(p, i, h, out, ob, obx, lane);
-    } else {
-      // a cut (request, head): leave this piece's state for combine_kernel
-      const int seg = i * p.Hk + h;
-      const int pslot = (seg == first_seg) ? 0 : 1;
-      constexpr int PW = G * (D + 4);  // per head: D outputs, m, l, 2 pad (16-byte rows)
-      float* part = p.partials + (size_t)(w * 2 + pslot) * PW;
-      for (int x = lane; x < G * D; x += 32) part[(x / D) * (D + 4) + (x % D)] = ob[x];
-      if (lane < 2 * G) part[(lane % G) * (D + 4) + D + lane / G] = ob[G * D + lane];
-    }
-    __syncwarp();  // the buffers are reused by the next piece
-    if (j < end) {  // next piece: block 0 of the following (request, head)
-      cc.blk = cc.nb - 1;
-      walk_next(p, cwin, cc, n, lane);
-    }
-  }
-  if (failed) {
-    // let the copies this warp has in flight land before the CTA may exit
-    for (int64_t c = citems; c < pitems; ++c)
-      (void)mbar_wait_bounded(&bars[c % S], (uint32_t)((c / S) & 1), kWaitLimitNs);
-  }
-}
-
-// ------------------------------------------------------------- combine ---
+// ------------------------------------------------------ cut segments ---
 //
-// One warp per (request, kv head) of the step.  A (request, head) whose
-// blocks were cut between several attention workers is merged here: the
-// workers' states (m, l, unnormalised output per query head) are combined
-// with weights 2^(m_k - max m), then finished like an uncut one.  Runs after
-// the attention kernel has completed, so no worker waits for another.
+// The output of a cut (request, head) from its pieces' states (workers
+// w_first .. w_last of si), its shared-prefix range states and the staged
+// token: the states are combined with weights 2^(m_k - max m), then the
+// staged token is merged in and the result normalised and stored.  Every
+// state must be final and visible (the caller orders it).
 template <int G>
-__global__ void __launch_bounds__(kSmallWarps * 32)
-combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
+__device__ __forceinline__ void merge_segment(const PoolDev& p, int layer, int i, int h, int slot,
+                                              int4 si, __nv_bfloat16* __restrict__ out, int lane) {
   constexpr int D = kMmaD, PW = G * (D + 4);
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // which workers cut this (request, head): from the plan, final before the step
-  const int n = p.plan_misc[0];
-  const int gw = blockIdx.x * kSmallWarps + warp;
-  if (gw >= n * p.Hk) return;
-  const int i = gw / p.Hk, h = gw % p.Hk;
-  const int slot = p.plan_slot[i];
-  const int4 si = p.seginfo[gw];   // first and last worker of this (request, head)
   const int64_t w_first = si.x, w_last = si.y;
-  if (w_first == w_last) return;  // finished by the attention kernel
   const bool first_is_second = si.z != 0;  // the first worker's second state slot
   const int nparts = (int)(w_last - w_first + 1);
   auto part_of = [&](int k) -> const float* {
@@ -956,17 +764,15 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
     const int ps = (k == 0 && first_is_second) ? 1 : 0;
     return p.partials + (size_t)(wk * 2 + ps) * PW;
   };
-  // the workers' states and the staged token come from earlier kernels
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   // every lane holds dims 4*lane .. 4*lane+3 of each head: 16-byte loads of
   // the states, 8-byte loads and stores of the bf16 rows
   const size_t srow = (((size_t)slot * p.L + layer) * p.Hk + h) * 2;
-  const uint2 vraw = reinterpret_cast<const uint2*>(p.staging + (srow + 1) * D * 2)[lane];
+  const uint2 vraw = __ldcg(reinterpret_cast<const uint2*>(p.staging + (srow + 1) * D * 2) + lane);
   const float vs[4] = {__uint_as_float(vraw.x << 16), __uint_as_float(vraw.x & 0xffff0000u),
                        __uint_as_float(vraw.y << 16), __uint_as_float(vraw.y & 0xffff0000u)};
   float sst[G];
 #pragma unroll
-  for (int g = 0; g < G; ++g) sst[g] = p.sstage[(i * p.Hk + h) * 4 + g];
+  for (int g = 0; g < G; ++g) sst[g] = __ldcg(p.sstage + (i * p.Hk + h) * 4 + g);
   float mmax[G], lsum[G], acc[G][4];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -1032,6 +838,255 @@ combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
     wv.y = *reinterpret_cast<const uint32_t*>(&hi);
     reinterpret_cast<uint2*>(out + ((size_t)i * p.Hq + h * G + g) * D)[lane] = wv;
   }
+}
+
+template <int G, int S>
+__global__ void __launch_bounds__(kMmaWarps * 32)
+attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
+                const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ knew,
+                const __nv_bfloat16* __restrict__ vnew, __nv_bfloat16* __restrict__ out) {
+  static_assert(G == 1 || G == 2 || G == 4, "G");
+  constexpr int D = kMmaD;
+  // The stages must start on 1024-byte boundaries (128-byte swizzle).  A
+  // CTA's dynamic shared memory starts 1024-byte aligned when, as here, the
+  // kernel declares no static shared memory; no slack is allocated for it
+  // (that keeps three CTAs per SM), and a misaligned base is reported below
+  // instead of run.
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  uint8_t* ring = smem + (size_t)warp * S * kMmaStageB;
+  float* ob = reinterpret_cast<float*>(smem + (size_t)kMmaWarps * S * kMmaStageB) + warp * kWarpBufFloats;
+  float* obx = ob + kObFloats;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kMmaWarps * S * kMmaStageB +
+                                               (size_t)kMmaWarps * kWarpBufFloats * 4) + warp * S;
+
+  const int n = p.plan_misc[0];
+  const int64_t Tb = (int64_t)p.plan_misc[2] * p.Hk;
+  const int64_t W = (int64_t)gridDim.x * kMmaWarps;
+  const int64_t Weff = W < Tb ? W : Tb;
+  const int64_t w = (int64_t)blockIdx.x * kMmaWarps + warp;
+  // Programmatic dependent launch: the next kernel in the stream may start
+  // its own prologue now.  Everything before griddepcontrol.wait below reads
+  // only what was final before this step's first attention launch (plan,
+  // block tables, K/V pages).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_status(p, GP_ST_SMEM_ALIGN, (int)(smem_u32(smem_raw) & 1023u));
+    return;
+  }
+  if (n <= 0 || w >= Weff) return;  // warp-uniform: warps never synchronise
+  const int start = p.wblk[w], end = p.wblk[w + 1];  // the plan's (weighted) share
+  if (start >= end) return;
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  // ---- the warp's item sequence: the blocks of its range, with a meta item
+  // in front of every piece.  Item c lives in stage c % S.  Producer state:
+  Cursor pc;
+  cursor_start(p, w, pc);
+  PlanWin pwin, cwin;
+  PageWinAhead win;
+  const int first_seg = pc.i * p.Hk + pc.h;
+  const int i_first = pc.i, h_first = pc.h;
+  (void)plan_at(p, pwin, pc.i, n, lane);  // lets the first page window see the next request
+  int pblk = start;       // next block to issue
+  bool pmeta = false;     // next item is a meta item
+  // Ring bookkeeping in 32 bits: the producer's next stage ps; items issued
+  // and not yet released (item 0, the first meta, is reserved: it is issued
+  // after the wait); the consumer's stage cs and phase cph.
+  int ps = 1, inflight = 1;
+  auto emit = [&](bool allow_meta) -> bool {
+    if (pblk >= end && !pmeta) return false;
+    if (pmeta && !allow_meta) return false;
+    const int s = ps;
+    uint8_t* st = ring + s * kMmaStageB;
+    if (pmeta) {
+      const PlanEntry e = plan_at(p, pwin, pc.i, n, lane);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue_meta<G>(p, layer, pc.i, pc.h, e.slot, e.pos, q, knew, vnew, st, &bars[s]);
+      }
+      pmeta = false;
+    } else {
+      const int page = page_of_ahead(p, win, pwin, pc, n, lane);
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        issue_block_tma(p, &kvmap, layer, pc, page, st, &bars[s]);
+      }
+      if (++pblk < end) {
+        walk_next(p, pwin, pc, n, lane);
+        if (pc.blk == 0) pmeta = true;
+      }
+    }
+    ps = (ps + 1 == S) ? 0 : ps + 1;
+    ++inflight;
+    return true;
+  };
+  // prologue: blocks only (meta items read this step's inputs)
+  while (inflight < S && emit(false)) {}
+  // The step's inputs, the split-K scratch and the outputs belong to earlier
+  // kernels: wait for them.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  {
+    const PlanEntry e = plan_at(p, pwin, i_first, n, lane);
+    if (lane == 0) issue_meta<G>(p, layer, i_first, h_first, e.slot, e.pos, q, knew, vnew, ring, &bars[0]);
+  }
+  while (inflight < S && emit(true)) {}
+
+  const uint32_t ring_u32 = smem_u32(ring);
+  const LdsmOffsets lofs = ldsm_offsets(lane);
+
+  bool failed = false;
+  int cs = 0;         // the consumer's stage
+  uint32_t cph = 0;   // and its phase
+  auto wait_item = [&](int slot) -> bool {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[cs], cph, kWaitLimitNs));
+    if (!ok && lane == 0) set_status(p, GP_ST_TIMEOUT, slot);
+    return ok;
+  };
+  auto release_item = [&]() {
+    __syncwarp();
+    if (++cs == S) { cs = 0; cph ^= 1u; }
+    --inflight;
+    if (inflight < S) emit(true);
+  };
+
+  Cursor cc;
+  cursor_start(p, w, cc);
+  int j = start;
+  while (j < end && !failed) {
+    const int i = cc.i, h = cc.h, slot = cc.slot, nb = cc.nb;
+    const int len = (nb - cc.blk < end - j) ? nb - cc.blk : end - j;
+    const bool full = (cc.blk == 0) && (len == nb);
+    const PlanEntry pe = plan_at(p, cwin, i, n, lane);
+    const int R = pe.R;
+    const bool score = (pe.flags & kPlanScore) != 0;
+#if GP_INKERNEL_MERGE
+    // the (request, head)'s first and last worker, used only when this piece
+    // is cut (plan data: loaded now, read at the piece's end)
+    const int4 seg_si = full ? make_int4(0, 0, 0, 0) : p.seginfo[i * p.Hk + h];
+#endif
+
+    // ---- operand rows, and the once-per-(request, head) duties
+    uint32_t afr[8][4];
+    {
+      if (!wait_item(slot)) { failed = true; break; }
+      const uint8_t* st = ring + cs * kMmaStageB;
+      PieceIn in;
+      in.q = reinterpret_cast<const __nv_bfloat16*>(st + kMetaQ);
+      in.k = reinterpret_cast<const __nv_bfloat16*>(st + kMetaK);
+      in.v = reinterpret_cast<const __nv_bfloat16*>(st + kMetaV);
+      in.s = reinterpret_cast<const float*>(st + kMetaS);
+      in.c32 = reinterpret_cast<const float*>(st + kMetaC32);
+      in.s32 = reinterpret_cast<const float*>(st + kMetaS32);
+      in.c32lo = reinterpret_cast<const float*>(st + kMetaC32lo);
+      in.s32lo = reinterpret_cast<const float*>(st + kMetaS32lo);
+      in.c64 = reinterpret_cast<const double*>(st + kMetaC64);
+      in.s64 = reinterpret_cast<const double*>(st + kMetaS64);
+      float* sf = reinterpret_cast<float*>(ring + cs * kMmaStageB + kMetaSF);
+      in.sf = sf;
+      if (score || cc.blk == 0) {  // the folded summaries are needed
+        fold_rows<G>(p, in, pe.flags, lane, sf);
+        __syncwarp();
+      }
+      build_rows<G>(p, in, pe.flags, lane, afr);
+      if (cc.blk == 0) segment_duties<G>(p, layer, i, h, slot, pe.flags, in, obx, lane);
+      release_item();
+    }
+    float* lgS = p.logits + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * p.logit_width;
+    float* lgX = lgS + (g & 1) * p.logit_width;
+
+    float m = -INFINITY, l = 0.f;
+    // O^T: o[mt][0..1] = dims 16mt + g, columns 2t, 2t+1; o[mt][2..3] = dims + 8
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    for (int k = 0; k < len; ++k, ++j) {
+      if (!wait_item(slot)) { failed = true; break; }
+      const uint32_t sK = ring_u32 + (uint32_t)cs * kMmaStageB;
+      const int t0 = pe.tb + (cc.blk + (int)k) * kBlockTok;
+      attend_block<G>(afr, o, m, l, sK, t0, R - t0, score, lgX, lofs, lane);
+      release_item();
+    }
+    if (failed) break;
+
+    // ---- piece totals into the warp buffer: ob[g][dim], m[g], l[g]
+    piece_totals<G>(o, m, l, ob, lane);
+    __syncwarp();
+    if (full) {
+      merge_prefix<G>(p, i, h, ob, lane);  // the shared prefix, attended beforehand
+      finish_mma<G>(p, i, h, out, ob, obx, lane);
+    } else {
+      // a cut (request, head): leave this piece's state for combine_kernel
+      const int seg = i * p.Hk + h;
+      const int pslot = (seg == first_seg) ? 0 : 1;
+      constexpr int PW = G * (D + 4);  // per head: D outputs, m, l, 2 pad (16-byte rows)
+      float* part = p.partials + (size_t)(w * 2 + pslot) * PW;
+      for (int x = lane; x < G * D; x += 32) part[(x / D) * (D + 4) + (x % D)] = ob[x];
+      if (lane < 2 * G) part[(lane % G) * (D + 4) + D + lane / G] = ob[G * D + lane];
+#if GP_INKERNEL_MERGE
+      // The piece that completes its (request, head) last merges all of them
+      // (each piece: state stored, fence, count).  The count goes back to 0
+      // for the next layer; the next kernel in the stream orders that.
+      __syncwarp();
+      __threadfence();
+      int last = 0;
+      if (lane == 0) {
+        const int pieces = seg_si.y - seg_si.x + 1;
+        last = atomicAdd(&p.seg_count[seg], 1) == pieces - 1;
+        if (last) p.seg_count[seg] = 0;
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        merge_segment<G>(p, layer, i, h, slot, seg_si, out, lane);
+      }
+#endif
+    }
+    __syncwarp();  // the buffers are reused by the next piece
+    if (j < end) {  // next piece: block 0 of the following (request, head)
+      cc.blk = cc.nb - 1;
+      walk_next(p, cwin, cc, n, lane);
+    }
+  }
+  if (failed) {
+    // let the copies this warp has in flight land before the CTA may exit
+    for (; inflight > 0; --inflight) {
+      (void)mbar_wait_bounded(&bars[cs], cph, kWaitLimitNs);
+      if (++cs == S) { cs = 0; cph ^= 1u; }
+    }
+  }
+}
+
+// ------------------------------------------------------------- combine ---
+//
+// One warp per (request, kv head) of the step (built with GP_INKERNEL_MERGE=0
+// only).  A (request, head) whose blocks were cut between several attention
+// workers is merged here (merge_segment), after the attention kernel has
+// completed, so no worker waits for another.
+template <int G>
+__global__ void __launch_bounds__(kSmallWarps * 32)
+combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // which workers cut this (request, head): from the plan, final before the step
+  const int n = p.plan_misc[0];
+  const int gw = blockIdx.x * kSmallWarps + warp;
+  if (gw >= n * p.Hk) return;
+  const int i = gw / p.Hk, h = gw % p.Hk;
+  const int slot = p.plan_slot[i];
+  const int4 si = p.seginfo[gw];   // first and last worker of this (request, head)
+  if (si.x == si.y) return;        // finished by the attention kernel
+  // the workers' states and the staged token come from earlier kernels
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  merge_segment<G>(p, layer, i, h, slot, si, out, lane);
 }
 
 // ------------------------------------------------------ shared prefixes ---
@@ -1274,12 +1329,14 @@ static cudaError_t launch_mma_t(const PoolDev& p, const CUtensorMap* map, int la
   e = cudaLaunchKernelEx(&c1, attn_mma_kernel<G, kMmaStages>, *map, p, layer,
                                      (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                                      (const __nv_bfloat16*)v, (__nv_bfloat16*)out);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || GP_INKERNEL_MERGE) return e;
   const int warps = n * p.Hk;
   cudaLaunchConfig_t c2 = pdl_config(attr, dim3((warps + kSmallWarps - 1) / kSmallWarps),
                                      dim3(kSmallWarps * 32), 0, st);
   return cudaLaunchKernelEx(&c2, combine_kernel<G>, p, layer, (__nv_bfloat16*)out);
 }
+
+int attention_mma_launches(bool prefix) { return 1 + (prefix ? 1 : 0) + (GP_INKERNEL_MERGE ? 0 : 1); }
 
 template <int G>
 static cudaError_t occupancy_mma_t(int* blocks) {

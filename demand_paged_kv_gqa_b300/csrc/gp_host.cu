@@ -23,6 +23,7 @@ cudaError_t launch_attention_mma(const PoolDev& p, const CUtensorMap* map, int l
                                  const void* q, const void* k, const void* v, void* out, int grid,
                                  bool prefix, cudaStream_t st);
 cudaError_t attention_mma_occupancy(const PoolDev& p, int* blocks);
+int attention_mma_launches(bool prefix);
 int mma_warps_per_cta();
 cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count, cudaStream_t st);
 cudaError_t ceiling_setup();
@@ -596,7 +597,7 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
       const bool prefix = pool->dev.prefix_batch && pool->prefixed_active > 0;
       GP_LAUNCH(pool, gp::launch_attention_mma(pool->dev, &pool->kvmap, layer, n, q, k_new, v_new,
                                                out, pool->attn_grid, prefix, pool->stream));
-      pool->launches += prefix ? 2 : 1;  // attention and combine (and shared-prefix) kernels
+      pool->launches += gp::attention_mma_launches(prefix) - 1;  // beyond the one counted above
     }
     else
       GP_LAUNCH(pool, gp::launch_attention(pool->dev, layer, q, k_new, v_new, out, pool->attn_grid,

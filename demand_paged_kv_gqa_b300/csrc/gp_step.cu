@@ -156,6 +156,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(PoolDev p, int n, const int3
     const long long Weff = W < Tb ? W : Tb;
     const long long c = p.seg_cost;
     const int nseg = n * p.Hk;
+    // the merge counters of cut (request, head)s start the step at zero (the
+    // last piece of each resets its own after every layer)
+    for (int k = threadIdx.x; count && k < nseg; k += blockDim.x) p.seg_count[k] = 0;
     const long long U = Tb + c * nseg;
     for (int w = threadIdx.x; w < Weff; w += blockDim.x) {
       const long long u = ((long long)w * U) / Weff;
