@@ -61,8 +61,8 @@ __device__ __forceinline__ void finalize(const PoolDev& p, int layer, int i, int
   load_row<T, Gm>(reinterpret_cast<const uint8_t*>(knew + ((size_t)i * p.Hk + h) * D), sigma, kraw);
   load_row<T, Gm>(reinterpret_cast<const uint8_t*>(vnew + ((size_t)i * p.Hk + h) * D), sigma, vraw);
   if (p.rope) {
-    const double* c64 = p.cos64 + (size_t)pos * (D / 2);
-    const double* s64 = p.sin64 + (size_t)pos * (D / 2);
+    const double* c64 = rope_c64(p, pos);
+    const double* s64 = rope_s64(p, pos);
 #pragma unroll
     for (int e = 0; e < H2; ++e) {
       const int di = dim_of<Gm>(e, sigma);
@@ -229,8 +229,8 @@ attn_kernel(PoolDev p, int layer, const T* __restrict__ q, const T* __restrict__
     }
     // RoPE(q) and RoPE(s) at the current position (fp32 table), then scale.
     if (p.rope) {
-      const float* c32 = p.cos32 + (size_t)pos * (D / 2);
-      const float* s32 = p.sin32 + (size_t)pos * (D / 2);
+      const float* c32 = rope_c32(p, pos);
+      const float* s32 = rope_s32(p, pos);
 #pragma unroll
       for (int e = 0; e < H2; ++e) {
         const int di = dim_of<Gm>(e, sigma);

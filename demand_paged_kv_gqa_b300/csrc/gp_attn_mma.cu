@@ -55,11 +55,6 @@ constexpr int kMmaStageB = 8192;           // 16 tokens x (K 4 KiB + V 4 KiB)
 #ifndef GP_MMA_STAGES
 #define GP_MMA_STAGES 3
 #endif
-// 1: the attention kernel merges a cut (request, head) itself, in the piece
-// that completes it last; 0: combine_kernel merges them after the kernel.
-#ifndef GP_INKERNEL_MERGE
-#define GP_INKERNEL_MERGE 0
-#endif
 constexpr int kMmaWarps = GP_MMA_WARPS;
 constexpr int kMmaStages = GP_MMA_STAGES;
 constexpr int kObFloats = 4 * (kMmaD + 2);  // per-warp merge buffer: [G<=4][D] + m + l
@@ -144,12 +139,12 @@ __device__ __forceinline__ void issue_block_tma(const PoolDev& p, const CUtensor
 // Besides K/V blocks, a warp's ring carries one "meta" item in front of each
 // piece: what the piece needs besides the keys, copied by the bulk-copy
 // engine with the blocks.  Offsets inside a stage:
-constexpr int kQPitch = kMmaD + 8;  // query row pitch (elements): 272-byte rows put the
-                                    // G rows' pair loads in different banks
-constexpr int kMetaQ = 0;       // the G query rows, bf16 (<= 4 x 272 B)
+constexpr int kQPitch = kMmaD;      // query row pitch (elements): the G rows are one copy
+constexpr int kMetaQ = 0;       // the G query rows, bf16 (<= 4 x 256 B)
 constexpr int kMetaK = 1088;    // the step's new key, bf16
 constexpr int kMetaV = 1344;    // the step's new value, bf16
 constexpr int kMetaS = 1600;    // short and long summary before this step, fp32
+// kMetaC32 .. kMetaSF: the position's RoPE row, as laid out in the pool
 constexpr int kMetaC32 = 2624;  // rotary cos / sin rows of the position, fp32
 constexpr int kMetaS32 = 2880;
 constexpr int kMetaC32lo = 3136;  // their fp32 residuals (cos, sin: c32 + c32lo ~ fp64)
@@ -157,6 +152,10 @@ constexpr int kMetaS32lo = 3392;
 constexpr int kMetaC64 = 3648;  // the fp64 rows (the rare pairs the fp32 evaluation leaves open)
 constexpr int kMetaS64 = 4160;
 constexpr int kMetaSF = 4672;   // written in place: both summaries after this step's fold
+static_assert(kMetaS32 == kMetaC32 + 2 * kMmaD && kMetaC32lo == kMetaC32 + 4 * kMmaD &&
+                  kMetaS32lo == kMetaC32 + 6 * kMmaD && kMetaC64 == kMetaC32 + 8 * kMmaD &&
+                  kMetaS64 == kMetaC64 + 4 * kMmaD && kMetaSF == kMetaC32 + 16 * kMmaD,
+              "the meta item holds the RoPE row as laid out in the pool");
 
 // Per-warp extra buffer (after ob): the staged-token score of each query
 // head and the staged value (fp32), for finishing a piece in place.
@@ -278,19 +277,13 @@ __device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, i
   constexpr int D = kMmaD;
   const uint32_t bytes = G * D * 2 + 2 * D * 2 + 2 * D * 4 + (p.rope ? 2 * D * 4 + D * 8 : 0);
   mbar_expect_tx(bar, bytes);
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-    bulk_g2s(st + kMetaQ + g * kQPitch * 2, q + ((size_t)i * p.Hq + h * G + g) * D, D * 2, bar);
+  bulk_g2s(st + kMetaQ, q + ((size_t)i * p.Hq + h * G) * D, G * D * 2, bar);  // the G query rows
   bulk_g2s(st + kMetaK, knew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
   bulk_g2s(st + kMetaV, vnew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
   bulk_g2s(st + kMetaS, p.summary + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * D, 2 * D * 4, bar);
   if (p.rope) {
-    bulk_g2s(st + kMetaC32, p.cos32 + (size_t)pos * (D / 2), D * 2, bar);
-    bulk_g2s(st + kMetaS32, p.sin32 + (size_t)pos * (D / 2), D * 2, bar);
-    bulk_g2s(st + kMetaC32lo, p.cos32lo + (size_t)pos * (D / 2), D * 2, bar);
-    bulk_g2s(st + kMetaS32lo, p.sin32lo + (size_t)pos * (D / 2), D * 2, bar);
-    bulk_g2s(st + kMetaC64, p.cos64 + (size_t)pos * (D / 2), D * 4, bar);
-    bulk_g2s(st + kMetaS64, p.sin64 + (size_t)pos * (D / 2), D * 4, bar);
+    // the position's RoPE row: c32, s32, their residuals, c64, s64 (one copy)
+    bulk_g2s(st + kMetaC32, rope_c32(p, pos), 16 * D, bar);
   }
 }
 
@@ -895,6 +888,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
   const int first_seg = pc.i * p.Hk + pc.h;
   const int i_first = pc.i, h_first = pc.h;
   (void)plan_at(p, pwin, pc.i, n, lane);  // lets the first page window see the next request
+  // the consumer starts where the producer starts: its cursor and plan window
+  // are copies (no loads after the wait)
+  const Cursor c_first = pc;
+  cwin = pwin;
   int pblk = start;       // next block to issue
   bool pmeta = false;     // next item is a meta item
   // Ring bookkeeping in 32 bits: the producer's next stage ps; items issued
@@ -957,8 +954,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     if (inflight < S) emit(true);
   };
 
-  Cursor cc;
-  cursor_start(p, w, cc);
+  Cursor cc = c_first;
   int j = start;
   while (j < end && !failed) {
     const int i = cc.i, h = cc.h, slot = cc.slot, nb = cc.nb;
@@ -967,11 +963,6 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     const PlanEntry pe = plan_at(p, cwin, i, n, lane);
     const int R = pe.R;
     const bool score = (pe.flags & kPlanScore) != 0;
-#if GP_INKERNEL_MERGE
-    // the (request, head)'s first and last worker, used only when this piece
-    // is cut (plan data: loaded now, read at the piece's end)
-    const int4 seg_si = full ? make_int4(0, 0, 0, 0) : p.seginfo[i * p.Hk + h];
-#endif
 
     // ---- operand rows, and the once-per-(request, head) duties
     uint32_t afr[8][4];
@@ -1031,24 +1022,6 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       float* part = p.partials + (size_t)(w * 2 + pslot) * PW;
       for (int x = lane; x < G * D; x += 32) part[(x / D) * (D + 4) + (x % D)] = ob[x];
       if (lane < 2 * G) part[(lane % G) * (D + 4) + D + lane / G] = ob[G * D + lane];
-#if GP_INKERNEL_MERGE
-      // The piece that completes its (request, head) last merges all of them
-      // (each piece: state stored, fence, count).  The count goes back to 0
-      // for the next layer; the next kernel in the stream orders that.
-      __syncwarp();
-      __threadfence();
-      int last = 0;
-      if (lane == 0) {
-        const int pieces = seg_si.y - seg_si.x + 1;
-        last = atomicAdd(&p.seg_count[seg], 1) == pieces - 1;
-        if (last) p.seg_count[seg] = 0;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        merge_segment<G>(p, layer, i, h, slot, seg_si, out, lane);
-      }
-#endif
     }
     __syncwarp();  // the buffers are reused by the next piece
     if (j < end) {  // next piece: block 0 of the following (request, head)
@@ -1067,10 +1040,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
 
 // ------------------------------------------------------------- combine ---
 //
-// One warp per (request, kv head) of the step (built with GP_INKERNEL_MERGE=0
-// only).  A (request, head) whose blocks were cut between several attention
-// workers is merged here (merge_segment), after the attention kernel has
-// completed, so no worker waits for another.
+// One warp per (request, kv head) of the step.  A (request, head) whose
+// blocks were cut between several attention workers is merged here
+// (merge_segment), after the attention kernel has completed, so no worker
+// waits for another.
 template <int G>
 __global__ void __launch_bounds__(kSmallWarps * 32)
 combine_kernel(PoolDev p, int layer, __nv_bfloat16* __restrict__ out) {
@@ -1211,8 +1184,8 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int lay
           p.summary + ((((size_t)mslot[kk] * p.L + layer) * p.Hk + h) * 2) * D);
       for (int x = lane; x < 2 * D / 4; x += 32) reinterpret_cast<float4*>(mb + kPmS)[x] = srow[x];
       if (p.rope) {  // cos in lanes 0-15, sin in lanes 16-31 (D/2 floats each)
-        const size_t at = (size_t)p.plan_pos[mi[kk]] * (D / 2);
-        const float4* src = reinterpret_cast<const float4*>((lane < 16 ? p.cos32 : p.sin32) + at);
+        const int pos_k = p.plan_pos[mi[kk]];
+        const float4* src = reinterpret_cast<const float4*>(lane < 16 ? rope_c32(p, pos_k) : rope_s32(p, pos_k));
         reinterpret_cast<float4*>(mb + (lane < 16 ? kPmC32 : kPmS32))[lane & 15] = src[lane & 15];
       }
     }
@@ -1329,14 +1302,14 @@ static cudaError_t launch_mma_t(const PoolDev& p, const CUtensorMap* map, int la
   e = cudaLaunchKernelEx(&c1, attn_mma_kernel<G, kMmaStages>, *map, p, layer,
                                      (const __nv_bfloat16*)q, (const __nv_bfloat16*)k,
                                      (const __nv_bfloat16*)v, (__nv_bfloat16*)out);
-  if (e != cudaSuccess || GP_INKERNEL_MERGE) return e;
+  if (e != cudaSuccess) return e;
   const int warps = n * p.Hk;
   cudaLaunchConfig_t c2 = pdl_config(attr, dim3((warps + kSmallWarps - 1) / kSmallWarps),
                                      dim3(kSmallWarps * 32), 0, st);
   return cudaLaunchKernelEx(&c2, combine_kernel<G>, p, layer, (__nv_bfloat16*)out);
 }
 
-int attention_mma_launches(bool prefix) { return 1 + (prefix ? 1 : 0) + (GP_INKERNEL_MERGE ? 0 : 1); }
+int attention_mma_launches(bool prefix) { return prefix ? 3 : 2; }
 
 template <int G>
 static cudaError_t occupancy_mma_t(int* blocks) {

@@ -233,13 +233,8 @@ void fill_dev(gp_pool* p) {
   d.ctrl = (gp_ctrl*)(b + l.ctrl);
   d.prefix = (gp_prefix_meta*)(b + l.prefix);
   d.prefix_pages = (int32_t*)(b + l.prefix_pages);
-  const uint64_t tab = (uint64_t)c.max_seq_len * (c.head_dim / 2);
-  d.cos64 = (const double*)(b + l.rope);
-  d.sin64 = d.cos64 + tab;
-  d.cos32 = (const float*)(d.sin64 + tab);
-  d.sin32 = d.cos32 + tab;
-  d.cos32lo = d.sin32 + tab;
-  d.sin32lo = d.cos32lo + tab;
+  d.rope_rows = b + l.rope;
+  d.rope_row_bytes = 16 * c.head_dim;
   const uint64_t R = c.max_requests;
   uint64_t off = l.scratch;
   auto take = [&](uint64_t bytes) { uint64_t o = off; off = align_up(off + bytes); return b + o; };
@@ -370,32 +365,31 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   cudaError_t e = cudaMemsetAsync(dev_buf, 0, l.total, p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   if (cfg->rope_theta != 0.0) {
-    // fp64 table from the C library (pow, cos, sin); fp32 copies rounded
-    // once, and the fp32 residuals fp32(x64 - x32) (the difference is exact)
+    // fp64 values from the C library (pow, cos, sin); fp32 copies rounded
+    // once, and the fp32 residuals fp32(x64 - x32) (the difference is exact);
+    // one row per position: c32 | s32 | c32 residual | s32 residual | c64 | s64
     const int H = cfg->head_dim / 2;
-    const size_t tab = (size_t)cfg->max_seq_len * H;
-    std::vector<double> c64(tab), s64(tab);
-    std::vector<float> c32(tab), s32(tab), c32lo(tab), s32lo(tab);
+    const size_t row = 16 * (size_t)cfg->head_dim;
+    std::vector<uint8_t> rows((size_t)cfg->max_seq_len * row);
     std::vector<double> inv(H);
     for (int i = 0; i < H; ++i) inv[i] = std::pow(cfg->rope_theta, -(2.0 * i) / cfg->head_dim);
-    for (int pos = 0; pos < cfg->max_seq_len; ++pos)
+    for (int pos = 0; pos < cfg->max_seq_len; ++pos) {
+      uint8_t* r = rows.data() + (size_t)pos * row;
+      float* f32 = reinterpret_cast<float*>(r);
+      double* f64 = reinterpret_cast<double*>(r + 16 * (size_t)H);
       for (int i = 0; i < H; ++i) {
         const double a = (double)pos * inv[i];
-        const size_t k = (size_t)pos * H + i;
-        c64[k] = std::cos(a);
-        s64[k] = std::sin(a);
-        c32[k] = (float)c64[k];
-        s32[k] = (float)s64[k];
-        c32lo[k] = (float)(c64[k] - (double)c32[k]);
-        s32lo[k] = (float)(s64[k] - (double)s32[k]);
+        const double c = std::cos(a), sn = std::sin(a);
+        const float c32 = (float)c, s32 = (float)sn;
+        f32[i] = c32;
+        f32[H + i] = s32;
+        f32[2 * H + i] = (float)(c - (double)c32);
+        f32[3 * H + i] = (float)(sn - (double)s32);
+        f64[i] = c;
+        f64[H + i] = sn;
       }
-    const gp::PoolDev& d = p->dev;
-    e = cudaMemcpyAsync((void*)d.cos64, c64.data(), tab * 8, cudaMemcpyHostToDevice, p->stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin64, s64.data(), tab * 8, cudaMemcpyHostToDevice, p->stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.cos32, c32.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin32, s32.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.cos32lo, c32lo.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
-    if (e == cudaSuccess) e = cudaMemcpyAsync((void*)d.sin32lo, s32lo.data(), tab * 4, cudaMemcpyHostToDevice, p->stream);
+    }
+    e = cudaMemcpyAsync((void*)p->dev.rope_rows, rows.data(), rows.size(), cudaMemcpyHostToDevice, p->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(p->stream);
     if (e != cudaSuccess) return bail(GP_ERR_CUDA);
   }

@@ -51,12 +51,11 @@ struct PoolDev {
   gp_ctrl* ctrl;
   gp_prefix_meta* prefix;
   int32_t* prefix_pages;
-  const double* cos64;
-  const double* sin64;
-  const float* cos32;
-  const float* sin32;
-  const float* cos32lo;   // fp32(cos64 - cos32): cos32 + cos32lo carries ~48 bits
-  const float* sin32lo;
+  // RoPE rows, one per position (rope_row_bytes = 16 d): cos, sin fp32 [d/2]
+  // each (the fp64 values rounded once), their fp32 residuals fp32(x64 - x32)
+  // (x32 + residual carries ~48 bits), then cos, sin fp64 [d/2] each
+  const uint8_t* rope_rows;
+  int32_t rope_row_bytes;
   // scratch: per-step plan
   int32_t* plan_slot;     // [max_req] slot of request i
   int32_t* plan_R;        // [max_req] resident tokens (prefix + private)
@@ -223,6 +222,18 @@ __device__ __forceinline__ bool rope_bf16_certified(float a, float b, float c1, 
   out = (uint16_t)(rb | (hi < 0.f ? 0x8000u : 0u));
   return true;
 }
+
+// The parts of the RoPE row of position pos.
+__device__ __forceinline__ const float* rope_c32(const PoolDev& p, int pos) {
+  return reinterpret_cast<const float*>(p.rope_rows + (size_t)pos * p.rope_row_bytes);
+}
+__device__ __forceinline__ const float* rope_s32(const PoolDev& p, int pos) { return rope_c32(p, pos) + p.D / 2; }
+__device__ __forceinline__ const float* rope_c32lo(const PoolDev& p, int pos) { return rope_c32(p, pos) + p.D; }
+__device__ __forceinline__ const float* rope_s32lo(const PoolDev& p, int pos) { return rope_c32(p, pos) + 3 * (p.D / 2); }
+__device__ __forceinline__ const double* rope_c64(const PoolDev& p, int pos) {
+  return reinterpret_cast<const double*>(rope_c32(p, pos) + 2 * p.D);
+}
+__device__ __forceinline__ const double* rope_s64(const PoolDev& p, int pos) { return rope_c64(p, pos) + p.D / 2; }
 
 template <typename T> struct ElemIO;
 template <> struct ElemIO<float> {

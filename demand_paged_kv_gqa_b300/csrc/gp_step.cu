@@ -1042,9 +1042,9 @@ __global__ void write_tokens_kernel(PoolDev p, const int32_t* pages, const T* k,
     for (int e = lane; e < H; e += 32) {
       if constexpr (sizeof(T) == 2) {
         if (p.rope) {  // the certified fp32 evaluation of the fp64 expression below
-          const size_t at = (size_t)pos * H + e;
           const float x = ElemIO<T>::load(src, e), y = ElemIO<T>::load(src, e + H);
-          const float c1 = p.cos32[at], c2 = p.cos32lo[at], s1 = p.sin32[at], s2 = p.sin32lo[at];
+          const float c1 = rope_c32(p, pos)[e], c2 = rope_c32lo(p, pos)[e];
+          const float s1 = rope_s32(p, pos)[e], s2 = rope_s32lo(p, pos)[e];
           uint16_t ra, rb;
           if (rope_bf16_certified(x, y, c1, c2, -s1, -s2, ra) &&
               rope_bf16_certified(y, x, c1, c2, s1, s2, rb)) {
@@ -1057,7 +1057,7 @@ __global__ void write_tokens_kernel(PoolDev p, const int32_t* pages, const T* k,
       const double x = (double)ElemIO<T>::load(src, e), y = (double)ElemIO<T>::load(src, e + H);
       double a = x, b = y;
       if (p.rope) {
-        const double c = p.cos64[(size_t)pos * H + e], s = p.sin64[(size_t)pos * H + e];
+        const double c = rope_c64(p, pos)[e], s = rope_s64(p, pos)[e];
         a = __dsub_rn(__dmul_rn(x, c), __dmul_rn(y, s));
         b = __dadd_rn(__dmul_rn(y, c), __dmul_rn(x, s));
       }

@@ -140,9 +140,10 @@ typedef struct gp_config {
  *  ctrl      gp_ctrl
  *  prefix    [max_prefixes] gp_prefix_meta; then [max_prefixes][max_prefix_pages]
  *            int32 page ids
- *  rope      cos, sin fp64 [max_seq_len][d/2] each; then cos, sin fp32 (the
- *            fp64 values rounded once); then their fp32 residuals
- *            (fp64 value minus the fp32 value, rounded once)
+ *  rope      [max_seq_len] rows of 16·d bytes, one per position: cos, sin
+ *            fp32 [d/2] each (the fp64 values rounded once), their fp32
+ *            residuals (fp64 value minus the fp32 value, rounded once), then
+ *            cos, sin fp64 [d/2] each
  *  scratch   plan, split-K partials, move lists (internal) */
 typedef struct gp_layout {
   uint64_t kv, tok_pos, block, req, summary, staging, logits, wset, free_stack,
