@@ -319,10 +319,20 @@ __device__ __forceinline__ void block_sum2_ull(unsigned long long& a, unsigned l
   __syncthreads();
 }
 
-// Probability mass of a token in fixed point: e * 2^40 rounded to nearest
-// (e in (0, 1]; the scaling is exact, the conversion rounds once).
+// Probability mass of a token in fixed point: e * 2^40 rounded to nearest,
+// ties to even (e in [0, 1]; the same value as converting the exact fp32
+// product e * 2^40 to an integer).  Worked on the bit pattern with integer
+// operations: e = m * 2^(E - 150), so e * 2^40 = m * 2^(E - 110).
 __device__ __forceinline__ unsigned long long mass_q(float e) {
-  return (unsigned long long)__float2ll_rn(e * 0x1p40f);
+  const uint32_t b = __float_as_uint(e);
+  const int E = (int)(b >> 23);  // biased exponent (e >= 0)
+  if (E == 0) return 0ull;       // zero or subnormal: e * 2^40 < 2^-86
+  const uint32_t m = (b & 0x7fffffu) | 0x800000u;
+  const int sh = 110 - E;
+  if (sh <= 0) return (-sh <= 40) ? (unsigned long long)m << (-sh) : 0ull;
+  if (sh > 25) return 0ull;      // m < 2^24 < half of 2^sh
+  const uint32_t q = m >> sh, rem = m & ((1u << sh) - 1u), half = 1u << (sh - 1);
+  return (unsigned long long)(q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u));
 }
 
 // ceil(top_p * T) exactly, top_p an fp32 value in (0, 1].
@@ -356,6 +366,8 @@ struct SelShared {
   unsigned int pick_d[2];
   unsigned long long pick_a[2], pick_b[2];
   int done;
+  int hcount[32];   // compaction holes per warp
+  float inv[2];     // 2^40 / total mass of each summary
 };
 
 // Sources of e_j = exp(u_j - max) for one summary's scores: computed from the
@@ -590,6 +602,12 @@ template <class ES, class EL, class PF>
 __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const gp_req_meta& m,
                             int R, ES eS, EL eL, unsigned long long TS, unsigned long long TL,
                             PF posf, int C, int pos, int nfree, bool replan, SelShared& sh) {
+  // the importance scales 2^40 / T, once per item (fp64 division, one thread;
+  // published by the next barrier)
+  if (threadIdx.x == 0) {
+    sh.inv[0] = (float)(0x1p40 / (double)(TS ? TS : 1ull));
+    sh.inv[1] = (float)(0x1p40 / (double)(TL ? TL : 1ull));
+  }
   if (!replan) {
     // Top-p counts from the fixed-point total masses TS, TL
     const int2 Wv = topp_radix2(eS, eL, R, ceil_mul(p.top_p, TS), ceil_mul(p.top_p, TL), sh);
@@ -598,34 +616,47 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
       p.wset[row * 2 + 1] = Wv.y;
       atomicAdd((unsigned long long*)&p.plan_delta[i], (unsigned long long)(long long)(Wv.x - Wv.y));
     }
+  } else {
+    __syncthreads();
   }
-  const float inv[2] = {(float)(0x1p40 / (double)(TS ? TS : 1ull)),
-                        (float)(0x1p40 / (double)(TL ? TL : 1ull))};
   const int keep = C - nfree;
   const int weff = min(p.recent_window, keep);
-  KeyOf<ES, EL, PF> key_of{eS, eL, posf, inv[0], inv[1], m.n_pre_pages * p.P, pos - weff};
+  KeyOf<ES, EL, PF> key_of{eS, eL, posf, sh.inv[0], sh.inv[1], m.n_pre_pages * p.P, pos - weff};
   const unsigned long long thr_key = kth_smallest(key_of, C, nfree, sh);
   // holes below C - nfree and the survivors above it, both ascending, paired
-  // in order straight into the move list
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int32_t* mv = p.moves + row * (size_t)p.P * 4;  // room for 2P moves
+  // in order straight into the move list.  The holes: every warp counts those
+  // of its chunk of slots, then writes them after the chunks before it.
+  int32_t* mv = p.moves + row * (size_t)p.P * 4;  // room for 2P moves
+  {
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int chunk = ((keep + nw - 1) / nw + 31) & ~31;
+    const int s0 = wid * chunk, s1 = min(keep, s0 + chunk);
+    auto dropped_at = [&](int s) -> bool {
+      if (s >= s1) return false;
+      bool cand;
+      const unsigned long long key = key_of(s, &cand);
+      return cand && key <= thr_key;
+    };
+    int cnt = 0;
+    for (int base = s0; base < s1; base += 32) cnt += __popc(__ballot_sync(0xffffffffu, dropped_at(base + lane)));
+    if (lane == 0) sh.hcount[wid] = cnt;
+    __syncthreads();
     int nh = 0;
-    for (int base = 0; base < keep; base += 32) {
-      const int s = base + lane;
-      bool dropped = false;
-      if (s < keep) {
-        bool cand;
-        const unsigned long long key = key_of(s, &cand);
-        dropped = cand && key <= thr_key;
-      }
+    for (int w2 = 0; w2 < wid; ++w2) nh += sh.hcount[w2];
+    for (int base = s0; base < s1; base += 32) {
+      const bool dropped = dropped_at(base + lane);
       const unsigned int bal = __ballot_sync(0xffffffffu, dropped);
       if (dropped) {
         const int r = nh + __popc(bal & ((1u << lane) - 1u));
-        if (r < nfree) mv[2 * r] = s;
+        if (r < nfree) mv[2 * r] = base + lane;
       }
       nh += __popc(bal);
     }
+  }
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int nh = 0;
+    for (int w2 = 0; w2 < (int)(blockDim.x >> 5); ++w2) nh += sh.hcount[w2];
     int ns = 0;
     for (int base = keep; base < C; base += 32) {
       const int s = base + lane;
@@ -683,10 +714,15 @@ __global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDe
     const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
     const float* uS = p.logits + row * 2 * p.logit_width;
     const float* uL = uS + p.logit_width;
+    // rows of up to kSelSmemTok tokens are staged: the scores now, e_j below
+    // (each thread rewrites its own entries)
+    const bool staged = R <= kSelSmemTok && C <= kSelSmemTok;
     float a = -INFINITY, b = -INFINITY;
     for (int j = threadIdx.x; j < R; j += blockDim.x) {
-      a = fmaxf(a, uS[j]);
-      b = fmaxf(b, uL[j]);
+      const float x = uS[j], y = uL[j];
+      a = fmaxf(a, x);
+      b = fmaxf(b, y);
+      if (staged) { eSs[j] = x; eLs[j] = y; }
     }
     const float2 mx = block_max2(a, b, sh.redf);
     PosGlobal pg{p.block + (size_t)slot * p.block_width + m.n_pre_pages, p.tok_pos, p.P, p.L, p.Hk,
@@ -694,9 +730,8 @@ __global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDe
     // fixed-point total masses; the staged path stages e_j in the same loop
     // (the sums' barriers also publish the staged rows)
     unsigned long long TS = 0ull, TL = 0ull;
-    const bool staged = R <= kSelSmemTok && C <= kSelSmemTok;
     for (int j = threadIdx.x; j < R; j += blockDim.x) {
-      const float eS = expf(uS[j] - mx.x), eL = expf(uL[j] - mx.y);
+      const float eS = expf((staged ? eSs[j] : uS[j]) - mx.x), eL = expf((staged ? eLs[j] : uL[j]) - mx.y);
       TS += mass_q(eS);
       TL += mass_q(eL);
       if (staged) { eSs[j] = eS; eLs[j] = eL; }
