@@ -360,7 +360,9 @@ __device__ __forceinline__ unsigned long long ceil_mul(float top_p, unsigned lon
 // Histograms for both summaries.
 struct SelShared {
   unsigned int cnt[2][256];
-  unsigned long long mass[2][256];
+  // the 64-bit masses as two 32-bit words, added with native 32-bit atomics
+  // (the low word's carry goes to the high word)
+  unsigned int mlo[2][256], mhi[2][256];
   ulonglong2 red[33];
   float2 redf[33];
   unsigned int pick_d[2];
@@ -369,6 +371,16 @@ struct SelShared {
   int hcount[32];   // compaction holes per warp
   float inv[2];     // 2^40 / total mass of each summary
 };
+
+// x as fp32: the high word (exact below 2^24) times 2^32 plus the low word,
+// rounded once more by the fused multiply-add (within an ulp of x).
+__device__ __forceinline__ float u64_to_f32(unsigned long long x) {
+  return __fmaf_rn(__uint2float_rn((unsigned int)(x >> 32)), 0x1p32f, __uint2float_rn((unsigned int)x));
+}
+
+__device__ __forceinline__ unsigned long long mass_at(const SelShared& sh, int X, int d) {
+  return ((unsigned long long)sh.mhi[X][d] << 32) | sh.mlo[X][d];
+}
 
 // Sources of e_j = exp(u_j - max) for one summary's scores: computed from the
 // scores in global memory, or read from shared memory where the kernel has
@@ -405,13 +417,33 @@ struct PosSmem {
 // most significant first) on the fp32 bit patterns of e_j, weighting each by
 // its fixed-point mass.  The two selects share their passes: warp X scans
 // summary X's histogram.
+__device__ __forceinline__ void bin_add(SelShared& sh, int X, int d, unsigned int c, unsigned long long v) {
+  atomicAdd(&sh.cnt[X][d], c);
+  const unsigned int vlo = (unsigned int)v, vhi = (unsigned int)(v >> 32);
+  const unsigned int old = atomicAdd(&sh.mlo[X][d], vlo);
+  const unsigned int up = vhi + ((old + vlo < old) ? 1u : 0u);
+  if (up) atomicAdd(&sh.mhi[X][d], up);
+}
+
+// Adds each lane's (digit d, mass mq) to the histogram X (d = 256: nothing).
+// A lane alone with its digit adds its own; lanes sharing a digit are summed
+// first, one group at a time, by full-warp reductions (a reduction over a
+// partial mask costs a pass per group anyway, and more).
 __device__ __forceinline__ void hist_add(SelShared& sh, int X, int d, unsigned long long mq) {
+  const int lane = threadIdx.x & 31;
   const unsigned int peers = __match_any_sync(0xffffffffu, d);
-  const unsigned int hi = __reduce_add_sync(peers, (unsigned int)(mq >> 20));
-  const unsigned int lo = __reduce_add_sync(peers, (unsigned int)(mq & 0xfffffull));
-  if (d < 256 && (threadIdx.x & 31) == __ffs(peers) - 1) {
-    atomicAdd(&sh.cnt[X][d], (unsigned int)__popc(peers));
-    atomicAdd(&sh.mass[X][d], ((unsigned long long)hi << 20) + (unsigned long long)lo);
+  const bool valid = d < 256;
+  const bool alone = __popc(peers) == 1;
+  if (valid && alone) bin_add(sh, X, d, 1u, mq);
+  unsigned int todo = __ballot_sync(0xffffffffu, valid && !alone);
+  while (todo) {  // warp-uniform
+    const int src = __ffs(todo) - 1;
+    const unsigned int members = __shfl_sync(0xffffffffu, peers, src);
+    const bool in = (members >> lane) & 1u;
+    const unsigned int hi = __reduce_add_sync(0xffffffffu, in ? (unsigned int)(mq >> 20) : 0u);
+    const unsigned int lo = __reduce_add_sync(0xffffffffu, in ? (unsigned int)(mq & 0xfffffull) : 0u);
+    if (lane == src) bin_add(sh, X, d, (unsigned int)__popc(members), ((unsigned long long)hi << 20) + lo);
+    todo &= ~members;
   }
 }
 
@@ -422,7 +454,8 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
   unsigned long long mass_above[2] = {0ull, 0ull}, cnt_above[2] = {0ull, 0ull};
   for (int d = threadIdx.x; d < 512; d += blockDim.x) {
     (&sh.cnt[0][0])[d] = 0u;
-    (&sh.mass[0][0])[d] = 0ull;
+    (&sh.mlo[0][0])[d] = 0u;
+    (&sh.mhi[0][0])[d] = 0u;
   }
   __syncthreads();
   for (int pass = 0; pass < 4; ++pass) {
@@ -451,7 +484,7 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
       unsigned long long mloc = 0ull, cloc = 0ull;
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        mloc += sh.mass[X][255 - 8 * lane - t];
+        mloc += mass_at(sh, X, 255 - 8 * lane - t);
         cloc += sh.cnt[X][255 - 8 * lane - t];
       }
       unsigned long long mex = mloc, cex = cloc;
@@ -471,19 +504,20 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
         unsigned long long macc = mex, cacc = cex;
         for (int t = 0; t < 8; ++t) {
           const int d = 255 - 8 * lane - t;
-          if (macc + sh.mass[X][d] >= need || t == 7) {
+          if (macc + mass_at(sh, X, d) >= need || t == 7) {
             sh.pick_d[X] = (unsigned)d;
             sh.pick_a[X] = macc;
             sh.pick_b[X] = cacc;
             break;
           }
-          macc += sh.mass[X][d];
+          macc += mass_at(sh, X, d);
           cacc += sh.cnt[X][d];
         }
       }
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        sh.mass[X][255 - 8 * lane - t] = 0ull;
+        sh.mlo[X][255 - 8 * lane - t] = 0u;
+        sh.mhi[X][255 - 8 * lane - t] = 0u;
         sh.cnt[X][255 - 8 * lane - t] = 0u;
       }
     }
@@ -602,11 +636,11 @@ template <class ES, class EL, class PF>
 __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const gp_req_meta& m,
                             int R, ES eS, EL eL, unsigned long long TS, unsigned long long TL,
                             PF posf, int C, int pos, int nfree, bool replan, SelShared& sh) {
-  // the importance scales 2^40 / T, once per item (fp64 division, one thread;
-  // published by the next barrier)
+  // the importance scales 2^40 / T in fp32 (T >= 2^40: the largest e_j is 1),
+  // once per item by one thread, published by the next barrier
   if (threadIdx.x == 0) {
-    sh.inv[0] = (float)(0x1p40 / (double)(TS ? TS : 1ull));
-    sh.inv[1] = (float)(0x1p40 / (double)(TL ? TL : 1ull));
+    sh.inv[0] = __fdiv_rn(0x1p40f, u64_to_f32(TS ? TS : 1ull));
+    sh.inv[1] = __fdiv_rn(0x1p40f, u64_to_f32(TL ? TL : 1ull));
   }
   if (!replan) {
     // Top-p counts from the fixed-point total masses TS, TL
