@@ -269,22 +269,39 @@ __device__ __forceinline__ void walk_next(const PoolDev& p, PlanWin& w, Cursor& 
   }
 }
 
+// A meta item in two halves on one mbarrier: the part that is final before
+// the step (the summaries and the position's RoPE row; it arms the barrier
+// for the whole item) and the step's inputs (query rows, new key, value).
 template <int G>
-__device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, int h, int slot,
-                                           int pos, const __nv_bfloat16* q,
-                                           const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
-                                           uint8_t* st, uint64_t* bar) {
+__device__ __forceinline__ void issue_meta_state(const PoolDev& p, int layer, int h, int slot, int pos,
+                                                 uint8_t* st, uint64_t* bar) {
   constexpr int D = kMmaD;
   const uint32_t bytes = G * D * 2 + 2 * D * 2 + 2 * D * 4 + (p.rope ? 2 * D * 4 + D * 8 : 0);
   mbar_expect_tx(bar, bytes);
-  bulk_g2s(st + kMetaQ, q + ((size_t)i * p.Hq + h * G) * D, G * D * 2, bar);  // the G query rows
-  bulk_g2s(st + kMetaK, knew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
-  bulk_g2s(st + kMetaV, vnew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
   bulk_g2s(st + kMetaS, p.summary + ((((size_t)slot * p.L + layer) * p.Hk + h) * 2) * D, 2 * D * 4, bar);
   if (p.rope) {
     // the position's RoPE row: c32, s32, their residuals, c64, s64 (one copy)
     bulk_g2s(st + kMetaC32, rope_c32(p, pos), 16 * D, bar);
   }
+}
+
+template <int G>
+__device__ __forceinline__ void issue_meta_inputs(const PoolDev& p, int i, int h, const __nv_bfloat16* q,
+                                                  const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
+                                                  uint8_t* st, uint64_t* bar) {
+  constexpr int D = kMmaD;
+  bulk_g2s(st + kMetaQ, q + ((size_t)i * p.Hq + h * G) * D, G * D * 2, bar);  // the G query rows
+  bulk_g2s(st + kMetaK, knew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
+  bulk_g2s(st + kMetaV, vnew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
+}
+
+template <int G>
+__device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, int h, int slot,
+                                           int pos, const __nv_bfloat16* q,
+                                           const __nv_bfloat16* knew, const __nv_bfloat16* vnew,
+                                           uint8_t* st, uint64_t* bar) {
+  issue_meta_state<G>(p, layer, h, slot, pos, st, bar);
+  issue_meta_inputs<G>(p, i, h, q, knew, vnew, st, bar);
 }
 
 // Pointers to what a piece needs (a meta item in shared memory).
@@ -925,15 +942,17 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
     ++inflight;
     return true;
   };
-  // prologue: blocks only (meta items read this step's inputs)
+  // prologue: the first meta item's state half, then blocks only (meta
+  // items read this step's inputs)
+  {
+    const PlanEntry e = plan_at(p, pwin, i_first, n, lane);
+    if (lane == 0) issue_meta_state<G>(p, layer, h_first, e.slot, e.pos, ring, &bars[0]);
+  }
   while (inflight < S && emit(false)) {}
   // The step's inputs, the split-K scratch and the outputs belong to earlier
   // kernels: wait for them.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  {
-    const PlanEntry e = plan_at(p, pwin, i_first, n, lane);
-    if (lane == 0) issue_meta<G>(p, layer, i_first, h_first, e.slot, e.pos, q, knew, vnew, ring, &bars[0]);
-  }
+  if (lane == 0) issue_meta_inputs<G>(p, i_first, h_first, q, knew, vnew, ring, &bars[0]);
   while (inflight < S && emit(true)) {}
 
   const uint32_t ring_u32 = smem_u32(ring);

@@ -953,7 +953,7 @@ __device__ __forceinline__ uint8_t* slot_row(const PoolDev& p, const int32_t* bt
          (size_t)h * p.head_bytes + (size_t)(s % p.P) * rowb;
 }
 
-__global__ void __launch_bounds__(256) commit_kernel(PoolDev p, int part) {
+__global__ void __launch_bounds__(256, 4) commit_kernel(PoolDev p, int part) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int n = p.plan_misc[0];
@@ -995,22 +995,20 @@ __global__ void __launch_bounds__(256) commit_kernel(PoolDev p, int part) {
           int pd, ps;
           uint8_t* rd = slot_row(p, bt, dst, layer, h, rowb, &pd);
           const uint8_t* rs = slot_row(p, bt, src, layer, h, rowb, &ps);
-          uint4 kx[4], vx[4];
-          const int per = chunks / 8;  // 2 or 4 chunks per lane
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j < per) {
-              kx[j] = *reinterpret_cast<const uint4*>(rs + 16 * (sub + 8 * j));
-              vx[j] = *reinterpret_cast<const uint4*>(rs + p.half_bytes + 16 * (sub + 8 * j));
-            }
-          }
+          const int per = chunks / 8;  // 2 or 4 chunks per lane, two at a time
           int tpos = 0;
           if (sub == 0) tpos = p.tok_pos[(((size_t)ps * p.L + layer) * p.Hk + h) * p.P + (src % p.P)];
+          for (int j0 = 0; j0 < per; j0 += 2) {
+            uint4 kx[2], vx[2];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (j < per) {
-              *reinterpret_cast<uint4*>(rd + 16 * (sub + 8 * j)) = kx[j];
-              *reinterpret_cast<uint4*>(rd + p.half_bytes + 16 * (sub + 8 * j)) = vx[j];
+            for (int j = 0; j < 2; ++j) {
+              kx[j] = *reinterpret_cast<const uint4*>(rs + 16 * (sub + 8 * (j0 + j)));
+              vx[j] = *reinterpret_cast<const uint4*>(rs + p.half_bytes + 16 * (sub + 8 * (j0 + j)));
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              *reinterpret_cast<uint4*>(rd + 16 * (sub + 8 * (j0 + j))) = kx[j];
+              *reinterpret_cast<uint4*>(rd + p.half_bytes + 16 * (sub + 8 * (j0 + j))) = vx[j];
             }
           }
           if (sub == 0) p.tok_pos[(((size_t)pd * p.L + layer) * p.Hk + h) * p.P + (dst % p.P)] = tpos;
