@@ -62,12 +62,16 @@ constexpr int kObFloats = 4 * (kMmaD + 2);  // per-warp merge buffer: [G<=4][D] 
 // griddepcontrol) and must fit beside two resident attention CTAs.
 constexpr int kSmallWarps = 1;
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
+// One 16-token block (K and V, both 64-column halves) of a (page, layer,
+// head) in one copy: the block map's box (64, 16, 2, 2, 1) at token offset
+// tok within the page and row index (page * L + layer) * Hk + head.
+__device__ __forceinline__ void tma_load_block(void* dst, const CUtensorMap* map, int tok, int prow,
+                                               uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(tok), "r"(0), "r"(0), "r"(prow),
+      "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -125,13 +129,8 @@ __device__ __forceinline__ void issue_block_tma(const PoolDev& p, const CUtensor
                                                 uint64_t* bar) {
   const int t0 = c.base + c.blk * kBlockTok;  // resident token of the block's first row
   const int in_page = p.P_log2 >= 0 ? (t0 & (p.P - 1)) : t0 % p.P;
-  // row of the pool viewed as [num_pages * L * Hk * 2 * P][d]
-  const int row = (((page * p.L + layer) * p.Hk + c.h) * 2) * p.P + in_page;
   mbar_expect_tx(bar, kMmaStageB);
-  tma_load_2d(stage, map, 0, row, bar);
-  tma_load_2d(stage + 2048, map, 64, row, bar);
-  tma_load_2d(stage + 4096, map, 0, row + p.P, bar);
-  tma_load_2d(stage + 6144, map, 64, row + p.P, bar);
+  tma_load_block(stage, map, in_page, (page * p.L + layer) * p.Hk + c.h, bar);
 }
 
 // ------------------------------------------------------------ meta items ---
@@ -635,12 +634,17 @@ __device__ __forceinline__ void attend_block(const uint32_t (&afr)[8][4], float 
     }
   }
   // ---- online softmax (log2 domain) for head row g
-  float mx = -INFINITY;
+  // rows beyond the G heads, and tokens beyond the resident count (the last
+  // block of a segment only), take no part in the softmax
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    if (!head_row || tok[u] >= nvalid) sv[u] = -INFINITY;
-    mx = fmaxf(mx, sv[u]);
+  for (int u = 0; u < 4; ++u)
+    if (!head_row) sv[u] = -INFINITY;
+  if (nvalid < kBlockTok) {  // warp-uniform
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (tok[u] >= nvalid) sv[u] = -INFINITY;
   }
+  float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
   mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
   // the running max moves only when a score exceeds it by more than 2^8:
@@ -852,7 +856,7 @@ __device__ __forceinline__ void merge_segment(const PoolDev& p, int layer, int i
 
 template <int G, int S>
 __global__ void __launch_bounds__(kMmaWarps * 32)
-attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
+attn_mma_kernel(const __grid_constant__ CUtensorMap kvblk, PoolDev p, int layer,
                 const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ knew,
                 const __nv_bfloat16* __restrict__ vnew, __nv_bfloat16* __restrict__ out) {
   static_assert(G == 1 || G == 2 || G == 4, "G");
@@ -931,7 +935,7 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
       const int page = page_of_ahead(p, win, pwin, pc, n, lane);
       if (lane == 0) {
         fence_proxy_async_smem();
-        issue_block_tma(p, &kvmap, layer, pc, page, st, &bars[s]);
+        issue_block_tma(p, &kvblk, layer, pc, page, st, &bars[s]);
       }
       if (++pblk < end) {
         walk_next(p, pwin, pc, n, lane);
@@ -1109,7 +1113,7 @@ size_t prefix_smem_bytes() {
 
 template <int G>
 __global__ void __launch_bounds__(kPrefWarps * 32)
-prefix_attn_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer,
+prefix_attn_kernel(const __grid_constant__ CUtensorMap kvblk, PoolDev p, int layer,
                    const __nv_bfloat16* __restrict__ q) {
   constexpr int D = kMmaD, S = kPrefStages, PW = G * (D + 4);
   // stages on 1024-byte boundaries (128-byte swizzle); see attn_mma_kernel
@@ -1170,14 +1174,10 @@ prefix_attn_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int lay
         set_status(p, GP_ST_BAD_PAGE, page);
         page = 0;
       }
-      const int row = (((page * p.L + layer) * p.Hk + h) * 2) * p.P + ((b * kBlockTok) % p.P);
       uint8_t* st = ring + s * kMmaStageB;
       fence_proxy_async_smem();
       mbar_expect_tx(&bars[s], kMmaStageB);
-      tma_load_2d(st, &kvmap, 0, row, &bars[s]);
-      tma_load_2d(st + 2048, &kvmap, 64, row, &bars[s]);
-      tma_load_2d(st + 4096, &kvmap, 0, row + p.P, &bars[s]);
-      tma_load_2d(st + 6144, &kvmap, 64, row + p.P, &bars[s]);
+      tma_load_block(st, &kvblk, (b * kBlockTok) % p.P, (page * p.L + layer) * p.Hk + h, &bars[s]);
       ++issued;
     };
     if (threadIdx.x == 0)

@@ -49,6 +49,7 @@ cudaError_t launch_release_prefix(const PoolDev& p, int pid, cudaStream_t st);
 
 struct gp_pool {
   CUtensorMap kvmap;  // (64-byte aligned type) K/V pages as [rows][d] bf16, 128-byte swizzle
+  CUtensorMap kvblk;  // the same pages as 5-D boxes of one 16-token block (K and V, both halves)
   bool use_mma = false;           // bf16 pages, head_dim 128: tensor-core kernel
   gp_config cfg;
   gp::PoolDev dev;
@@ -419,6 +420,21 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return bail(GP_ERR_CUDA);
+    // One 16-token block of a (page, layer, head) in one copy: dims (inner
+    // first) 64 columns, P tokens (256-byte stride), 2 column halves (128 B),
+    // K|V (P * 256 B), page * L * Hk + layer * Hk + head (2 * P * 256 B).  The
+    // box (64, 16, 2, 2, 1) lands as [K|V][half][token][64] with the same
+    // 128-byte swizzle as four 2-D boxes of 16 rows x 64 columns.
+    const cuuint64_t P = (cuuint64_t)cfg->page_size, rb = (cuuint64_t)cfg->head_dim * 2;
+    const cuuint64_t dims5[5] = {64, P, 2, 2,
+                                 (cuuint64_t)cfg->num_pages * cfg->num_layers * cfg->num_kv_heads};
+    const cuuint64_t strides5[4] = {rb, 128, P * rb, 2 * P * rb};
+    const cuuint32_t box5[5] = {64, (cuuint32_t)gp::kBlockTok, 2, 2, 1};
+    const cuuint32_t estr5[5] = {1, 1, 1, 1, 1};
+    r = encode(&p->kvblk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, (void*)p->dev.kv, dims5, strides5, box5,
+               estr5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return bail(GP_ERR_CUDA);
     if (gp::ceiling_setup() != cudaSuccess) return bail(GP_ERR_CUDA);
   }
   int dev = 0, sms = 0, blocks = 0;
@@ -589,7 +605,7 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
   if (n > 0) {
     if (pool->use_mma) {
       const bool prefix = pool->dev.prefix_batch && pool->prefixed_active > 0;
-      GP_LAUNCH(pool, gp::launch_attention_mma(pool->dev, &pool->kvmap, layer, n, q, k_new, v_new,
+      GP_LAUNCH(pool, gp::launch_attention_mma(pool->dev, &pool->kvblk, layer, n, q, k_new, v_new,
                                                out, pool->attn_grid, prefix, pool->stream));
       pool->launches += gp::attention_mma_launches(prefix) - 1;  // beyond the one counted above
     }
