@@ -2,9 +2,10 @@
 // bandwidth ceiling the attention kernel is measured against.
 //
 // kv_read_kernel walks exactly the blocks the bf16 attention kernel walks for
-// one layer (same persistent grid, same per-warp split, same 2-D tensor-map
-// copies into a per-warp ring of stages) but does no arithmetic: it folds one
-// word of each stage into a checksum so the copies cannot be elided.
+// one layer (same persistent grid, same per-warp split, the same one-copy
+// tensor-map loads of a block into a per-warp ring of stages) but does no
+// arithmetic: it folds one word of each stage into a checksum so the copies
+// cannot be elided.
 //   mode 0  paged:       the request's own pages, in block-table order;
 //   mode 1  sequential:  the same number of 8 KiB blocks, taken in address
 //                        order from the start of the K/V region (TMA);
@@ -21,17 +22,21 @@ constexpr int kCeilWarps = 4;
 constexpr int kCeilStages = 3;
 constexpr int kCeilStageB = 8192;
 
-__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, int y,
-                                      uint64_t* bar) {
+// A 16-token block (K and V, both 64-column halves) of row index
+// (page * L + layer) * Hk + head, token offset tok, through the pool's 5-D
+// block map: one copy.
+__device__ __forceinline__ void tma_block(void* dst, const CUtensorMap* map, int tok, int prow,
+                                          uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(tok), "r"(0), "r"(0), "r"(prow),
+      "r"(smem_u32(bar))
       : "memory");
 }
 
 __global__ void __launch_bounds__(kCeilWarps * 32)
-kv_read_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer, int mode,
+kv_read_kernel(const __grid_constant__ CUtensorMap kvblk, PoolDev p, int layer, int mode,
                uint32_t* sink) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -76,23 +81,22 @@ kv_read_kernel(const __grid_constant__ CUtensorMap kvmap, PoolDev p, int layer, 
     cursor_start(p, w, pc);
     PageWin win;
     int64_t issued = start;
+    const int bpp = p.P / kBlockTok;  // blocks per page
     auto issue = [&](int s) {
-      int row;
+      int prow, tok;
       if (mode == 0) {
         const int page = page_of(p, win, pc, lane);
-        const int t0 = pc.blk * kBlockTok;
-        row = (((page * p.L + layer) * p.Hk + pc.h) * 2) * p.P + (t0 % p.P);
+        prow = (page * p.L + layer) * p.Hk + pc.h;
+        tok = (pc.blk * kBlockTok) % p.P;
       } else {
-        row = (int)((issued % region_blocks) * 2 * kBlockTok);
+        const int64_t b = issued % region_blocks;
+        prow = (int)(b / bpp);
+        tok = (int)(b % bpp) * kBlockTok;
       }
       if (lane == 0) {
         fence_proxy_async_smem();
         mbar_expect_tx(&bars[s], kCeilStageB);
-        uint8_t* st = ring + s * kCeilStageB;
-        tma2d(st, &kvmap, 0, row, &bars[s]);
-        tma2d(st + 2048, &kvmap, 64, row, &bars[s]);
-        tma2d(st + 4096, &kvmap, 0, row + kBlockTok, &bars[s]);
-        tma2d(st + 6144, &kvmap, 64, row + kBlockTok, &bars[s]);
+        tma_block(ring + s * kCeilStageB, &kvblk, tok, prow, &bars[s]);
       }
       if (issued + 1 < end) cursor_next(p, pc);
       ++issued;

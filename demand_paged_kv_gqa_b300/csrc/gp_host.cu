@@ -48,8 +48,8 @@ cudaError_t launch_release_prefix(const PoolDev& p, int pid, cudaStream_t st);
 }  // namespace gp
 
 struct gp_pool {
-  CUtensorMap kvmap;  // (64-byte aligned type) K/V pages as [rows][d] bf16, 128-byte swizzle
-  CUtensorMap kvblk;  // the same pages as 5-D boxes of one 16-token block (K and V, both halves)
+  CUtensorMap kvblk;  // (64-byte aligned type) K/V pages as 5-D boxes of one 16-token block
+                      // (K and V, both column halves), 128-byte swizzle
   bool use_mma = false;           // bf16 pages, head_dim 128: tensor-core kernel
   gp_config cfg;
   gp::PoolDev dev;
@@ -402,36 +402,24 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   p->dev.summary_via_next = p->use_mma ? 1 : 0;
   p->dev.seg_cost = p->use_mma ? GP_SEG_COST : 0;
   if (p->use_mma) {
-    // The pool's K/V pages viewed as one 2-D bf16 tensor [rows][d], rows =
-    // ((page * L + layer) * Hk + head) * 2 * P + kv * P + token; boxes of
-    // 16 rows x 64 columns (128 bytes) land in shared memory 128B-swizzled.
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult qr;
     e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
     if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return bail(GP_ERR_CUDA);
     auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    const cuuint64_t rows = (cuuint64_t)cfg->num_pages * cfg->num_layers * cfg->num_kv_heads * 2 *
-                            cfg->page_size;
-    const cuuint64_t dims[2] = {(cuuint64_t)cfg->head_dim, rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cfg->head_dim * 2};
-    const cuuint32_t box[2] = {64, (cuuint32_t)gp::kBlockTok};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&p->kvmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (void*)p->dev.kv, dims, strides,
-                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return bail(GP_ERR_CUDA);
-    // One 16-token block of a (page, layer, head) in one copy: dims (inner
-    // first) 64 columns, P tokens (256-byte stride), 2 column halves (128 B),
-    // K|V (P * 256 B), page * L * Hk + layer * Hk + head (2 * P * 256 B).  The
-    // box (64, 16, 2, 2, 1) lands as [K|V][half][token][64] with the same
-    // 128-byte swizzle as four 2-D boxes of 16 rows x 64 columns.
+    // The pool's K/V pages as a 5-D bf16 tensor, one 16-token block of a
+    // (page, layer, head) per copy: dims (inner first) 64 columns, P tokens
+    // (256-byte stride), 2 column halves (128 B), K|V (P * 256 B), and
+    // page * L * Hk + layer * Hk + head (2 * P * 256 B).  The box
+    // (64, 16, 2, 2, 1) lands in shared memory as [K|V][half][token][64],
+    // 128-byte rows 128B-swizzled by token.
     const cuuint64_t P = (cuuint64_t)cfg->page_size, rb = (cuuint64_t)cfg->head_dim * 2;
     const cuuint64_t dims5[5] = {64, P, 2, 2,
                                  (cuuint64_t)cfg->num_pages * cfg->num_layers * cfg->num_kv_heads};
     const cuuint64_t strides5[4] = {rb, 128, P * rb, 2 * P * rb};
     const cuuint32_t box5[5] = {64, (cuuint32_t)gp::kBlockTok, 2, 2, 1};
     const cuuint32_t estr5[5] = {1, 1, 1, 1, 1};
-    r = encode(&p->kvblk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, (void*)p->dev.kv, dims5, strides5, box5,
+    const CUresult r = encode(&p->kvblk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, (void*)p->dev.kv, dims5, strides5, box5,
                estr5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return bail(GP_ERR_CUDA);
@@ -703,7 +691,7 @@ int gp_kv_read_ceiling(gp_pool* pool, int32_t layer0, int32_t count, int32_t mod
   const int wpc = gp::ceiling_warps_per_cta();
   const int grid = (pool->dev.num_workers + wpc - 1) / wpc;
   for (int l = layer0; l < layer0 + count; ++l)
-    GP_LAUNCH(pool, gp::launch_kv_read(pool->dev, &pool->kvmap, l, mode, sink_dev, grid, pool->stream));
+    GP_LAUNCH(pool, gp::launch_kv_read(pool->dev, &pool->kvblk, l, mode, sink_dev, grid, pool->stream));
   return GP_OK;
 }
 
@@ -783,7 +771,7 @@ int gp_kv_read_ceiling_static(gp_pool* pool, int32_t layer0, int32_t count, int3
   const int wpc = gp::ceiling_warps_per_cta();
   const int grid = (d.num_workers + wpc - 1) / wpc;
   for (int l = layer0; l < layer0 + count; ++l)
-    GP_LAUNCH(pool, gp::launch_kv_read(d, &pool->kvmap, l, mode, sink_dev, grid, pool->stream));
+    GP_LAUNCH(pool, gp::launch_kv_read(d, &pool->kvblk, l, mode, sink_dev, grid, pool->stream));
   return GP_OK;
 }
 
