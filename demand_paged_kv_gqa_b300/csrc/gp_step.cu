@@ -449,7 +449,8 @@ __device__ __forceinline__ void hist_add(SelShared& sh, int X, int d, unsigned l
 
 template <class ES, class EL>
 __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsigned long long thr1,
-                            SelShared& sh) {
+                            SelShared& sh, uint32_t* wbins_a = nullptr,
+                            uint32_t* wbins_b = nullptr) {
   uint32_t prefix[2] = {0u, 0u}, pmask = 0u;
   unsigned long long mass_above[2] = {0ull, 0ull}, cnt_above[2] = {0ull, 0ull};
   for (int d = threadIdx.x; d < 512; d += blockDim.x) {
@@ -460,6 +461,53 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
   __syncthreads();
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
+    if (pass == 0 && wbins_a) {
+      // The top byte of e in [0, 1] is one of 64 digits (sign 0, exponent
+      // <= 127).  Each warp counts into bins of its own (cnt, mass low and
+      // high words: [warp][X][64] each, in shared memory the caller leaves
+      // free), so only lanes of one warp ever meet on a bin; the warps' bins
+      // are then summed into the histogram.
+      const int nw = blockDim.x >> 5, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+      uint32_t* wc = wbins_a;               // [nw][2][64] counts
+      uint32_t* wl = wbins_a + nw * 128;    // mass low words
+      uint32_t* wh = wbins_b;               // mass high words
+      for (int k = lane; k < 128; k += 32) {
+        wc[wid * 128 + k] = 0u;
+        wl[wid * 128 + k] = 0u;
+        wh[wid * 128 + k] = 0u;
+      }
+      __syncwarp();
+      for (int base = 0; base < R; base += blockDim.x) {
+        const int j = base + threadIdx.x;
+        if (j < R) {
+#pragma unroll
+          for (int X = 0; X < 2; ++X) {
+            const float e = X ? eL(j) : eS(j);
+            const int b = wid * 128 + X * 64 + (int)min(__float_as_uint(e) >> 24, 63u);
+            const unsigned long long mq = mass_q(e);
+            atomicAdd(&wc[b], 1u);
+            const unsigned int vlo = (unsigned int)mq, vhi = (unsigned int)(mq >> 32);
+            const unsigned int old = atomicAdd(&wl[b], vlo);
+            const unsigned int up = vhi + ((old + vlo < old) ? 1u : 0u);
+            if (up) atomicAdd(&wh[b], up);
+          }
+        }
+      }
+      __syncthreads();
+      for (int k = threadIdx.x; k < 128; k += blockDim.x) {
+        unsigned int c = 0u;
+        unsigned long long m = 0ull;
+        for (int w2 = 0; w2 < nw; ++w2) {
+          c += wc[w2 * 128 + k];
+          m += ((unsigned long long)wh[w2 * 128 + k] << 32) | wl[w2 * 128 + k];
+        }
+        const int X = k >> 6, d = k & 63;
+        sh.cnt[X][d] = c;
+        sh.mlo[X][d] = (unsigned int)m;
+        sh.mhi[X][d] = (unsigned int)(m >> 32);
+      }
+      __syncthreads();
+    } else {
     // Most weights share their top digits, so lanes with the same digit are
     // combined inside the warp first and one lane per digit does the atomics.
     for (int base = 0; base < R; base += blockDim.x) {
@@ -476,6 +524,7 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
       hist_add(sh, 1, d1, m1);
     }
     __syncthreads();
+    }
     const int wid = threadIdx.x >> 5;
     if (wid < 2) {
       // descending digits: lane L owns digits 255-8L .. 248-8L and is the
@@ -635,7 +684,8 @@ __device__ unsigned long long kth_smallest(const KF& key_of, int C, int k, SelSh
 template <class ES, class EL, class PF>
 __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const gp_req_meta& m,
                             int R, ES eS, EL eL, unsigned long long TS, unsigned long long TL,
-                            PF posf, int C, int pos, int nfree, bool replan, SelShared& sh) {
+                            PF posf, int C, int pos, int nfree, bool replan, SelShared& sh,
+                            uint32_t* wbins_a = nullptr, uint32_t* wbins_b = nullptr) {
   // the importance scales 2^40 / T in fp32 (T >= 2^40: the largest e_j is 1),
   // once per item by one thread, published by the next barrier
   if (threadIdx.x == 0) {
@@ -644,7 +694,8 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
   }
   if (!replan) {
     // Top-p counts from the fixed-point total masses TS, TL
-    const int2 Wv = topp_radix2(eS, eL, R, ceil_mul(p.top_p, TS), ceil_mul(p.top_p, TL), sh);
+    const int2 Wv = topp_radix2(eS, eL, R, ceil_mul(p.top_p, TS), ceil_mul(p.top_p, TL), sh, wbins_a,
+                                wbins_b);
     if (threadIdx.x == 0) {
       p.wset[row * 2 + 0] = Wv.x;
       p.wset[row * 2 + 1] = Wv.y;
@@ -773,9 +824,14 @@ __global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDe
     if (staged)
       for (int s = threadIdx.x; s < C; s += blockDim.x) poss[s] = pg(s);
     block_sum2_ull(TS, TL, sh.red);
+    // rows of up to half the staging size leave the upper halves of the two
+    // e_j arrays free: the first Top-p pass keeps its per-warp bins there
+    const bool wide = staged && R <= kSelSmemTok / 2 && 2 * kSelThreads / 32 * 128 <= kSelSmemTok / 2;
     if (staged)
       select_item(p, i, slot, row, m, R, ESmem{eSs}, ESmem{eLs}, TS, TL, PosSmem{poss}, C, pos,
-                  nfree, replan != 0, sh);
+                  nfree, replan != 0, sh,
+                  wide ? reinterpret_cast<uint32_t*>(eSs + kSelSmemTok / 2) : nullptr,
+                  wide ? reinterpret_cast<uint32_t*>(eLs + kSelSmemTok / 2) : nullptr);
     else
       select_item(p, i, slot, row, m, R, EGlobal{uS, mx.x}, EGlobal{uL, mx.y}, TS, TL, pg, C, pos,
                   nfree, replan != 0, sh);
