@@ -55,12 +55,20 @@ constexpr int kMmaStageB = 8192;           // 16 tokens x (K 4 KiB + V 4 KiB)
 #ifndef GP_MMA_STAGES
 #define GP_MMA_STAGES 3
 #endif
+#ifndef GP_PREF_L2
+#define GP_PREF_L2 3  // blocks a warp prefetches into L2 before the dependency wait
+#endif
 constexpr int kMmaWarps = GP_MMA_WARPS;
 constexpr int kMmaStages = GP_MMA_STAGES;
 constexpr int kObFloats = 4 * (kMmaD + 2);  // per-warp merge buffer: [G<=4][D] + m + l
 // prep and combine run one warp per CTA: their CTAs are launched early (see
 // griddepcontrol) and must fit beside two resident attention CTAs.
 constexpr int kSmallWarps = 1;
+
+// An L2 prefetch of bytes (a multiple of 16) at a 16-byte aligned address.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 // One 16-token block (K and V, both 64-column halves) of a (page, layer,
 // head) in one copy: the block map's box (64, 16, 2, 2, 1) at token offset
@@ -953,6 +961,26 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvblk, PoolDev p, int layer,
     if (lane == 0) issue_meta_state<G>(p, layer, h_first, e.slot, e.pos, ring, &bars[0]);
   }
   while (inflight < S && emit(false)) {}
+  // The next GP_PREF_L2 blocks of the range into L2 (pages are final before
+  // the step): the blocks issued right after the wait then come from L2,
+  // fetched while the previous kernels finish.
+  {
+    Cursor c2 = pc;
+    PlanWin w2 = pwin;
+    PageWinAhead win2 = win;
+    int b2 = pblk;
+    for (int k = 0; k < GP_PREF_L2 && b2 < end; ++k) {
+      const int page = page_of_ahead(p, win2, w2, c2, n, lane);
+      if (lane == 0) {
+        const int t0 = c2.base + c2.blk * kBlockTok;
+        const int in_page = p.P_log2 >= 0 ? (t0 & (p.P - 1)) : t0 % p.P;
+        const size_t krow = ((((size_t)page * p.L + layer) * p.Hk + c2.h) * 2) * p.P + in_page;
+        prefetch_l2(p.kv + krow * (kMmaD * 2), kBlockTok * kMmaD * 2);
+        prefetch_l2(p.kv + (krow + p.P) * (kMmaD * 2), kBlockTok * kMmaD * 2);
+      }
+      if (++b2 < end) walk_next(p, w2, c2, n, lane);
+    }
+  }
   // The step's inputs, the split-K scratch and the outputs belong to earlier
   // kernels: wait for them.
   asm volatile("griddepcontrol.wait;" ::: "memory");
