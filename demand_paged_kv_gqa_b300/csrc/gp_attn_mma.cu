@@ -70,6 +70,15 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// The K and V rows of the cursor's block (page given) into L2.
+__device__ __forceinline__ void prefetch_block_l2(const PoolDev& p, int layer, const Cursor& c, int page) {
+  const int t0 = c.base + c.blk * kBlockTok;
+  const int in_page = p.P_log2 >= 0 ? (t0 & (p.P - 1)) : t0 % p.P;
+  const size_t krow = ((((size_t)page * p.L + layer) * p.Hk + c.h) * 2) * p.P + in_page;
+  prefetch_l2(p.kv + krow * (kMmaD * 2), kBlockTok * kMmaD * 2);
+  prefetch_l2(p.kv + (krow + p.P) * (kMmaD * 2), kBlockTok * kMmaD * 2);
+}
+
 // One 16-token block (K and V, both 64-column halves) of a (page, layer,
 // head) in one copy: the block map's box (64, 16, 2, 2, 1) at token offset
 // tok within the page and row index (page * L + layer) * Hk + head.
@@ -965,20 +974,13 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvblk, PoolDev p, int layer,
   // the step): the blocks issued right after the wait then come from L2,
   // fetched while the previous kernels finish.
   {
-    Cursor c2 = pc;
-    PlanWin w2 = pwin;
-    PageWinAhead win2 = win;
-    int b2 = pblk;
-    for (int k = 0; k < GP_PREF_L2 && b2 < end; ++k) {
-      const int page = page_of_ahead(p, win2, w2, c2, n, lane);
-      if (lane == 0) {
-        const int t0 = c2.base + c2.blk * kBlockTok;
-        const int in_page = p.P_log2 >= 0 ? (t0 & (p.P - 1)) : t0 % p.P;
-        const size_t krow = ((((size_t)page * p.L + layer) * p.Hk + c2.h) * 2) * p.P + in_page;
-        prefetch_l2(p.kv + krow * (kMmaD * 2), kBlockTok * kMmaD * 2);
-        prefetch_l2(p.kv + (krow + p.P) * (kMmaD * 2), kBlockTok * kMmaD * 2);
-      }
-      if (++b2 < end) walk_next(p, w2, c2, n, lane);
+    Cursor pa = pc;
+    PlanWin wa = pwin;
+    PageWinAhead wina = win;
+    for (int k = 0, b2 = pblk; k < GP_PREF_L2 && b2 < end; ++k) {
+      const int page = page_of_ahead(p, wina, wa, pa, n, lane);
+      if (lane == 0) prefetch_block_l2(p, layer, pa, page);
+      if (++b2 < end) walk_next(p, wa, pa, n, lane);
     }
   }
   // The step's inputs, the split-K scratch and the outputs belong to earlier
