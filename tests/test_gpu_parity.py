@@ -272,6 +272,22 @@ def test_select_rows_beyond_shared_memory(env):
     assert rep.max_out_err < 2e-2
 
 
+def test_select_rows_staged_without_first_pass_bins(env):
+    # Rows of 2049 .. 4096 tokens are staged in shared memory but leave no
+    # room for the first Top-p pass's per-warp bins: that pass takes the
+    # digit-group adds.  Two Llama-3-8B-shaped layers, 3 requests whose
+    # 3072-token prompts fill their 192-page budgets.
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(num_layers=2, prompt_min=3072, prompt_max=3072,
+                                                  budget_pages=192, max_pages_per_req=240,
+                                                  num_pages=900)
+    h = H.Harness(w, 3, budget_pages=192, max_seq_len=3072 + 120)
+    rep = h.run(70)
+    _check(rep)
+    assert rep.boundaries == 3 * 5
+    assert rep.compacts > 0
+
+
 def test_select_rows_beyond_shared_memory_with_prefix(env):
     # The 36-layer Qwen3-shaped workload's request shape on one layer: a
     # 2048-token shared prefix plus 2304 private tokens (R = 4352 > 4096,
