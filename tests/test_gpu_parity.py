@@ -139,6 +139,20 @@ def test_review_hyperparameters_page_256(env):
     assert rep.boundaries >= 12
 
 
+def test_page_size_not_a_power_of_two(env):
+    # 48-token pages: three 16-token blocks per page, block-table and
+    # in-page offsets by division rather than shifts, in the attention
+    # kernel, its block copies and the compaction moves
+    H, gp, synth = env
+    w = synth.WORKLOADS["llama8b_1layer"].replace(page_size=48, prompt_min=280, prompt_max=288,
+                                                  budget_pages=6, num_pages=200, max_pages_per_req=24)
+    h = H.Harness(w, 5, budget_pages=6)
+    rep = h.run(160)
+    _check(rep)
+    assert rep.boundaries >= 10
+    assert rep.compacts > 0
+
+
 def test_shrink_policy(env):
     # the SHRINK ablation: boundaries that do not grow release a page while
     # the kept set still holds the recent window, else compact in place;
