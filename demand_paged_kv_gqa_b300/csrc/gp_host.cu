@@ -30,9 +30,9 @@ cudaError_t ceiling_setup();
 int ceiling_warps_per_cta();
 cudaError_t launch_kv_read(const PoolDev& p, const CUtensorMap* map, int layer, int mode,
                            uint32_t* sink, int grid, cudaStream_t st);
-cudaError_t launch_select(const PoolDev& p, int grid, int replan, cudaStream_t st);
+cudaError_t launch_select(const PoolDev& p, int grid, int replan, bool big, cudaStream_t st);
 cudaError_t select_setup();
-cudaError_t select_occupancy(int* blocks);
+cudaError_t select_occupancy(int* blocks, bool big);
 cudaError_t launch_decide(const PoolDev& p, int part, cudaStream_t st);
 cudaError_t launch_commit(const PoolDev& p, int grid, int part, cudaStream_t st);
 cudaError_t launch_release_busy(const PoolDev& p, cudaStream_t st);
@@ -60,7 +60,7 @@ struct gp_pool {
   int next_layer = 0;
   int step_n = -1;
   const int32_t* step_slots = nullptr;
-  int attn_grid = 0, select_grid = 0, commit_grid = 0;
+  int attn_grid = 0, select_grid = 0, select_grid_big = 0, commit_grid = 0;
   int64_t launches = 0;
   std::vector<char> slot_active;
   std::vector<int> slot_prefix;
@@ -437,8 +437,10 @@ int gp_create_pool(const gp_config* cfg, void* dev_buf, size_t bytes, void* stre
   p->attn_grid = grid;
   p->dev.num_workers = grid * wpc;
   int sel_blocks = 0;
-  if (gp::select_occupancy(&sel_blocks) != cudaSuccess || sel_blocks < 1) return bail(GP_ERR_CUDA);
+  if (gp::select_occupancy(&sel_blocks, false) != cudaSuccess || sel_blocks < 1) return bail(GP_ERR_CUDA);
   p->select_grid = sms * sel_blocks;
+  if (gp::select_occupancy(&sel_blocks, true) != cudaSuccess || sel_blocks < 1) return bail(GP_ERR_CUDA);
+  p->select_grid_big = sms * sel_blocks;
   p->commit_grid = sms * 4;
   e = cudaStreamSynchronize(p->stream);
   if (e != cudaSuccess) return bail(GP_ERR_CUDA);
@@ -605,6 +607,13 @@ int gp_decode_step(gp_pool* pool, int32_t layer, int32_t n, const int32_t* slots
   return GP_OK;
 }
 
+// The select kernel's shape for a boundary call over n requests: at most
+// n * L * Hk items (those at a boundary); when that many fit one wave of the
+// 512-thread shape, per-item latency decides and it is taken.
+bool select_big(const gp_pool* pool, int n) {
+  return (int64_t)n * pool->cfg.num_layers * pool->cfg.num_kv_heads <= pool->select_grid_big;
+}
+
 int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev) {
   if (!pool) return GP_ERR_INVALID;
   if (pool->next_layer != pool->cfg.num_layers)
@@ -614,13 +623,15 @@ int gp_boundary(gp_pool* pool, int32_t n, const int32_t* slots_dev) {
   pool->next_layer = 0;
   if (n == 0) return GP_OK;
   GP_JOIN(pool);  // pages are popped below: after any earlier step's boundary work
+  const bool big = select_big(pool, n);
+  const int sgrid = big ? pool->select_grid_big : pool->select_grid;
   if (pool->cfg.mode != GP_MODE_FULL_KV)
-    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 0, pool->stream));
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, sgrid, 0, big, pool->stream));
   GP_LAUNCH(pool, gp::launch_decide(pool->dev, gp::kPartAll, pool->stream));
   // SHRINK: the requests that release a page drop 2P tokens, not P; their
   // plans are redone once the decisions are known
   if (pool->cfg.mode == GP_MODE_SHRINK)
-    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 1, pool->stream));
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, sgrid, 1, big, pool->stream));
   GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, gp::kPartAll, pool->stream));
   return GP_OK;
 }
@@ -648,11 +659,13 @@ int gp_boundary_async(gp_pool* pool, int32_t n, const int32_t* slots_dev, void* 
   if (e == cudaSuccess && pool->side_pending[b ^ 1]) e = cudaStreamWaitEvent(side, pool->side_ev[b ^ 1], 0);
   if (e != cudaSuccess) return cuda_fail(pool, e, "order the second stream");
   // the requests at a boundary, on the second stream
+  const bool big = select_big(pool, n);
+  const int sgrid = big ? pool->select_grid_big : pool->select_grid;
   if (pool->cfg.mode != GP_MODE_FULL_KV)
-    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 0, side));
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, sgrid, 0, big, side));
   GP_LAUNCH(pool, gp::launch_decide(pool->dev, gp::kPartBoundary, side));
   if (pool->cfg.mode == GP_MODE_SHRINK)
-    GP_LAUNCH(pool, gp::launch_select(pool->dev, pool->select_grid, 1, side));
+    GP_LAUNCH(pool, gp::launch_select(pool->dev, sgrid, 1, big, side));
   GP_LAUNCH(pool, gp::launch_commit(pool->dev, pool->commit_grid, gp::kPartBoundary, side));
   GP_LAUNCH(pool, gp::launch_release_busy(pool->dev, side));
   e = cudaEventRecord(pool->side_ev[b], side);

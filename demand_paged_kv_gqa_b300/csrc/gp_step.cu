@@ -772,7 +772,10 @@ __device__ void select_item(const PoolDev& p, int i, int slot, size_t row, const
 constexpr int kSelSmemTok = GP_SEL_TOK;
 constexpr size_t kSelSmemBytes = (size_t)kSelSmemTok * (4 + 4 + 4);
 
-__global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDev p, int replan) {
+// Two shapes of the same kernel: 256 threads, 4 CTAs per SM (many items:
+// throughput) and 512 threads, 2 CTAs per SM (few items: latency per item).
+template <int T, int MINB>
+__global__ void __launch_bounds__(T, MINB) select_kernel(PoolDev p, int replan) {
   // programmatic dependent of the kernel before it; lets the next one launch
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -826,7 +829,7 @@ __global__ void __launch_bounds__(kSelThreads, GP_SEL_MINB) select_kernel(PoolDe
     block_sum2_ull(TS, TL, sh.red);
     // rows of up to half the staging size leave the upper halves of the two
     // e_j arrays free: the first Top-p pass keeps its per-warp bins there
-    const bool wide = staged && R <= kSelSmemTok / 2 && 2 * kSelThreads / 32 * 128 <= kSelSmemTok / 2;
+    const bool wide = staged && R <= kSelSmemTok / 2 && 2 * T / 32 * 128 <= kSelSmemTok / 2;
     if (staged)
       select_item(p, i, slot, row, m, R, ESmem{eSs}, ESmem{eLs}, TS, TL, PosSmem{poss}, C, pos,
                   nfree, replan != 0, sh,
@@ -1250,16 +1253,25 @@ static cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, int block, size_
 cudaError_t launch_plan(const PoolDev& p, int n, const int32_t* slots, int count, cudaStream_t st) {
   return launch_pdl(plan_kernel, 1, 1024, 0, st, p, n, slots, count);
 }
+constexpr int kSelBigThreads = 512;
 cudaError_t select_setup() {
-  return cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kSelSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel<kSelThreads, GP_SEL_MINB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(select_kernel<kSelBigThreads, 2>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSelSmemBytes);
 }
-cudaError_t select_occupancy(int* blocks) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, select_kernel, kSelThreads,
-                                                       kSelSmemBytes);
+cudaError_t select_occupancy(int* blocks, bool big) {
+  return big ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, select_kernel<kSelBigThreads, 2>,
+                                                             kSelBigThreads, kSelSmemBytes)
+             : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, select_kernel<kSelThreads, GP_SEL_MINB>,
+                                                             kSelThreads, kSelSmemBytes);
 }
-cudaError_t launch_select(const PoolDev& p, int grid, int replan, cudaStream_t st) {
-  return launch_pdl(select_kernel, grid, kSelThreads, kSelSmemBytes, st, p, replan);
+cudaError_t launch_select(const PoolDev& p, int grid, int replan, bool big, cudaStream_t st) {
+  return big ? launch_pdl(select_kernel<kSelBigThreads, 2>, grid, kSelBigThreads, kSelSmemBytes, st, p,
+                          replan)
+             : launch_pdl(select_kernel<kSelThreads, GP_SEL_MINB>, grid, kSelThreads, kSelSmemBytes, st, p,
+                          replan);
 }
 cudaError_t launch_decide(const PoolDev& p, int part, cudaStream_t st) {
   return launch_pdl(decide_kernel, 1, 1024, 0, st, p, part);
