@@ -311,6 +311,16 @@ __device__ __forceinline__ void issue_meta_inputs(const PoolDev& p, int i, int h
   bulk_g2s(st + kMetaV, vnew + ((size_t)i * p.Hk + h) * D, D * 2, bar);
 }
 
+// The same rows as issue_meta_inputs, prefetched into L2 only.
+template <int G>
+__device__ __forceinline__ void prefetch_inputs_l2(const PoolDev& p, int i, int h, const __nv_bfloat16* q,
+                                                   const __nv_bfloat16* knew, const __nv_bfloat16* vnew) {
+  constexpr int D = kMmaD;
+  prefetch_l2(q + ((size_t)i * p.Hq + h * G) * D, G * D * 2);
+  prefetch_l2(knew + ((size_t)i * p.Hk + h) * D, D * 2);
+  prefetch_l2(vnew + ((size_t)i * p.Hk + h) * D, D * 2);
+}
+
 template <int G>
 __device__ __forceinline__ void issue_meta(const PoolDev& p, int layer, int i, int h, int slot,
                                            int pos, const __nv_bfloat16* q,
@@ -983,6 +993,10 @@ attn_mma_kernel(const __grid_constant__ CUtensorMap kvblk, PoolDev p, int layer,
       if (++b2 < end) walk_next(p, wa, pa, n, lane);
     }
   }
+  // The first piece's input rows into L2 as well.  They may still be being
+  // written by the kernel before this one; a prefetch only warms L2, which
+  // every writer updates, and nothing is read from them before the wait.
+  if (lane == 0) prefetch_inputs_l2<G>(p, i_first, h_first, q, knew, vnew);
   // The step's inputs, the split-K scratch and the outputs belong to earlier
   // kernels: wait for them.
   asm volatile("griddepcontrol.wait;" ::: "memory");
