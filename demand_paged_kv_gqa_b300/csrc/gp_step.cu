@@ -365,7 +365,7 @@ struct SelShared {
   unsigned int mlo[2][256], mhi[2][256];
   ulonglong2 red[33];
   float2 redf[33];
-  unsigned int pick_d[2];
+  unsigned int pick_d[2], pick_c[2];  // picked digit and how many elements it holds
   unsigned long long pick_a[2], pick_b[2];
   int done;
   int hcount[32];   // compaction holes per warp
@@ -416,7 +416,10 @@ struct PosSmem {
 // (mass of the k largest) >= thr, by a 4-pass radix select (8 bits per pass,
 // most significant first) on the fp32 bit patterns of e_j, weighting each by
 // its fixed-point mass.  The two selects share their passes: warp X scans
-// summary X's histogram.
+// summary X's histogram.  A summary whose picked digit holds one element is
+// settled there: that element is the last one the set needs (the mass still
+// needed is positive and at most its own), so k = (count above it) + 1, which
+// is what the remaining passes would give; it takes no part in them.
 __device__ __forceinline__ void bin_add(SelShared& sh, int X, int d, unsigned int c, unsigned long long v) {
   atomicAdd(&sh.cnt[X][d], c);
   const unsigned int vlo = (unsigned int)v, vhi = (unsigned int)(v >> 32);
@@ -453,6 +456,7 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
                             uint32_t* wbins_b = nullptr) {
   uint32_t prefix[2] = {0u, 0u}, pmask = 0u;
   unsigned long long mass_above[2] = {0ull, 0ull}, cnt_above[2] = {0ull, 0ull};
+  bool settled[2] = {false, false};  // block-uniform (from shared picks)
   for (int d = threadIdx.x; d < 512; d += blockDim.x) {
     (&sh.cnt[0][0])[d] = 0u;
     (&sh.mlo[0][0])[d] = 0u;
@@ -517,16 +521,16 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
       if (j < R) {
         const float e0 = eS(j), e1 = eL(j);
         const uint32_t b0 = __float_as_uint(e0), b1 = __float_as_uint(e1);
-        if ((b0 & pmask) == prefix[0]) { d0 = (b0 >> shift) & 255; m0 = mass_q(e0); }
-        if ((b1 & pmask) == prefix[1]) { d1 = (b1 >> shift) & 255; m1 = mass_q(e1); }
+        if (!settled[0] && (b0 & pmask) == prefix[0]) { d0 = (b0 >> shift) & 255; m0 = mass_q(e0); }
+        if (!settled[1] && (b1 & pmask) == prefix[1]) { d1 = (b1 >> shift) & 255; m1 = mass_q(e1); }
       }
-      hist_add(sh, 0, d0, m0);
-      hist_add(sh, 1, d1, m1);
+      if (!settled[0]) hist_add(sh, 0, d0, m0);
+      if (!settled[1]) hist_add(sh, 1, d1, m1);
     }
     __syncthreads();
     }
     const int wid = threadIdx.x >> 5;
-    if (wid < 2) {
+    if (wid < 2 && !settled[wid]) {
       // descending digits: lane L owns digits 255-8L .. 248-8L and is the
       // only lane that reads them, so it clears them for the next pass
       const int X = wid, lane = threadIdx.x & 31;
@@ -548,13 +552,16 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
       const unsigned long long need = X ? thr1 - mass_above[1] : thr0 - mass_above[0];
       const bool here = (mex < need) && (mex + mloc >= need);
       const unsigned int bal = __ballot_sync(0xffffffffu, here);
-      if (bal == 0u && lane == 0) { sh.pick_d[X] = 0u; sh.pick_a[X] = 0ull; sh.pick_b[X] = 0ull; }
+      if (bal == 0u && lane == 0) {
+        sh.pick_d[X] = 0u; sh.pick_c[X] = 0u; sh.pick_a[X] = 0ull; sh.pick_b[X] = 0ull;
+      }
       if (here && lane == __ffs(bal) - 1) {
         unsigned long long macc = mex, cacc = cex;
         for (int t = 0; t < 8; ++t) {
           const int d = 255 - 8 * lane - t;
           if (macc + mass_at(sh, X, d) >= need || t == 7) {
             sh.pick_d[X] = (unsigned)d;
+            sh.pick_c[X] = sh.cnt[X][d];
             sh.pick_a[X] = macc;
             sh.pick_b[X] = cacc;
             break;
@@ -574,15 +581,22 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
     // the picks are rewritten only after the next pass's histogram barrier
 #pragma unroll
     for (int X = 0; X < 2; ++X) {
+      if (settled[X]) continue;
       prefix[X] |= sh.pick_d[X] << shift;
       mass_above[X] += sh.pick_a[X];
       cnt_above[X] += sh.pick_b[X];
+      settled[X] = sh.pick_c[X] == 1u;
     }
     pmask |= 255u << shift;
+    if (settled[0] && settled[1]) break;
   }
   int W[2];
 #pragma unroll
   for (int X = 0; X < 2; ++X) {
+    if (settled[X]) {
+      W[X] = (int)(cnt_above[X] + 1ull);
+      continue;
+    }
     const unsigned long long thr = X ? thr1 : thr0;
     const unsigned long long qstar = mass_q(__uint_as_float(prefix[X]));
     const unsigned long long rest = thr > mass_above[X] ? thr - mass_above[X] : 0ull;
