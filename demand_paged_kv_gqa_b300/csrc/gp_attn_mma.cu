@@ -552,7 +552,12 @@ __device__ void segment_duties(const PoolDev& p, int layer, int i, int h, int sl
       obx[grp] = sa;
     }
   }
-  float* nxt = p.summary_next + srow * D;
+  // The folded summaries.  A request at a boundary has them read again,
+  // unfolded, by the other pieces of its (request, head) for their summary
+  // scores, so its fold goes to summary_next and commit_kernel makes it
+  // current.  No other piece uses the summaries of any other request (its
+  // meta items load them unused), so its fold is written in place.
+  float* nxt = ((flags & kPlanScore) ? p.summary_next : p.summary) + srow * D;
   reinterpret_cast<float4*>(nxt)[lane] = reinterpret_cast<const float4*>(in.sf)[lane];
   reinterpret_cast<float4*>(nxt + D)[lane] = reinterpret_cast<const float4*>(in.sf + D)[lane];
 }

@@ -76,8 +76,8 @@ struct PoolDev {
   float* partials;        // [num_workers][2][G][D + 2]
   int32_t* seg_count;     // [max_req][Hk]
   float* summary_next;    // [max_req][L][Hk][2][d] this step's folded summaries
-                          // (bf16 attention path), copied over `summary` by the
-                          // commit kernel once every layer has been read
+                          // of the requests at a boundary (bf16 attention path),
+                          // copied over `summary` by the commit kernel
   float* sstage;          // [max_req][Hk][4] each query head's score against the
                           // staged token (log2 domain)
   int32_t summary_via_next;  // 1: the attention kernel writes summary_next

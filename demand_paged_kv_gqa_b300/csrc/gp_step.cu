@@ -15,8 +15,9 @@
 //                   ascending slot order, released pages pushed after every
 //                   pop; metadata.
 //   commit_kernel   per (request, layer, kv head): the step's folded
-//                   summaries made current, compaction moves, then the
-//                   staged token written into its slot.
+//                   summaries of a request at a boundary made current (the
+//                   attention kernel writes the others in place), compaction
+//                   moves, then the staged token written into its slot.
 // For the asynchronous boundary path, decide and commit run twice: once on
 // the pool's stream for the requests not at a boundary, once on a second
 // stream for those at a boundary (which sit out the next step).
@@ -530,7 +531,7 @@ __device__ int2 topp_radix2(ES eS, EL eL, int R, unsigned long long thr0, unsign
     __syncthreads();
     }
     const int wid = threadIdx.x >> 5;
-    if (wid < 2 && !settled[wid]) {
+    if (wid < 2 && !(wid ? settled[1] : settled[0])) {  // (no indexing: registers)
       // descending digits: lane L owns digits 255-8L .. 248-8L and is the
       // only lane that reads them, so it clears them for the next pass
       const int X = wid, lane = threadIdx.x & 31;
@@ -1049,7 +1050,9 @@ __global__ void __launch_bounds__(256, 4) commit_kernel(PoolDev p, int part) {
     const int npre = p.req[slot].n_pre_pages;
     const int32_t* bt = p.block + (size_t)slot * p.block_width + npre;
     const size_t row = ((size_t)slot * p.L + layer) * p.Hk + h;
-    if (p.summary_via_next) {  // this step's folded summaries become current
+    if (p.summary_via_next && (p.plan_flags[i] & kPlanScore)) {
+      // the folded summaries of a request at a boundary become current (the
+      // attention kernel wrote every other request's in place)
       const float4* src = reinterpret_cast<const float4*>(p.summary_next + row * 2 * p.D);
       float4* dst = reinterpret_cast<float4*>(p.summary + row * 2 * p.D);
       for (int c = lane; c < 2 * p.D / 4; c += 32) dst[c] = src[c];
