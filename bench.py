@@ -22,6 +22,8 @@ each timed step.  Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import contextlib
+import gc
 import json
 import math
 import os
@@ -38,12 +40,12 @@ import torch  # noqa: E402
 
 # DRAM bytes (read + write) per attention launch over its algorithmic K/V
 # bytes, from one ncu capture of attn_mma_kernel on the same heads and
-# requests with 4 layers and a 1.5 GB pool (two launches: 1.032 and 1.030).
+# requests with 4 layers and a 1.5 GB pool (two launches: 1.033 and 1.031).
 # The bench's launches are too large to capture, so the traffic it reports
 # is this ratio times its own algorithmic bytes per launch.
-TRAFFIC_RATIO = 1.031
+TRAFFIC_RATIO = 1.032
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of attn_mma_kernel on a "
-                  "4-layer, 1.5 GB-pool case (ratio 1.031 to its algorithmic bytes), scaled to "
+                  "4-layer, 1.5 GB-pool case (ratio 1.032 to its algorithmic bytes), scaled to "
                   "this launch's algorithmic bytes")
 
 
@@ -221,6 +223,19 @@ def _load_peaks():
     return 6400.0, "fallback"
 
 
+@contextlib.contextmanager
+def no_gc():
+    """Python's garbage collector off inside a timed region (collected just
+    before): a collection pause while the host is issuing a step's launches
+    would leave the GPU idle inside that step's events."""
+    gc.collect()
+    gc.disable()
+    try:
+        yield
+    finally:
+        gc.enable()
+
+
 def time_window(eng, steps, w, sample_clocks=False, local=0, layer_events=True):
     """Time `steps` decode steps of an engine with CUDA events on its stream.
 
@@ -246,33 +261,34 @@ def time_window(eng, steps, w, sample_clocks=False, local=0, layer_events=True):
     # the whole window, input draws between steps included (compares the
     # synchronous and asynchronous boundary paths on equal terms)
     w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    w0.record(stream)
-    for _ in range(steps):
-        eng.prepare_inputs()
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    with no_gc():
+        w0.record(stream)
+        for _ in range(steps):
+            eng.prepare_inputs()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
 
-        def before():
-            e[0].record(stream)
+            def before():
+                e[0].record(stream)
 
-        def after_layer(l):
-            if l == 0:
-                e[1].record(stream)
-            if l == L - 1:
-                e[2].record(stream)
+            def after_layer(l):
+                if l == 0:
+                    e[1].record(stream)
+                if l == L - 1:
+                    e[2].record(stream)
 
-        def after():
-            e[3].record(stream)
+            def after():
+                e[3].record(stream)
 
-        n = eng.step(timed=True, before_step=before, after_step=after,
-                     after_layer=after_layer if layer_events else None)
-        if n:
-            req_steps += n
-            evs.append(e)
-            nbs.append(eng.last_boundaries)
-    if eng.side is not None:
-        stream.wait_stream(eng.side)
-    w1.record(stream)
-    torch.cuda.synchronize()
+            n = eng.step(timed=True, before_step=before, after_step=after,
+                         after_layer=after_layer if layer_events else None)
+            if n:
+                req_steps += n
+                evs.append(e)
+                nbs.append(eng.last_boundaries)
+        if eng.side is not None:
+            stream.wait_stream(eng.side)
+        w1.record(stream)
+        torch.cuda.synchronize()
     clocks = clk.stop() if clk else None
     st1 = eng.pool.stats()
     step_t = [e[0].elapsed_time(e[3]) for e in evs]
@@ -436,49 +452,50 @@ def run_ours(args, ws, rank, local):
         ms = 0.0
         toks = 0
         warm = 3  # untimed: the copy stream's and pinned buffers' first use
-        for it in range(k + warm):
-            eng.prepare_inputs()
-            hq_.copy_(eng.q); hk_.copy_(eng.k); hv_.copy_(eng.v)
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            in_ready = {c0: torch.cuda.Event() for c0, _ in chunks}
-            out_ready = {c1 - 1: torch.cuda.Event() for _, c1 in out_chunks}
+        with no_gc():
+            for it in range(k + warm):
+                eng.prepare_inputs()
+                hq_.copy_(eng.q); hk_.copy_(eng.k); hv_.copy_(eng.v)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                in_ready = {c0: torch.cuda.Event() for c0, _ in chunks}
+                out_ready = {c1 - 1: torch.cuda.Event() for _, c1 in out_chunks}
 
-            def before():
-                e0.record(stream)
-                copy.wait_event(e0)
-                with torch.cuda.stream(copy):
-                    for c0, c1 in chunks:
-                        eng.q[c0:c1].copy_(hq_[c0:c1], non_blocking=True)
-                        eng.k[c0:c1].copy_(hk_[c0:c1], non_blocking=True)
-                        eng.v[c0:c1].copy_(hv_[c0:c1], non_blocking=True)
-                        in_ready[c0].record(copy)
-
-            def before_layer(l):
-                if l in in_ready:
-                    stream.wait_event(in_ready[l])
-
-            def after_layer(l):
-                if l in out_ready:
-                    c0 = max(c for c, _ in out_chunks if c <= l)
-                    out_ready[l].record(stream)
-                    copy.wait_event(out_ready[l])
+                def before():
+                    e0.record(stream)
+                    copy.wait_event(e0)
                     with torch.cuda.stream(copy):
-                        ho_[c0:l + 1].copy_(eng.out[c0:l + 1], non_blocking=True)
+                        for c0, c1 in chunks:
+                            eng.q[c0:c1].copy_(hq_[c0:c1], non_blocking=True)
+                            eng.k[c0:c1].copy_(hk_[c0:c1], non_blocking=True)
+                            eng.v[c0:c1].copy_(hv_[c0:c1], non_blocking=True)
+                            in_ready[c0].record(copy)
 
-            def after():
-                done = torch.cuda.Event()
-                done.record(copy)
-                stream.wait_event(done)
-                e1.record(stream)
+                def before_layer(l):
+                    if l in in_ready:
+                        stream.wait_event(in_ready[l])
 
-            n = eng.step(before_step=before, after_step=after, before_layer=before_layer,
-                         after_layer=after_layer)
-            torch.cuda.synchronize()
-            if it >= warm:
-                ms += e0.elapsed_time(e1)
-                toks += n
+                def after_layer(l):
+                    if l in out_ready:
+                        c0 = max(c for c, _ in out_chunks if c <= l)
+                        out_ready[l].record(stream)
+                        copy.wait_event(out_ready[l])
+                        with torch.cuda.stream(copy):
+                            ho_[c0:l + 1].copy_(eng.out[c0:l + 1], non_blocking=True)
+
+                def after():
+                    done = torch.cuda.Event()
+                    done.record(copy)
+                    stream.wait_event(done)
+                    e1.record(stream)
+
+                n = eng.step(before_step=before, after_step=after, before_layer=before_layer,
+                             after_layer=after_layer)
+                torch.cuda.synchronize()
+                if it >= warm:
+                    ms += e0.elapsed_time(e1)
+                    toks += n
         h2d = hq_.nbytes + hk_.nbytes + hv_.nbytes
         d2h = ho_.nbytes
         return dict(value=toks / (ms * 1e-3), h2d=h2d, d2h=d2h)
