@@ -80,7 +80,8 @@ struct PoolDev {
                           // copied over `summary` by the commit kernel
   float* sstage;          // [max_req][Hk][4] each query head's score against the
                           // staged token (log2 domain)
-  int32_t summary_via_next;  // 1: the attention kernel writes summary_next
+  int32_t summary_via_next;  // 1: the attention kernel writes the folds of requests
+                             // at a boundary to summary_next (bf16 path)
   int32_t* wblk;          // [kMaxWorkersBound + 1] first block of each worker's share
                           // (bf16 path; the last entry is the total)
   int4* seginfo;          // [max_req][Hk] first and last worker of each (request,
