@@ -1,4 +1,4 @@
-"""The Top-p count's radix select, restated on the host, against its definition.
+"""The boundary selects' radix passes, restated on the host, against their definitions.
 
 The boundary select kernel counts each summary's Top-p working set ("GrowPage:
 On-Demand KV Budgeting for Efficient LLM Reasoning Serving", evolve.pub review,
@@ -13,7 +13,8 @@ This file restates those steps in exact integer arithmetic and checks, on rows
 chosen to settle at every pass, to tie at the threshold and to hold zeros, that
 (1) the select with settling gives the same W as the select that always runs
 all four passes, and (2) both equal the definition computed by sorting.  The
-GPU parity tests compare the kernel itself with the fp64 oracle.
+compaction select is restated the same way at the end of the file.  The GPU
+parity tests compare the kernels themselves with the fp64 oracle.
 """
 from fractions import Fraction
 from math import ceil
@@ -166,3 +167,71 @@ def test_single_weight_and_all_zero_rows():
         assert topp_radix(one, tp, settle=True)[0] == topp_by_sorting(one, tp) == 1
         assert topp_radix(zeros, tp, settle=True)[0] == 1
         assert topp_radix(zeros, tp, settle=False)[0] == 1
+
+
+# ---- the compaction select ------------------------------------------------
+#
+# The compaction plan drops the k lowest candidates by the 64-bit key
+# (importance bits << 32 | position), importance = max(p_S, p_L) of a private
+# token older than the recent window ("GrowPage: On-Demand KV Budgeting for
+# Efficient LLM Reasoning Serving", evolve.pub review, section "Summary":
+# compaction ranks history by the maximum of both importance scores).  The
+# kernel finds a threshold key with exactly k candidates at or below it by an
+# 8-bit radix select from the top byte, and stops as soon as the digit it
+# picks is taken whole (the threshold is then that prefix with all lower bits
+# set).  Keys are distinct: they end with the token position.
+
+
+def kth_smallest_radix(keys, k):
+    """The kernel's select over candidate keys (Python ints < 2^64)."""
+    prefix, pmask, below = 0, 0, 0
+    for p in range(8):
+        shift = 56 - 8 * p
+        cnt = [0] * 256
+        for x in keys:
+            if x & pmask == prefix:
+                cnt[(x >> shift) & 255] += 1
+        acc, pick = below, None
+        for d in range(256):
+            if acc + cnt[d] >= k:
+                pick = d
+                break
+            acc += cnt[d]
+        if pick is None:            # fewer than k candidates: the scan ends on 255
+            pick, acc = 255, acc - cnt[255]
+        prefix |= pick << shift
+        pmask |= 255 << shift
+        below = acc
+        if acc + cnt[pick] == k:    # the picked digit is taken whole
+            return prefix | ((1 << shift) - 1)
+    return prefix
+
+
+def _compaction_keys(rng, n, ties):
+    imp = rng.random(n).astype(np.float32)
+    if ties:                        # few distinct importances: ties broken by position
+        imp = rng.choice(imp[:4], n)
+    bits = imp.view(np.uint32).astype(np.uint64)
+    pos = rng.permutation(1 << 20)[:n].astype(np.uint64)
+    return [int(b) << 32 | int(q) for b, q in zip(bits, pos)]
+
+
+@pytest.mark.parametrize("n,k,ties", [(16, 16, False), (40, 16, False), (1000, 16, False),
+                                      (1000, 16, True), (3000, 32, True), (17, 1, False),
+                                      (256, 255, True)])
+def test_compaction_select_takes_exactly_the_k_lowest(n, k, ties):
+    rng = np.random.default_rng(n * 7 + k + ties)
+    keys = _compaction_keys(rng, n, ties)
+    thr = kth_smallest_radix(keys, k)
+    chosen = sorted(x for x in keys if x <= thr)
+    assert chosen == sorted(keys)[:k]
+
+
+def test_compaction_select_stops_early_on_a_whole_digit():
+    # the k lowest keys share a top byte that no other key has: the select
+    # stops after the first pass with every lower bit of the threshold set
+    low = [(0x10 << 56) | i for i in range(16)]
+    high = [(0x20 << 56) | i for i in range(100)]
+    thr = kth_smallest_radix(low + high, 16)
+    assert thr == (0x10 << 56) | ((1 << 56) - 1)
+    assert sorted(x for x in low + high if x <= thr) == low
