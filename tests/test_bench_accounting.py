@@ -38,3 +38,19 @@ def test_reference_arm_line_on_cpu():
     for k in ("metric", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
               "scaling", "dtype", "config"):
         assert k in line
+
+
+def test_timed_regions_run_without_garbage_collection():
+    # the collector is off inside a timed region and back on after it, also
+    # when the region raises
+    import gc
+    assert gc.isenabled()
+    with bench.no_gc():
+        assert not gc.isenabled()
+    assert gc.isenabled()
+    try:
+        with bench.no_gc():
+            raise ValueError("inside a timed region")
+    except ValueError:
+        pass
+    assert gc.isenabled()
